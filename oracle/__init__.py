@@ -1,0 +1,138 @@
+"""fp64 CPU oracle of the Kimi Delta Attention recurrence.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The CUDA product path
+never imports this package, and this package imports nothing from it.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C, one token at a time, fp64),
+which follows the state-update, delta-form and readout equations of
+"Understanding Kimi K3's Attention" and the recurrent walk-through in
+"Hybrid Attention", section "KDA: don't write the same information twice".
+This module only compiles it with gcc and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "libkda_oracle.so")
+_lib = None
+
+G_MIN = -5.0
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no -march flags: the same code builds on
+    x86_64 and aarch64 and gives the same results)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "kda_oracle.h")))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Oracle:
+    """Bindings to one compiled copy of the oracle (the default build, or a
+    copy compiled elsewhere, e.g. by a test that plants a mistake in a
+    scratch copy of the source to show that the pins catch it)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        i32 = ctypes.c_int32
+        lib.kda_oracle_prefill.argtypes = [i32, i32, i32, i32, i32, dp, dp, dp, dp, dp,
+                                           dp, ip, dp, dp, i32]
+        lib.kda_oracle_prefill.restype = ctypes.c_int
+        lib.kda_oracle_decode.argtypes = [i32, i32, i32, i32, dp, dp, dp, dp, dp, dp, dp, i32]
+        lib.kda_oracle_decode.restype = ctypes.c_int
+        lib.kda_oracle_num_cpus.restype = ctypes.c_int
+        self.lib = lib
+
+    def num_cpus(self) -> int:
+        return int(self.lib.kda_oracle_num_cpus())
+
+    def prefill(self, q, k, v, g, beta, init_state=None, cu_seqlens=None, num_seqs=None,
+                num_threads: int = 0):
+        """Token-by-token KDA over a packed batch, in fp64.
+
+        q, k, g: [T, H, d_k]; v: [T, H, d_v]; beta: [T, H]; init_state:
+        [N, H, d_k, d_v] or None (zeros); cu_seqlens: int [N+1] or None (then
+        ``num_seqs`` equal-length sequences, default 1).
+        Returns (out [T, H, d_v], final_state [N, H, d_k, d_v]), both fp64.
+        """
+        q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+        T, H, dk = q.shape
+        dv = v.shape[2]
+        if cu_seqlens is not None:
+            cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+            N = cu.shape[0] - 1
+        else:
+            cu = None
+            N = 1 if num_seqs is None else int(num_seqs)
+        init = _f64(init_state)
+        out = np.zeros((T, H, dv), np.float64)
+        fin = np.zeros((N, H, dk, dv), np.float64)
+        rc = self.lib.kda_oracle_prefill(N, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                         _ptr(beta), _ptr(init), _ptr(cu, ctypes.c_int32),
+                                         _ptr(out), _ptr(fin), int(num_threads))
+        if rc != 0:
+            raise ValueError("kda_oracle_prefill rejected its arguments (shapes, "
+                             "cu_seqlens, or gates outside g in [-5,0], beta in [0,1])")
+        return out, fin
+
+    def decode(self, q, k, v, g, beta, state, num_threads: int = 0):
+        """One decode step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
+        beta [N, H]; state [N, H, d_k, d_v].  Returns (out, new_state), fp64;
+        the input ``state`` is not modified."""
+        q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+        st = np.array(state, dtype=np.float64, copy=True, order="C")
+        N, H, dk = q.shape
+        dv = v.shape[2]
+        out = np.zeros((N, H, dv), np.float64)
+        rc = self.lib.kda_oracle_decode(N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(st), _ptr(out), int(num_threads))
+        if rc != 0:
+            raise ValueError("kda_oracle_decode rejected its arguments")
+        return out, st
+
+
+def _load() -> Oracle:
+    global _lib
+    if _lib is None:
+        _lib = Oracle(build())
+    return _lib
+
+
+def num_cpus() -> int:
+    return _load().num_cpus()
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def prefill(*args, **kwargs):
+    """Module-level form of :meth:`Oracle.prefill` on the default build."""
+    return _load().prefill(*args, **kwargs)
+
+
+def decode(*args, **kwargs):
+    """Module-level form of :meth:`Oracle.decode` on the default build."""
+    return _load().decode(*args, **kwargs)

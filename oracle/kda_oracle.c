@@ -1,0 +1,202 @@
+/*
+ * kda_oracle.c -- plain fp64 CPU oracle for the Kimi Delta Attention (KDA)
+ * recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this library.  The CUDA product
+ * path never calls it and shares no code, header or table with it.
+ *
+ * What it computes, per sequence n and head h, token by token, in fp64:
+ *
+ *   alpha_t = exp(g_t)                        (per key channel)
+ *   M       = Diag(alpha_t) S_{t-1}           decay the rows (key channels)
+ *   p       = M^T k_t                         what the memory returns for k_t
+ *   u       = beta_t (v_t - p)                the correction
+ *   S_t     = M + k_t u^T                     write
+ *   o_t     = S_t^T q_t                       read, after the write
+ *
+ * Sources (the pages describe one recurrence in several equivalent forms):
+ *  - "Understanding Kimi K3's Attention" (dhruvpendharkar.github.io): the
+ *    state-update equation S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1}
+ *    + beta_t k_t v_t^T, the readout equation o_t = S_t^T q_t, and the
+ *    rewritten "delta" form S_t = Diag(alpha_t)S_{t-1} + beta_t k_t (v_t -
+ *    (Diag(alpha_t)S_{t-1})^T k_t)^T that this loop follows.  The symbol
+ *    table gives alpha_t = exp(g_t) per channel and beta_t in (0,1); the
+ *    log-decay bound equation gives g_t in (g_min, 0) with g_min = -5.
+ *  - "Hybrid Attention" (kimi-k3.adriaflores.com), section "KDA: don't
+ *    write the same information twice": retain (S = alpha*S, alpha
+ *    broadcast over the value axis, i.e. it scales key channels), predict
+ *    v_old = S^T k, correct by beta*(v - v_old), and the query reads the
+ *    updated S.
+ *  - "Kimi K3 course, lesson 2: KDA: the memory matrix": the read uses S at
+ *    time t, not t-1.
+ *
+ * Layouts (row-major, contiguous, fp64):
+ *   q, k  [T_tot, H, d_k];  v, out [T_tot, H, d_v];  g [T_tot, H, d_k];
+ *   beta  [T_tot, H];       states [N, H, d_k, d_v] (row i = key channel i).
+ *   cu_seqlens int32 [N+1]: sequence n covers tokens [cu[n], cu[n+1]).
+ *
+ * Domain: g must lie in [-5, 0] and beta in [0, 1] (the pages' open
+ * intervals, closed so that the special cases beta = 0, beta = 1 and
+ * alpha = 1 are inside).  Out-of-domain input returns -1 before any work.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#include "kda_oracle.h"
+
+#define KDA_ORACLE_G_MIN (-5.0)
+
+typedef struct {
+    int64_t h_count, dk, dv;
+    const double *q, *k, *v, *g, *beta, *init_state;
+    const int32_t *cu;
+    double *out, *final_state;
+    int64_t n_items;
+    int64_t next; /* work counter, guarded by lock */
+    pthread_mutex_t lock;
+} oracle_job;
+
+/* One (sequence, head) pair: the token loop written out. */
+static void run_one(const oracle_job *J, int64_t n, int64_t h, double *S,
+                    double *alpha, double *p, double *u) {
+    const int64_t H = J->h_count, dk = J->dk, dv = J->dv;
+    if (J->init_state)
+        memcpy(S, J->init_state + (n * H + h) * dk * dv, sizeof(double) * dk * dv);
+    else
+        memset(S, 0, sizeof(double) * dk * dv);
+
+    for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
+        const double *qt = J->q + (t * H + h) * dk;
+        const double *kt = J->k + (t * H + h) * dk;
+        const double *vt = J->v + (t * H + h) * dv;
+        const double *gt = J->g + (t * H + h) * dk;
+        const double bt = J->beta[t * H + h];
+        double *ot = J->out + (t * H + h) * dv;
+
+        for (int64_t i = 0; i < dk; ++i) alpha[i] = exp(gt[i]);
+        /* M = Diag(alpha) S */
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] *= alpha[i];
+        /* p = M^T k */
+        for (int64_t j = 0; j < dv; ++j) p[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) p[j] += S[i * dv + j] * kt[i];
+        /* u = beta (v - p) */
+        for (int64_t j = 0; j < dv; ++j) u[j] = bt * (vt[j] - p[j]);
+        /* S = M + k u^T */
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S[i * dv + j] += kt[i] * u[j];
+        /* o = S^T q */
+        for (int64_t j = 0; j < dv; ++j) ot[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) ot[j] += S[i * dv + j] * qt[i];
+    }
+    if (J->final_state)
+        memcpy(J->final_state + (n * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+}
+
+static void *worker(void *arg) {
+    oracle_job *J = (oracle_job *)arg;
+    const int64_t dk = J->dk, dv = J->dv;
+    double *S = (double *)malloc(sizeof(double) * dk * dv);
+    double *alpha = (double *)malloc(sizeof(double) * dk);
+    double *p = (double *)malloc(sizeof(double) * dv);
+    double *u = (double *)malloc(sizeof(double) * dv);
+    if (!S || !alpha || !p || !u) {
+        free(S); free(alpha); free(p); free(u);
+        return (void *)1;
+    }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t item = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (item >= J->n_items) break;
+        run_one(J, item / J->h_count, item % J->h_count, S, alpha, p, u);
+    }
+    free(S); free(alpha); free(p); free(u);
+    return NULL;
+}
+
+int kda_oracle_num_cpus(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                       int32_t d_k, int32_t d_v, const double *q, const double *k,
+                       const double *v, const double *g, const double *beta,
+                       const double *init_state, const int32_t *cu_seqlens,
+                       double *out, double *final_state, int32_t num_threads) {
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || d_k <= 0 || d_v <= 0)
+        return -1;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return -1;
+
+    int32_t *cu_local = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        if (num_seqs == 0 ? total_tokens != 0 : total_tokens % num_seqs != 0) return -1;
+        cu_local = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs + 1));
+        if (!cu_local) return -1;
+        int32_t len = num_seqs ? total_tokens / num_seqs : 0;
+        for (int32_t n = 0; n <= num_seqs; ++n) cu_local[n] = n * len;
+        cu = cu_local;
+    }
+    int rc = 0;
+    if (cu[0] != 0 || cu[num_seqs] != total_tokens) rc = -1;
+    for (int32_t n = 0; n < num_seqs && rc == 0; ++n)
+        if (cu[n + 1] < cu[n]) rc = -1;
+    /* domain of the gates */
+    const int64_t nk = (int64_t)total_tokens * num_heads * d_k;
+    for (int64_t i = 0; i < nk && rc == 0; ++i)
+        if (!(g[i] >= KDA_ORACLE_G_MIN && g[i] <= 0.0)) rc = -1;
+    for (int64_t i = 0; i < (int64_t)total_tokens * num_heads && rc == 0; ++i)
+        if (!(beta[i] >= 0.0 && beta[i] <= 1.0)) rc = -1;
+    if (rc != 0) {
+        free(cu_local);
+        return rc;
+    }
+
+    oracle_job J;
+    J.h_count = num_heads; J.dk = d_k; J.dv = d_v;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta; J.init_state = init_state;
+    J.cu = cu; J.out = out; J.final_state = final_state;
+    J.n_items = (int64_t)num_seqs * num_heads;
+    J.next = 0;
+    pthread_mutex_init(&J.lock, NULL);
+
+    int nt = num_threads > 0 ? num_threads : kda_oracle_num_cpus();
+    if (nt > J.n_items) nt = (int)(J.n_items > 0 ? J.n_items : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    int started = 0;
+    if (th) {
+        for (int i = 1; i < nt; ++i)
+            if (pthread_create(&th[i], NULL, worker, &J) == 0) ++started;
+            else break;
+    }
+    if (worker(&J) != NULL) rc = -1;
+    for (int i = 1; i <= started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -1;
+    }
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    free(cu_local);
+    return rc;
+}
+
+int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
+                      const double *q, const double *k, const double *v,
+                      const double *g, const double *beta, double *state_inout,
+                      double *out, int32_t num_threads) {
+    /* One token per sequence: the same loop body applied once to each state.
+     * The states are read before they are written inside run_one (the copy
+     * into the per-thread buffer happens first), so in-place use is safe. */
+    return kda_oracle_prefill(num_seqs, num_seqs, num_heads, d_k, d_v, q, k, v, g,
+                              beta, state_inout, NULL, out, state_inout, num_threads);
+}

@@ -1,0 +1,39 @@
+/*
+ * kda_oracle.h -- fp64 CPU oracle of the KDA recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the CUDA product path.
+ *
+ * All arrays are fp64 (bf16 or fp32 inputs are widened exactly by the
+ * caller); layouts as in kda_oracle.c.  Returns 0 on success, -1 on a bad
+ * argument or an input outside the gates' domain (g in [-5, 0], beta in
+ * [0, 1]).  num_threads <= 0 uses every online CPU.
+ */
+#ifndef KDA_ORACLE_H
+#define KDA_ORACLE_H
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int kda_oracle_num_cpus(void);
+
+/* Token-by-token recurrence over a packed batch.  init_state may be NULL
+ * (zeros); cu_seqlens may be NULL (num_seqs equal-length sequences);
+ * final_state may be NULL (not written). */
+int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                       int32_t d_k, int32_t d_v, const double *q, const double *k,
+                       const double *v, const double *g, const double *beta,
+                       const double *init_state, const int32_t *cu_seqlens,
+                       double *out, double *final_state, int32_t num_threads);
+
+/* One decode step: one token per sequence, state updated in place. */
+int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
+                      const double *q, const double *k, const double *v,
+                      const double *g, const double *beta, double *state_inout,
+                      double *out, int32_t num_threads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,324 @@
+"""Pins of the fp64 oracle to facts the pages and the mathematics fix.
+
+Each pin is written so that a plausible mistake in the oracle (a dropped term,
+a wrong sign, the decay on the wrong axis, the read before the write, the
+wrong operand) fails at least one of them; ``test_planted_mistakes_are_caught``
+plants such mistakes in scratch copies of the oracle source and checks that.
+
+Sources:
+- "Understanding Kimi K3's Attention": state-update equation (factored form),
+  delta form, regression loss and its gradient step, readout equation.
+- "Hybrid Attention", section "KDA: don't write the same information twice":
+  the worked example (predict 2, target 6, beta 0.5 -> 4).
+- "Kimi K3.1 and the Road From Softmax Attention to Kimi Delta Attention",
+  section "3. The delta rule": beta = 1 with a unit key reads back v exactly;
+  the toy memory experiment and its printed errors.
+"""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+def _unit(x, axis=-1):
+    return x / np.linalg.norm(x, axis=axis, keepdims=True)
+
+
+def _rand_case(rng, T, H, dk, dv, unit_keys=True):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_keys:
+        q, k = _unit(q), _unit(k)
+    v = rng.standard_normal((T, H, dv))
+    g = np.maximum(-5.0, -np.logaddexp(0.0, -(rng.standard_normal((T, H, dk)) + 1.0)))
+    beta = rng.uniform(0.0, 1.0, (T, H))
+    return q, k, v, g, beta
+
+
+# ----------------------------------------------------------------------------
+# the pins, each a plain function of an oracle object (so that the planted-
+# mistake test can run them against a mutated build)
+# ----------------------------------------------------------------------------
+
+def pin_worked_example(orc, gold):
+    """Hybrid Attention, worked example: prediction 2, target 6, beta 0.5 -> 4
+    along a normalised key; untouched key directions keep their content."""
+    dk, dv = 4, 3
+    key = np.zeros(dk); key[2] = 1.0                       # unit key e_2
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    S0[0, 0, 2, :] = gold["prediction"]                    # S0^T k = prediction
+    v = np.full((1, 1, dv), gold["target"])
+    g = np.full((1, 1, dk), gold["g"])
+    beta = np.full((1, 1), gold["beta"])
+    out, fin = orc.prefill(key[None, None], key[None, None], v, g, beta, init_state=S0)
+    assert np.allclose(fin[0, 0].T @ key, gold["expected_after_write"], atol=1e-15, rtol=0)
+    assert np.allclose(out[0, 0], gold["expected_after_write"], atol=1e-15, rtol=0)
+    other = [i for i in range(dk) if i != 2]
+    assert np.array_equal(fin[0, 0][other], S0[0, 0][other])
+
+
+def pin_beta_one_reads_back_v(orc):
+    """The delta rule, beta = 1, unit key: reading k after the write returns v
+    exactly.  With q = k the readout after the write is therefore v_t for any
+    decay and any prior state."""
+    T, H, dk, dv = 12, 2, 5, 3
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    beta[:] = 1.0
+    S0 = RNG.standard_normal((1, H, dk, dv))
+    out, _ = orc.prefill(k, k, v, g, beta, init_state=S0)
+    assert np.max(np.abs(out - v)) < 1e-12
+
+
+def pin_beta_zero_closed_form(orc):
+    """beta = 0 writes nothing: S_t = Diag(exp(Gamma_t)) S_0 with Gamma_t the
+    running sum of g, and o_t = S_t^T q_t."""
+    T, H, dk, dv = 9, 2, 4, 6
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    beta[:] = 0.0
+    S0 = RNG.standard_normal((1, H, dk, dv))
+    out, fin = orc.prefill(q, k, v, g, beta, init_state=S0)
+    Gam = np.cumsum(g, axis=0)                            # [T, H, dk]
+    for h in range(H):
+        for t in range(T):
+            St = np.exp(Gam[t, h])[:, None] * S0[0, h]
+            assert np.allclose(out[t, h], St.T @ q[t, h], atol=1e-13, rtol=1e-13)
+        assert np.allclose(fin[0, h], np.exp(Gam[-1, h])[:, None] * S0[0, h],
+                           atol=1e-13, rtol=1e-13)
+
+
+def pin_toy_memory(orc, gold):
+    """The toy experiment with alpha = 1 (g = 0), beta = 1: regenerate the
+    stream with the same generator and draw order, check it with a plain
+    linear-attention sum (independent of the oracle), then feed it through
+    the oracle and compare its errors with the printed ones."""
+    d, n = int(gold["d"]), int(gold["pairs"])
+    rng = np.random.default_rng(int(gold["seed"]))
+    keys = np.stack([_unit(rng.standard_normal(d)) for _ in range(n)])
+    vals = np.stack([rng.standard_normal(d) for _ in range(n)])
+    new0 = rng.standard_normal(d)
+    ks = np.concatenate([keys, keys[:1]])                 # 20 writes, then key 0 again
+    vs = np.concatenate([vals, new0[None]])
+
+    def rel(S, key, target):
+        return np.linalg.norm(S.T @ key - target) / np.linalg.norm(target)
+
+    lin = sum(np.outer(a, b) for a, b in zip(ks, vs))
+    assert round(rel(lin, keys[0], new0), 2) == gold["linear_attention_key0"]
+    assert round(rel(lin, keys[5], vals[5]), 2) == gold["linear_attention_key5"]
+
+    T = ks.shape[0]
+    _, fin = orc.prefill(ks[:, None], ks[:, None], vs[:, None], np.zeros((T, 1, d)),
+                         np.ones((T, 1)))
+    S = fin[0, 0]
+    assert round(rel(S, keys[0], new0), 2) == gold["delta_rule_key0"]
+    assert round(rel(S, keys[5], vals[5]), 2) == gold["delta_rule_key5"]
+
+
+def _brute(q, k, v, g, beta, S0):
+    """Unrolled products of the factored state-update equation with explicit
+    d_k x d_k transition matrices A_s = (I - beta_s k_s k_s^T) Diag(exp g_s):
+    S_t = A_t...A_1 S_0 + sum_s A_t...A_{s+1} beta_s k_s v_s^T; o_t = S_t^T q_t."""
+    T, dk = k.shape
+    A = [(np.eye(dk) - beta[s] * np.outer(k[s], k[s])) @ np.diag(np.exp(g[s])) for s in range(T)]
+    outs = []
+    for t in range(T):
+        P = np.eye(dk)
+        S = np.zeros_like(S0)
+        for s in range(t, -1, -1):
+            S = S + P @ (beta[s] * np.outer(k[s], v[s]))
+            P = P @ A[s]
+        S = S + P @ S0
+        outs.append(S.T @ q[t])
+    return np.stack(outs), S
+
+
+def pin_brute_force(orc):
+    """Whole recurrence against brute-force unrolled products (tiny sizes,
+    d_k != d_v so that a transposed operand cannot pass, keys not normalised
+    so that no unit-norm shortcut hides a mistake)."""
+    for (T, dk, dv) in [(1, 3, 2), (5, 3, 4), (8, 4, 4), (7, 2, 5)]:
+        H = 2
+        q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv, unit_keys=False)
+        S0 = RNG.standard_normal((1, H, dk, dv))
+        out, fin = orc.prefill(q, k, v, g, beta, init_state=S0)
+        for h in range(H):
+            o_ref, S_ref = _brute(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], S0[0, h])
+            assert np.max(np.abs(out[:, h] - o_ref)) < 1e-12
+            assert np.max(np.abs(fin[0, h] - S_ref)) < 1e-12
+
+
+def pin_gradient_step(orc):
+    """One token equals one gradient-descent step of size beta on
+    L(S) = 1/2 ||S^T k - v||^2 taken from the decayed state Diag(alpha) S_0.
+    The gradient is taken by central finite differences (exact for a
+    quadratic up to rounding), not from its closed form."""
+    dk, dv = 4, 3
+    q, k, v, g, beta = _rand_case(RNG, 1, 1, dk, dv, unit_keys=False)
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    M = np.exp(g[0, 0])[:, None] * S0[0, 0]
+
+    def loss(S):
+        r = S.T @ k[0, 0] - v[0, 0]
+        return 0.5 * r @ r
+
+    h = 1e-3
+    grad = np.zeros_like(M)
+    for i in range(dk):
+        for j in range(dv):
+            E = np.zeros_like(M); E[i, j] = h
+            grad[i, j] = (loss(M + E) - loss(M - E)) / (2 * h)
+    _, fin = orc.prefill(q, k, v, g, beta, init_state=S0)
+    assert np.max(np.abs(fin[0, 0] - (M - beta[0, 0] * grad))) < 1e-9
+
+
+def pin_norm_bound(orc):
+    """For unit keys and beta in [0,1], (I - beta k k^T) has spectral norm <= 1
+    and alpha <= 1, so ||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||."""
+    T, H, dk, dv = 40, 1, 8, 8
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    S = RNG.standard_normal((1, H, dk, dv))
+    for t in range(T):
+        _, S_next = orc.prefill(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1],
+                                beta[t:t + 1], init_state=S)
+        lhs = np.linalg.norm(S_next[0, 0], 2)
+        rhs = np.linalg.norm(S[0, 0], 2) + beta[t, 0] * np.linalg.norm(v[t, 0])
+        assert lhs <= rhs * (1 + 1e-12)
+        S = S_next
+
+
+PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
+        pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound]
+
+
+def _run_pin(pin, orc, golden):
+    if pin is pin_worked_example:
+        pin(orc, golden("worked_delta_example.txt"))
+    elif pin is pin_toy_memory:
+        pin(orc, golden("toy_delta_memory.txt"))
+    else:
+        pin(orc)
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin, golden):
+    _run_pin(pin, oracle._load(), golden)
+
+
+# ----------------------------------------------------------------------------
+# host logic of the oracle (packing, empty sequences, domain, decode)
+# ----------------------------------------------------------------------------
+
+def test_packed_equals_separate():
+    lens = [5, 0, 11, 1, 7]
+    H, dk, dv = 2, 4, 3
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q, k, v, g, beta = _rand_case(RNG, int(cu[-1]), H, dk, dv)
+    S0 = RNG.standard_normal((len(lens), H, dk, dv))
+    out, fin = oracle.prefill(q, k, v, g, beta, init_state=S0, cu_seqlens=cu)
+    for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        o1, f1 = oracle.prefill(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b],
+                                init_state=S0[n:n + 1])
+        assert np.array_equal(out[a:b], o1)
+        assert np.array_equal(fin[n], f1[0])
+    assert np.array_equal(fin[1], S0[1])       # zero-length: final = initial
+
+
+def test_split_resume():
+    """final_state of a prefix is the initial state of the rest."""
+    T, H, dk, dv = 23, 2, 4, 5
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    out, fin = oracle.prefill(q, k, v, g, beta)
+    o1, f1 = oracle.prefill(q[:9], k[:9], v[:9], g[:9], beta[:9])
+    o2, f2 = oracle.prefill(q[9:], k[9:], v[9:], g[9:], beta[9:], init_state=f1)
+    assert np.array_equal(np.concatenate([o1, o2]), out)
+    assert np.array_equal(f2, fin)
+
+
+def test_decode_is_one_token():
+    N, H, dk, dv = 3, 2, 4, 4
+    q, k, v, g, beta = _rand_case(RNG, N, H, dk, dv)
+    S0 = RNG.standard_normal((N, H, dk, dv))
+    o_dec, s_dec = oracle.decode(q, k, v, g, beta, S0)
+    for n in range(N):
+        o1, f1 = oracle.prefill(q[n:n + 1], k[n:n + 1], v[n:n + 1], g[n:n + 1],
+                                beta[n:n + 1], init_state=S0[n:n + 1])
+        assert np.array_equal(o_dec[n], o1[0])
+        assert np.array_equal(s_dec[n], f1[0])
+
+
+def test_equal_length_default_layout():
+    T, N, H, dk, dv = 12, 3, 1, 3, 3
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    cu = np.arange(0, T + 1, T // N, dtype=np.int32)
+    a = oracle.prefill(q, k, v, g, beta, cu_seqlens=cu)
+    b = oracle.prefill(q, k, v, g, beta, num_seqs=N)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("bad", ["g_low", "g_pos", "beta_high", "cu_bad"])
+def test_domain_rejected(bad):
+    T, H, dk, dv = 4, 1, 2, 2
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    cu = None
+    if bad == "g_low":
+        g[1, 0, 0] = -5.5
+    elif bad == "g_pos":
+        g[2, 0, 1] = 0.1
+    elif bad == "beta_high":
+        beta[0, 0] = 1.5
+    else:
+        cu = np.array([0, 3, 2, 4], np.int32)
+    with pytest.raises(ValueError):
+        oracle.prefill(q, k, v, g, beta, cu_seqlens=cu)
+
+
+def test_threads_do_not_change_results():
+    T, H, dk, dv = 30, 7, 8, 8
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    a = oracle.prefill(q, k, v, g, beta, num_threads=1)
+    b = oracle.prefill(q, k, v, g, beta, num_threads=5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes (in scratch copies of the oracle, on the CPU)
+# ----------------------------------------------------------------------------
+
+MUTANTS = {
+    "no_decay": ("alpha[i] = exp(gt[i]);", "alpha[i] = 1.0;"),
+    "decay_sign": ("alpha[i] = exp(gt[i]);", "alpha[i] = exp(-gt[i]);"),
+    "decay_on_value_axis": ("S[i * dv + j] *= alpha[i];", "S[i * dv + j] *= alpha[j % dk];"),
+    "correction_sign": ("u[j] = bt * (vt[j] - p[j]);", "u[j] = bt * (vt[j] + p[j]);"),
+    "beta_dropped": ("u[j] = bt * (vt[j] - p[j]);", "u[j] = (vt[j] - p[j]);"),
+    "predict_with_q": ("p[j] += S[i * dv + j] * kt[i];", "p[j] += S[i * dv + j] * qt[i];"),
+    "read_before_write": ("ot[j] += S[i * dv + j] * qt[i];",
+                          "ot[j] += (S[i * dv + j] - kt[i] * u[j]) * qt[i];"),
+    "write_with_q": ("S[i * dv + j] += kt[i] * u[j];", "S[i * dv + j] += qt[i] * u[j];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name, tmp_path, golden):
+    src_dir = os.path.dirname(oracle.__file__)
+    src = open(os.path.join(src_dir, "kda_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor not found once: {old}"
+    shutil.copy(os.path.join(src_dir, "kda_oracle.h"), tmp_path / "kda_oracle.h")
+    (tmp_path / "m.c").write_text(src.replace(old, new))
+    so = tmp_path / f"libmut_{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", str(so),
+                    str(tmp_path / "m.c"), "-lm"], check=True)
+    mutant = oracle.Oracle(str(so))
+    failed = []
+    for pin in PINS:
+        try:
+            _run_pin(pin, mutant, golden)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake '{name}' passed every pin"
