@@ -1,0 +1,409 @@
+"""Benchmark of the KDA operator on one GB300 (or N, one process each).
+
+Headline: prefill tokens/s of one 96-head KDA layer (B=1, T=8192, H=96,
+d=128; bf16 q/k/v/o, fp32 g/beta/state) -- one step is one kda_prefill call
+over the whole layer, every row of the hot path (decay prefix, decay-weighted
+operands, Gram matrices, triangular solve, inter-chunk readout, state carry,
+epilogue).  The decode workload (256 sequences x 64 single-token steps) is
+measured in the same run and reported under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (weak
+scaling, no collective on the data path); rank 0 prints one JSON line with the
+aggregate over ranks timed as the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA tokens/s per layer (96 heads, d=128) prefill & decode; % of roofline"
+UNIT = "tokens/s"
+
+# Algorithmic bytes per token of one 96-head layer (prefill): q, k, v, o bf16
+# (4 x 96 x 128 x 2) + g fp32 (96 x 128 x 4) + beta fp32 (96 x 4).
+PREFILL_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 96 * 128 * 4 + 96 * 4  # 147840
+# Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
+# q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
+DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
+L2_BYTES = 129 * 2 ** 20
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (host side; no collective on the data path)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank sets the
+    job's time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; samples are tagged
+    with wall time so that those inside the timed region can be picked."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if not inside:  # region shorter than the sampling period: take the nearest
+            near = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside, note = [near[1]], "nearest sample (timed region shorter than 100 ms)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i] == "Active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_digest(relpath: str) -> str:
+    with open(os.path.join(ROOT, relpath), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def profiled_traffic(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(source)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[2] == digest:
+                return float(parts[3])
+    return None
+
+
+def time_steps(fn, steps: int, warmup: int, world: int, stream):
+    """W untimed steps, then exactly K steps between CUDA events on `stream`,
+    bracketed by a barrier and a device synchronize.  Returns
+    (ms_per_step max over ranks, t_wall_start, t_wall_end)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        fn()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / steps
+    return reduce_max(ms, world, device="cuda"), t0, t1
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle as it stands, on this host's cores
+# ----------------------------------------------------------------------------
+
+def cpu_baseline_prefill(heads: int = 96, tokens: int = 8192, seed: int = 1):
+    """Time the oracle on a sample of the prefill workload (the first
+    `tokens` tokens of `heads` heads, the same recipe), scaled to layer
+    tokens/s (96 heads)."""
+    import torch
+    import oracle
+    from linear_attention_sequence_gb300 import synth
+    w = synth.WORKLOADS["prefill_8k"]
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    q, k, v, g, beta = synth.draw_tokens(tokens, heads, w.d, w.d, w.dtype, w.mu, gen, "cpu")
+    args = [x.to(torch.float64).numpy() for x in (q, k, v, g, beta)]
+    cores = oracle.num_cpus()
+    t0 = time.perf_counter()
+    oracle.prefill(*args, num_threads=cores)
+    dt = time.perf_counter() - t0
+    layer_tokens = tokens * heads / 96.0
+    return {"value": layer_tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{heads} heads x {tokens} tokens of the prefill_8k recipe "
+                      f"(fp64 token loop, {cores} threads), {dt:.2f} s wall"}
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    heads, tokens = 24, 8192
+    # warm-up and timed steps, each one bounded sample of the workload
+    import torch
+    import oracle
+    from linear_attention_sequence_gb300 import synth
+    w = synth.WORKLOADS["prefill_8k"]
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(1)
+    q, k, v, g, beta = synth.draw_tokens(tokens, heads, w.d, w.d, w.dtype, w.mu, gen, "cpu")
+    a = [x.to(torch.float64).numpy() for x in (q, k, v, g, beta)]
+    cores = oracle.num_cpus()
+    for _ in range(args.warmup):
+        oracle.prefill(*a, num_threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prefill(*a, num_threads=cores)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = tokens * heads / 96.0 / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "prefill_8k sample: 24 of 96 heads x 8192 tokens (B=1, d=128, "
+                               "bf16 q/k/v widened to fp64), scaled to 96-head layer tokens/s"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{heads} heads x {tokens} tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from linear_attention_sequence_gb300 import _build
+    _build.build()
+    import linear_attention_sequence_gb300 as kda
+    from linear_attention_sequence_gb300 import synth
+
+    stream = torch.cuda.current_stream()
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+
+    # ---------------- prefill (headline) ----------------
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, dev)
+    T = w.total_tokens
+    out = torch.empty((T, w.heads, w.d), dtype=w.dtype, device=dev)
+    fin = torch.empty((1, w.heads, w.d, w.d), dtype=torch.float32, device=dev)
+    in_bytes = sum(inp[x].numel() * inp[x].element_size() for x in ("q", "k", "v", "g", "beta"))
+
+    def prefill_step():
+        kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                        cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin, stream=stream)
+
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    ms, t0, t1 = time_steps(prefill_step, args.steps, args.warmup, world, stream)
+    clocks = sampler.summary(t0, t1) if sampler else None
+    value = T * world / (ms * 1e-3)
+    achieved = PREFILL_BYTES_PER_TOKEN * T / (ms * 1e-3) / 1e9
+    kernel_src = "linear_attention_sequence_gb300/csrc/kda_prefill_fp32.cu"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "peak_source": peak_src,
+                "kernel": "kda_prefill_fp32_kernel",
+                "traffic": profiled_traffic("kda_prefill_fp32_kernel", kernel_src, "prefill_8k"),
+                "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TOKEN * T}
+
+    # ---------------- e2e through the public API, host buffers ----------------
+    host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
+    dbuf = {x: torch.empty_like(inp[x]) for x in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+
+    def e2e_step():
+        for x in host:
+            dbuf[x].copy_(host[x], non_blocking=True)
+        kda.kda_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
+                        cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    ms_e2e, _, _ = time_steps(e2e_step, e2e_steps, max(args.warmup, 3), world, stream)
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+    e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    del host, dbuf, out_h, fin_h, inp, out, fin
+    torch.cuda.empty_cache()
+
+    # ---------------- decode ----------------
+    wd = synth.WORKLOADS["decode_256x64"]
+    dx = synth.decode_inputs(wd, dev)
+    state = dx["state"]
+    dout = torch.empty((wd.num_seqs, wd.heads, wd.d), dtype=wd.dtype, device=dev)
+
+    def decode_round():
+        for s in range(wd.steps):
+            kda.kda_decode(dx["q"][s], dx["k"][s], dx["v"][s], dx["g"][s], dx["beta"][s], state,
+                           out=dout, stream=stream)
+
+    d_rounds = max(1, min(args.steps, 5))
+    ms_round, dt0, dt1 = time_steps(decode_round, d_rounds, max(1, min(args.warmup, 2)), world,
+                                    stream)
+    dclocks = sampler.summary(dt0, dt1) if sampler else None
+    ms_dstep = ms_round / wd.steps
+    d_tokens = wd.num_seqs
+    d_ach = DECODE_BYTES_PER_HEAD_STEP * wd.num_seqs * wd.heads / (ms_dstep * 1e-3) / 1e9
+    decode = {"value": d_tokens * world / (ms_dstep * 1e-3), "unit": UNIT,
+              "ms_per_step": ms_dstep, "steps_per_round": wd.steps, "rounds": d_rounds,
+              "config": {"workload": "decode_256x64: 256 sequences x 64 single-token steps, "
+                                     "H=96, d=128, fp32 state 1.61 GB (> L2), bf16 q/k/v/o"},
+              "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm_gbs, "unit": "GB/s",
+                           "frac": d_ach / hbm_gbs, "peak_source": peak_src,
+                           "kernel": "kda_decode_kernel",
+                           "traffic": profiled_traffic(
+                               "kda_decode_kernel",
+                               "linear_attention_sequence_gb300/csrc/kda_decode.cu",
+                               "decode_256x64"),
+                           "algorithmic_bytes_per_launch":
+                               DECODE_BYTES_PER_HEAD_STEP * wd.num_seqs * wd.heads},
+              "gpu_launches": d_rounds * wd.steps, "clocks": dclocks}
+    if sampler:
+        sampler.stop()
+
+    if rank == 0:
+        cpu = None if world > 1 else cpu_baseline_prefill()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "prefill_8k: B=1, T=8192, H=96, d_k=d_v=128, bf16 q/k/v/o, "
+                                   "fp32 g/beta/state, zero initial state",
+                       "l2": f"inputs {in_bytes / 1e9:.2f} GB > L2 {L2_BYTES / 2**20:.0f} MiB; "
+                             "no flush between steps",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

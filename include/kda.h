@@ -1,0 +1,146 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention operator.
+ *
+ * The operator is the per-head gated delta-rule recurrence
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = S_t^T q_t,            alpha_t = exp(g_t)  (one factor per key channel)
+ *
+ * from "Understanding Kimi K3's Attention" (state-update and readout
+ * equations, symbol table) and "Kimi K3.1 and the Road From Softmax Attention
+ * to Kimi Delta Attention" (section "5. Kimi Delta Attention").  The readout
+ * uses the state after the token's own write ("Kimi K3 course, lesson 2";
+ * "Inside Kimi K3", section "Sequence mixing": the intra-chunk causal matrix
+ * includes the diagonal).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensors are row-major and contiguous, in DEVICE memory, owned by
+ *    the caller.  The library allocates no device memory on these paths.
+ *  - q, k  [T_tot, H, d_k];  v, out [T_tot, H, d_v];  g [T_tot, H, d_k] fp32
+ *    (log-decay); beta [T_tot, H] fp32; states [N, H, d_k, d_v] fp32 with row
+ *    i = key channel i (the decay scales rows: "Hybrid Attention", section
+ *    "Forgetting can be selective, too").
+ *  - No scaling, normalisation or gating is applied: q and k arrive already
+ *    L2-normalised, the 1/sqrt(d) readout scale and the output gate belong to
+ *    the caller ("Understanding Kimi K3's Attention", symbol table and output
+ *    equation).
+ *  - Preconditions that are documented but not checked on the device (they
+ *    would need a read of device memory): g in [-5, 0] (the log-decay bound
+ *    g_t = g_min Sigmoid(e^A z_t), g_min = -5) and beta in [0, 1].  Inputs
+ *    outside them give finite but unspecified results; they never fault.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  KDA_OK means "enqueued".  Arguments are validated on
+ *    the host before anything is launched; an error return launches nothing.
+ *  - Supported head sizes: d_k == d_v, either 64 or 128.  Anything else
+ *    returns KDA_ERR_UNSUPPORTED.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* null pointer, negative size, bad dtype */
+    KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (head size, dtype combo) */
+    KDA_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+    KDA_ERR_TIMEOUT = 4           /* a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/* Prefill kernel selection.  KDA_PREFILL_DEFAULT picks the tensor-core
+ * kernel where it supports the shape and dtype, else the fp32 CUDA-core one. */
+typedef enum {
+    KDA_PREFILL_DEFAULT = 0,
+    KDA_PREFILL_FP32 = 1,  /* CUDA-core fp32 chunked kernel (any supported shape) */
+    KDA_PREFILL_TC = 2     /* tcgen05 tensor-core chunked kernel (d = 128) */
+} kda_prefill_variant;
+
+typedef void *kda_stream_t; /* a cudaStream_t */
+
+typedef struct {
+    int32_t num_seqs;     /* N >= 0 */
+    int32_t total_tokens; /* T_tot >= 0 (decode: must equal num_seqs) */
+    int32_t num_heads;    /* H >= 1 */
+    int32_t d_k;          /* key/query head size */
+    int32_t d_v;          /* value head size */
+    int32_t in_dtype;     /* kda_dtype of q, k, v */
+    int32_t out_dtype;    /* kda_dtype of out */
+    int32_t variant;      /* kda_prefill_variant (ignored by decode) */
+} kda_dims;
+
+/*
+ * kda_prefill -- chunk-parallel prefill over a packed variable-length batch.
+ *
+ * Evaluates the recurrence for every sequence n and head h over tokens
+ * [cu_seqlens[n], cu_seqlens[n+1]), starting from init_state[n,h] (zeros if
+ * init_state is NULL), writes o_t for every token into `out` and, if
+ * final_state is non-NULL, the state after the last token of each sequence.
+ * Tokens inside a chunk are evaluated together and the state is carried
+ * from chunk to chunk ("Inside Kimi K3", section "Sequence mixing";
+ * "Hybrid Attention", section "But isn't a recurrent update sequential?");
+ * the result equals the token-by-token recurrence up to rounding, for any
+ * sequence length (no divisibility requirement).
+ *
+ *   q, k, v     device, in_dtype, layouts above.
+ *   g, beta     device, fp32.
+ *   init_state  device fp32 [N, H, d_k, d_v] or NULL.
+ *   cu_seqlens  device int32 [N+1] or NULL.  If NULL, T_tot must be a
+ *               multiple of N and sequence n covers [n T, (n+1) T) with
+ *               T = T_tot / N.  Otherwise cu[0] = 0, non-decreasing,
+ *               cu[N] = T_tot; entries outside [0, T_tot] are clamped on the
+ *               device and a decreasing pair is read as an empty sequence, so
+ *               a malformed array can never cause an out-of-bounds access.
+ *               An empty sequence copies init_state (or zeros) to final_state.
+ *   out         device, out_dtype [T_tot, H, d_v]; must not alias any input.
+ *   final_state device fp32 [N, H, d_k, d_v] or NULL.  May alias init_state
+ *               exactly (each slice is read before it is written).
+ *
+ * Accumulation is fp32; a bf16 `out` is the round-to-nearest-even of the
+ * value an fp32 `out` would hold.
+ */
+kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const float *init_state,
+                       const int32_t *cu_seqlens, void *out, float *final_state,
+                       kda_stream_t stream);
+
+/*
+ * kda_decode -- one single-token update of N independent fixed-size states.
+ *
+ * For each sequence n and head h: M = Diag(exp g) S, u = beta (v - M^T k),
+ * S <- M + k u^T (in place), o = S^T q -- the delta form of the recurrence
+ * ("Understanding Kimi K3's Attention", rewritten update; "Hybrid
+ * Attention", recurrent implementation).  Each fp32 state is read once and
+ * written once.
+ *
+ *   dims        total_tokens must equal num_seqs (one token per sequence).
+ *   q, k, v     device, in_dtype, [N, H, d]; g device fp32 [N, H, d_k];
+ *               beta device fp32 [N, H].
+ *   state_inout device fp32 [N, H, d_k, d_v], updated in place.
+ *   out         device, out_dtype [N, H, d_v]; must not alias any input.
+ */
+kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,
+                      const float *g, const float *beta, float *state_inout, void *out,
+                      kda_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *kda_status_string(kda_status status);
+
+/* Text of the most recent CUDA error seen by this thread's calls into the
+ * library ("" if none).  Static storage per thread; valid until the next call. */
+const char *kda_last_cuda_error(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

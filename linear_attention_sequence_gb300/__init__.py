@@ -1,0 +1,169 @@
+"""GB300 (sm_103a) Kimi Delta Attention operator.
+
+The compute lives in ``libkda.so`` (hand-written CUDA kernels behind the C ABI
+declared in ``include/kda.h``).  This module is the thin Python binding: it
+turns torch tensors into pointers and sizes, calls the C entry points of the
+same names and raises on a non-OK status.  It performs no arithmetic of the
+method and has no fallback: if the library is missing, every call raises.
+
+    kda_prefill(q, k, v, g, beta, ...)  chunk-parallel prefill, packed batch
+    kda_decode(q, k, v, g, beta, state) one-token in-place state update
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["KdaError", "kda_prefill", "kda_decode", "kda_status_string", "lib", "library_path",
+           "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK = 0
+DTYPE_F32, DTYPE_BF16 = 0, 1
+PREFILL_DEFAULT, PREFILL_FP32, PREFILL_TC = 0, 1, 2
+_DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = kda_status_string(status)
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("variant", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libkda.so (ctypes).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()'); there is no fallback")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, fp = ctypes.c_void_p, ctypes.c_void_p
+        L.kda_prefill.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp, fp, vp]
+        L.kda_prefill.restype = ctypes.c_int
+        L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
+        L.kda_decode.restype = ctypes.c_int
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_last_cuda_error.restype = ctypes.c_char_p
+        L.kda_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def kda_status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != KDA_OK:
+        detail = lib().kda_last_cuda_error().decode() if st == 3 else ""
+        raise KdaError(st, where, detail)
+
+
+def _require(t, name, dtype=None, ndim=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,
+                out=None, final_state=None, out_dtype=None, variant=PREFILL_DEFAULT,
+                return_final_state=True, stream=None):
+    """Chunked KDA prefill (C entry point ``kda_prefill``).
+
+    q, k [T, H, d_k] and v [T, H, d_v] in fp32 or bf16; g [T, H, d_k] fp32;
+    beta [T, H] fp32; init_state [N, H, d_k, d_v] fp32 or None; cu_seqlens
+    int32 [N+1] (device) or None (``num_seqs`` equal-length sequences,
+    default 1).  Returns ``(out, final_state)``.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, ndim=3)
+    _require(g, "g", torch.float32, 3)
+    _require(beta, "beta", torch.float32, 2)
+    _require(init_state, "init_state", torch.float32, 4)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, fp32 or bf16")
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:2] != (T, H) or beta.shape != (T, H):
+        raise ValueError("inconsistent q/k/v/g/beta shapes")
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=out_dtype, device=q.device)
+    _require(out, "out", out_dtype, 3)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    _require(final_state, "final_state", torch.float32, 4)
+    dims = Dims(N, T, H, dk, dv, _DTYPES[q.dtype], _DTYPES[out_dtype], int(variant))
+    st = lib().kda_prefill(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                           _stream(stream))
+    _check(st, "kda_prefill")
+    return out, final_state
+
+
+def kda_decode(q, k, v, g, beta, state, *, out=None, out_dtype=None, stream=None):
+    """One decode step (C entry point ``kda_decode``): q, k, g [N, H, d_k];
+    v [N, H, d_v]; beta [N, H]; state [N, H, d_k, d_v] fp32, updated in place.
+    Returns ``out`` [N, H, d_v]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, n, ndim=3)
+    _require(g, "g", torch.float32, 3)
+    _require(beta, "beta", torch.float32, 2)
+    _require(state, "state", torch.float32, 4)
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, fp32 or bf16")
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=out_dtype, device=q.device)
+    _require(out, "out", out_dtype, 3)
+    dims = Dims(N, N, H, dk, dv, _DTYPES[q.dtype], _DTYPES[out_dtype], 0)
+    st = lib().kda_decode(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                          _ptr(state), _ptr(out), _stream(stream))
+    _check(st, "kda_decode")
+    return out

@@ -1,0 +1,110 @@
+// kda_api.cu -- the C ABI front end: argument validation, kernel selection,
+// launch and error mapping.  Declarations and semantics: include/kda.h.
+
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+kda_status cuda_fail(cudaError_t e, const char *where) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", where,
+             cudaGetErrorName(e), cudaGetErrorString(e));
+    return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid_dtype(int32_t d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16; }
+
+// Shared checks of the dims struct.  Fills P on success.
+kda_status check_dims(const kda_dims *d, kda::Problem &P) {
+    if (!d) return KDA_ERR_INVALID_ARGUMENT;
+    if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads < 1 || d->d_k < 1 || d->d_v < 1)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!valid_dtype(d->in_dtype) || !valid_dtype(d->out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (d->variant < KDA_PREFILL_DEFAULT || d->variant > KDA_PREFILL_TC) return KDA_ERR_INVALID_ARGUMENT;
+    if (d->d_k != d->d_v || (d->d_k != 64 && d->d_k != 128)) return KDA_ERR_UNSUPPORTED;
+    // element counts must fit the kernels' 64-bit index arithmetic comfortably
+    const int64_t elems = (int64_t)d->total_tokens * d->num_heads * d->d_k;
+    const int64_t states = (int64_t)d->num_seqs * d->num_heads * d->d_k * d->d_v;
+    if (elems > ((int64_t)1 << 50) || states > ((int64_t)1 << 50)) return KDA_ERR_INVALID_ARGUMENT;
+    P.N = d->num_seqs;
+    P.T = d->total_tokens;
+    P.H = d->num_heads;
+    P.dk = d->d_k;
+    P.dv = d->d_v;
+    P.in_dtype = d->in_dtype;
+    P.out_dtype = d->out_dtype;
+    P.variant = d->variant;
+    P.seq_len = 0;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char *kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t kda_version(void) { return 100; /* 0.1.0 */ }
+
+kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const float *init_state,
+                       const int32_t *cu_seqlens, void *out, float *final_state,
+                       kda_stream_t stream) {
+    kda::Problem P;
+    kda_status st = check_dims(dims, P);
+    if (st != KDA_OK) return st;
+    if (P.T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens) {
+        if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
+        P.seq_len = P.N ? P.T / P.N : 0;
+    }
+    if (P.T > 0 && out == (const void *)q) return KDA_ERR_INVALID_ARGUMENT;
+    if (final_state && init_state && final_state != init_state) {
+        // partial overlap of the two state arrays is not supported
+        const char *a = (const char *)init_state, *b = (const char *)final_state;
+        const size_t bytes = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
+        if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if (P.variant == KDA_PREFILL_TC) return KDA_ERR_UNSUPPORTED;
+    if (P.N == 0) return KDA_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens, out,
+                                            final_state, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_prefill");
+    return KDA_OK;
+}
+
+kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,
+                      const float *g, const float *beta, float *state_inout, void *out,
+                      kda_stream_t stream) {
+    kda::Problem P;
+    kda_status st = check_dims(dims, P);
+    if (st != KDA_OK) return st;
+    if (P.T != P.N) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.N == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(state_inout)) return KDA_ERR_INVALID_ARGUMENT;  // 16-byte vector access
+    if (out == (const void *)state_inout) return KDA_ERR_INVALID_ARGUMENT;
+    cudaError_t e = kda_launch_decode(P, q, k, v, g, beta, state_inout, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_decode");
+    return KDA_OK;
+}
+
+}  // extern "C"

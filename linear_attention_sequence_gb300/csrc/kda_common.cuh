@@ -1,0 +1,51 @@
+// kda_common.cuh -- small helpers shared by the KDA kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Element loads/stores for the two supported activation dtypes.
+__device__ __forceinline__ float ld_elem(const float *p) { return *p; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st_elem(float *p, float x) { *p = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Sequence bounds for sequence n.  Entries of cu_seqlens are clamped into
+// [0, total] and a decreasing pair is read as an empty sequence, so a
+// malformed array never leads to an out-of-range access.
+__device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, int64_t total,
+                                           int64_t seq_len, int64_t &a, int64_t &b) {
+    if (cu) {
+        int64_t x = cu[n], y = cu[n + 1];
+        x = x < 0 ? 0 : (x > total ? total : x);
+        y = y < 0 ? 0 : (y > total ? total : y);
+        a = x;
+        b = y < x ? x : y;
+    } else {
+        a = (int64_t)n * seq_len;
+        b = a + seq_len;
+    }
+}
+
+// Host-side launch parameters after validation.
+struct Problem {
+    int32_t N, T, H, dk, dv;
+    int32_t in_dtype, out_dtype, variant;
+    int64_t seq_len;  // used when cu_seqlens == NULL
+};
+
+}  // namespace kda
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t kda_launch_decode(const kda::Problem &P, const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, float *state, void *out,
+                              cudaStream_t stream);
+cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *init_state, const int32_t *cu, void *out,
+                                    float *final_state, cudaStream_t stream);

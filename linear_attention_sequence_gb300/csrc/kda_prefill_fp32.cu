@@ -1,0 +1,249 @@
+// kda_prefill_fp32.cu -- chunked KDA prefill on the CUDA cores, fp32 throughout.
+//
+// This is the accuracy path (fp32 inputs are checked at 1e-4 of rms) and the
+// kernel for shapes the tensor-core path does not take.  It evaluates the
+// chunk form of the recurrence: tokens of a chunk are processed together and
+// the state is carried from chunk to chunk ("Inside Kimi K3", section
+// "Sequence mixing"; "Hybrid Attention", section "But isn't a recurrent update
+// sequential?").  Within a chunk of C tokens (positions r = 0..C-1), with
+// Gamma_r = sum_{i<=r} g_i per key channel and S0 the state entering it,
+// unrolling the token recurrence gives (exactly, up to rounding):
+//
+//   u_r = beta_r (v_r - S0^T (e^{Gamma_r} . k_r)) - sum_{i<r} Akk[r,i] u_i
+//   o_r = S0^T (e^{Gamma_r} . q_r) + sum_{i<=r} Aqk[r,i] u_i
+//   S_C = Diag(e^{Gamma_{C-1}}) S0 + sum_i (e^{Gamma_{C-1} - Gamma_i} . k_i) u_i^T
+//
+//   Akk[r,i] = beta_r sum_c k_rc k_ic e^{Gamma_rc - Gamma_ic}   (i <  r)
+//   Aqk[r,i] =        sum_c q_rc k_ic e^{Gamma_rc - Gamma_ic}   (i <= r: the
+//                                           diagonal is included, each token
+//                                           reads the state after its write)
+//
+// The u_r form is a forward substitution with the unit lower-triangular
+// (I + Akk), the "triangular solve" of the chunkwise form.  Every decay factor
+// is an exponential of a non-positive number, so nothing overflows for any
+// chunk length.  Rows past the end of a sequence are loaded as zeros (k = q =
+// v = 0, g = 0, beta = 0): they neither decay nor write the state, and their
+// outputs are not stored, so sequence lengths need not divide C.
+//
+// Grid: one CTA per (d_v block of BV columns, head, sequence).  Columns of the
+// state evolve independently given k, g and beta, so d_v splits without
+// communication; the Gram matrices are recomputed per block.
+
+#include "kda_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int BV = 32;  // state columns per CTA (one per lane)
+
+template <int DK, int C>
+struct Smem {
+    float G[C][DK];    // Gamma, then e^{Gamma} . k
+    float K[C][DK];    // k, then e^{Gamma_last - Gamma} . k
+    float Q[C][DK];    // q, then e^{Gamma} . q
+    float S[DK][BV];   // state slice (fp32)
+    float U[C][BV];    // v, then v', then u
+    float Akk[C][C + 1];
+    float Aqk[C][C + 1];
+    float beta[C];
+    float glast[DK];   // Gamma of the last row
+};
+
+template <int DK, int C, typename IN_T, typename OUT_T>
+__global__ void __launch_bounds__(kThreads)
+kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
+                        const IN_T *__restrict__ v, const float *__restrict__ g,
+                        const float *__restrict__ beta, const float *__restrict__ init_state,
+                        const int32_t *__restrict__ cu, OUT_T *__restrict__ out,
+                        float *__restrict__ final_state, int H, int DV, int64_t total,
+                        int64_t seq_len) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem<DK, C> &sm = *reinterpret_cast<Smem<DK, C> *>(smem_raw);
+
+    const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int j0 = vb * BV;
+
+    int64_t a, b;
+    kda::seq_bounds(cu, n, total, seq_len, a, b);
+
+    const int64_t state_off = ((int64_t)n * H + h) * DK * (int64_t)DV;
+    for (int idx = t; idx < DK * BV; idx += kThreads) {
+        const int c = idx / BV, j = idx % BV;
+        sm.S[c][j] = init_state ? init_state[state_off + (int64_t)c * DV + j0 + j] : 0.f;
+    }
+
+    const int64_t rowK = (int64_t)H * DK, rowV = (int64_t)H * DV;
+    for (int64_t t0 = a; t0 < b; t0 += C) {
+        const int L = (int)((b - t0) < C ? (b - t0) : C);
+        __syncthreads();  // previous chunk done with every buffer
+        // ---- load the chunk (rows >= L are zeros) ----
+        for (int idx = t; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, c = idx % DK;
+            float gv = 0.f, kv = 0.f, qv = 0.f;
+            if (r < L) {
+                const int64_t off = (t0 + r) * rowK + (int64_t)h * DK + c;
+                gv = g[off];
+                kv = kda::ld_elem(k + off);
+                qv = kda::ld_elem(q + off);
+            }
+            sm.G[r][c] = gv;
+            sm.K[r][c] = kv;
+            sm.Q[r][c] = qv;
+        }
+        for (int idx = t; idx < C * BV; idx += kThreads) {
+            const int r = idx / BV, j = idx % BV;
+            sm.U[r][j] = r < L ? kda::ld_elem(v + (t0 + r) * rowV + (int64_t)h * DV + j0 + j) : 0.f;
+        }
+        if (t < C) sm.beta[t] = t < L ? beta[(t0 + t) * H + h] : 0.f;
+        __syncthreads();
+
+        // ---- Gamma: running sum of g over the chunk, per key channel ----
+        if (t < DK) {
+            float run = 0.f;
+            for (int r = 0; r < C; ++r) {
+                run += sm.G[r][t];
+                sm.G[r][t] = run;
+            }
+            sm.glast[t] = run;
+        }
+        __syncthreads();
+
+        // ---- Gram matrices Akk (strict, beta rows) and Aqk (inclusive) ----
+        constexpr int NPAIR = C * (C + 1) / 2;
+        for (int p = warp; p < NPAIR; p += kWarps) {
+            int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+            while (r * (r + 1) / 2 > p) --r;
+            while ((r + 1) * (r + 2) / 2 <= p) ++r;
+            const int i = p - r * (r + 1) / 2;
+            float akk = 0.f, aqk = 0.f;
+#pragma unroll 4
+            for (int c = lane; c < DK; c += 32) {
+                const float e = __expf(sm.G[r][c] - sm.G[i][c]);
+                const float ke = sm.K[i][c] * e;
+                akk += sm.K[r][c] * ke;
+                aqk += sm.Q[r][c] * ke;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                akk += __shfl_xor_sync(0xffffffffu, akk, o);
+                aqk += __shfl_xor_sync(0xffffffffu, aqk, o);
+            }
+            if (lane == 0) {
+                sm.Akk[r][i] = i < r ? sm.beta[r] * akk : 0.f;
+                sm.Aqk[r][i] = aqk;
+            }
+        }
+        __syncthreads();
+
+        // ---- decay-weighted operands for the state terms ----
+        for (int idx = t; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, c = idx % DK;
+            const float gam = sm.G[r][c];
+            const float e = __expf(gam);
+            const float kv = sm.K[r][c];
+            sm.Q[r][c] *= e;
+            sm.G[r][c] = kv * e;
+            sm.K[r][c] = kv * __expf(sm.glast[c] - gam);
+        }
+        __syncthreads();
+
+        // ---- v' = v - (e^Gamma . K) S0 and the inter-chunk readout (e^Gamma . Q) S0 ----
+        constexpr int RPW = C / kWarps;  // rows per warp
+        float o_acc[RPW];
+        {
+            float vs[RPW];
+#pragma unroll
+            for (int x = 0; x < RPW; ++x) { vs[x] = 0.f; o_acc[x] = 0.f; }
+            for (int c = 0; c < DK; ++c) {
+                const float s = sm.S[c][lane];
+#pragma unroll
+                for (int x = 0; x < RPW; ++x) {
+                    const int r = warp * RPW + x;
+                    vs[x] += sm.G[r][c] * s;
+                    o_acc[x] += sm.Q[r][c] * s;
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < RPW; ++x) sm.U[warp * RPW + x][lane] -= vs[x];
+        }
+        __syncthreads();
+
+        // ---- forward substitution: u_r = beta_r v'_r - sum_{i<r} Akk[r,i] u_i ----
+        if (warp == 0) {
+            for (int r = 0; r < C; ++r) {
+                float acc = sm.beta[r] * sm.U[r][lane];
+                for (int i = 0; i < r; ++i) acc -= sm.Akk[r][i] * sm.U[i][lane];
+                sm.U[r][lane] = acc;
+            }
+        }
+        __syncthreads();
+
+        // ---- intra-chunk readout and output store ----
+#pragma unroll
+        for (int x = 0; x < RPW; ++x) {
+            const int r = warp * RPW + x;
+            float acc = o_acc[x];
+            for (int i = 0; i <= r; ++i) acc += sm.Aqk[r][i] * sm.U[i][lane];
+            if (r < L) kda::st_elem(out + (t0 + r) * rowV + (int64_t)h * DV + j0 + lane, acc);
+        }
+
+        // ---- state carry: S = Diag(e^{Gamma_last}) S0 + Kbar^T U ----
+        constexpr int CPW = DK / kWarps;  // state rows per warp
+#pragma unroll
+        for (int x = 0; x < CPW; ++x) {
+            const int c = warp * CPW + x;
+            float acc = __expf(sm.glast[c]) * sm.S[c][lane];
+            for (int r = 0; r < C; ++r) acc += sm.K[r][c] * sm.U[r][lane];
+            sm.S[c][lane] = acc;
+        }
+    }
+    __syncthreads();
+    if (final_state) {
+        for (int idx = t; idx < DK * BV; idx += kThreads) {
+            const int c = idx / BV, j = idx % BV;
+            final_state[state_off + (int64_t)c * DV + j0 + j] = sm.S[c][j];
+        }
+    }
+}
+
+template <int DK, int C, typename IN_T, typename OUT_T>
+cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const void *v,
+                   const float *g, const float *beta, const float *init_state,
+                   const int32_t *cu, void *out, float *final_state, cudaStream_t stream) {
+    if (P.N == 0) return cudaSuccess;
+    auto kern = kda_prefill_fp32_kernel<DK, C, IN_T, OUT_T>;
+    const size_t smem = sizeof(Smem<DK, C>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(P.dv / BV, P.H, P.N);
+    kern<<<grid, kThreads, smem, stream>>>((const IN_T *)q, (const IN_T *)k, (const IN_T *)v, g,
+                                           beta, init_state, cu, (OUT_T *)out, final_state, P.H,
+                                           P.dv, (int64_t)P.T, P.seq_len);
+    return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t dispatch_dtypes(const kda::Problem &P, const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, const float *init,
+                            const int32_t *cu, void *out, float *fin, cudaStream_t s) {
+    constexpr int C = 32;
+    const bool in_bf = P.in_dtype == KDA_DTYPE_BF16, out_bf = P.out_dtype == KDA_DTYPE_BF16;
+    if (in_bf && out_bf)
+        return launch<DK, C, __nv_bfloat16, __nv_bfloat16>(P, q, k, v, g, beta, init, cu, out, fin, s);
+    if (in_bf) return launch<DK, C, __nv_bfloat16, float>(P, q, k, v, g, beta, init, cu, out, fin, s);
+    if (out_bf) return launch<DK, C, float, __nv_bfloat16>(P, q, k, v, g, beta, init, cu, out, fin, s);
+    return launch<DK, C, float, float>(P, q, k, v, g, beta, init, cu, out, fin, s);
+}
+
+}  // namespace
+
+cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *init_state, const int32_t *cu, void *out,
+                                    float *final_state, cudaStream_t stream) {
+    if (P.dk == 128)
+        return dispatch_dtypes<128>(P, q, k, v, g, beta, init_state, cu, out, final_state, stream);
+    return dispatch_dtypes<64>(P, q, k, v, g, beta, init_state, cu, out, final_state, stream);
+}

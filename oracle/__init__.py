@@ -89,12 +89,19 @@ class Oracle:
                              "cu_seqlens, or gates outside g in [-5,0], beta in [0,1])")
         return out, fin
 
-    def decode(self, q, k, v, g, beta, state, num_threads: int = 0):
+    def decode(self, q, k, v, g, beta, state, num_threads: int = 0, inplace: bool = False):
         """One decode step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
-        beta [N, H]; state [N, H, d_k, d_v].  Returns (out, new_state), fp64;
-        the input ``state`` is not modified."""
+        beta [N, H]; state [N, H, d_k, d_v].  Returns (out, new_state), fp64.
+        The input ``state`` is left alone unless ``inplace`` (then it must be
+        a C-contiguous float64 array and is updated and returned)."""
         q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
-        st = np.array(state, dtype=np.float64, copy=True, order="C")
+        if inplace:
+            if not (isinstance(state, np.ndarray) and state.dtype == np.float64
+                    and state.flags.c_contiguous):
+                raise ValueError("inplace decode needs a C-contiguous float64 state")
+            st = state
+        else:
+            st = np.array(state, dtype=np.float64, copy=True, order="C")
         N, H, dk = q.shape
         dv = v.shape[2]
         out = np.zeros((N, H, dv), np.float64)

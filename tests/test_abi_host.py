@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute launched).
+
+- the library builds and loads, and exports every function include/kda.h declares;
+- argument validation rejects bad input with the documented status before
+  any launch (every call here is invalid, so nothing reaches the device).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+import linear_attention_sequence_gb300 as kda
+from linear_attention_sequence_gb300 import Dims, _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return kda.lib()
+
+
+def declared_functions():
+    names = []
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert "kda_prefill" in names and "kda_decode" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(kda_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_status_strings(L):
+    for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_CUDA"), (4, "KDA_ERR_TIMEOUT")]:
+        assert kda.kda_status_string(code) == name
+    assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
+    assert L.kda_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: every call below is rejected
+FAKE_MISALIGNED = ctypes.c_void_p(0x10004)
+
+
+def prefill(L, dims, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, init=None, cu=None,
+                out=ctypes.c_void_p(0x20000), fin=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_prefill(d, args["q"], args["k"], args["v"], args["g"], args["beta"],
+                         args["init"], args["cu"], args["out"], args["fin"], None)
+
+
+def decode(L, dims, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=ctypes.c_void_p(0x30000),
+                out=ctypes.c_void_p(0x20000))
+    args.update(over)
+    return L.kda_decode(ctypes.byref(dims), args["q"], args["k"], args["v"], args["g"],
+                        args["beta"], args["state"], args["out"], None)
+
+
+def D(**kw):
+    base = dict(num_seqs=1, total_tokens=16, num_heads=2, d_k=128, d_v=128, in_dtype=1,
+                out_dtype=1, variant=0)
+    base.update(kw)
+    return Dims(**base)
+
+
+@pytest.mark.parametrize("dims,over,want", [
+    (None, {}, INVALID),
+    (D(num_seqs=-1), {}, INVALID),
+    (D(total_tokens=-5), {}, INVALID),
+    (D(num_heads=0), {}, INVALID),
+    (D(d_k=0), {}, INVALID),
+    (D(in_dtype=7), {}, INVALID),
+    (D(out_dtype=-1), {}, INVALID),
+    (D(variant=9), {}, INVALID),
+    (D(d_k=96, d_v=96), {}, UNSUPPORTED),
+    (D(d_k=128, d_v=64), {}, UNSUPPORTED),
+    (D(d_k=32, d_v=32), {}, UNSUPPORTED),
+    (D(), {"q": None}, INVALID),
+    (D(), {"g": None}, INVALID),
+    (D(), {"beta": None}, INVALID),
+    (D(), {"out": None}, INVALID),
+    (D(num_seqs=3, total_tokens=16), {}, INVALID),          # T % N != 0 without cu_seqlens
+    (D(num_seqs=0, total_tokens=4), {}, INVALID),
+    (D(), {"out": FAKE}, INVALID),                           # out aliases q
+    (D(num_seqs=2, total_tokens=16), {"init": ctypes.c_void_p(0x40000),
+                                       "fin": ctypes.c_void_p(0x40000 + 4096)}, INVALID),
+])
+def test_prefill_rejects(L, dims, over, want):
+    assert prefill(L, dims, **over) == want
+
+
+def test_prefill_empty_batch_is_ok(L):
+    # nothing to do: no sequences, no tokens -> OK without touching the device
+    assert prefill(L, D(num_seqs=0, total_tokens=0), q=None, k=None, v=None, g=None,
+                   beta=None, out=None) == OK
+
+
+@pytest.mark.parametrize("dims,over,want", [
+    (D(num_seqs=4, total_tokens=5), {}, INVALID),           # one token per sequence
+    (D(num_seqs=4, total_tokens=4, d_k=64, d_v=128), {}, UNSUPPORTED),
+    (D(num_seqs=4, total_tokens=4), {"state": None}, INVALID),
+    (D(num_seqs=4, total_tokens=4), {"state": FAKE_MISALIGNED}, INVALID),
+    (D(num_seqs=4, total_tokens=4), {"out": ctypes.c_void_p(0x30000)}, INVALID),
+    (D(num_seqs=4, total_tokens=4), {"k": None}, INVALID),
+])
+def test_decode_rejects(L, dims, over, want):
+    assert decode(L, dims, **over) == want
+
+
+def test_decode_empty_is_ok(L):
+    assert decode(L, D(num_seqs=0, total_tokens=0)) == OK
+
+
+def test_python_binding_rejects_cpu_tensors():
+    x = torch.zeros(4, 1, 64)
+    with pytest.raises(ValueError):
+        kda.kda_prefill(x, x, x, x, torch.zeros(4, 1))

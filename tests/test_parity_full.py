@@ -1,0 +1,103 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times (default variant, whole batch in one call).  Every (sequence,
+head) pair is independent, so the oracle checks all of them where it finishes
+in seconds (the 8K prefill, the decode workload) and a seeded sample of
+pairs, each over its whole length, where it does not (the packed varlen batch,
+the 256K context)."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_sequence_gb300 as kda
+from linear_attention_sequence_gb300 import synth
+import oracle
+from kda_testutil import TOL, rel_err, host64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _gpu(inp, out_dtype):
+    return kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                           init_state=inp["init_state"], cu_seqlens=inp["cu_seqlens"],
+                           out_dtype=out_dtype)
+
+
+def _oracle_pairs(inp, pairs):
+    """Run the oracle on the given (sequence, head) pairs; returns lists of
+    (slice, head, o_ref, s_ref)."""
+    cu = inp["cu_seqlens"].cpu().numpy()
+    res = []
+    for n, h in pairs:
+        sl = slice(int(cu[n]), int(cu[n + 1]))
+        args = [host64(inp[x][sl, h:h + 1]) for x in ("q", "k", "v", "g", "beta")]
+        init = None if inp["init_state"] is None else host64(inp["init_state"][n:n + 1, h:h + 1])
+        o, s = oracle.prefill(*args, init_state=init)
+        res.append((n, sl, h, o[:, 0], s[0, 0]))
+    return res
+
+
+def test_prefill_8k_all_heads():
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, DEV)
+    out32, fin32 = _gpu(inp, torch.float32)
+    out16, fin16 = _gpu(inp, torch.bfloat16)
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    assert torch.equal(fin16, fin32)
+    o_ref, s_ref = oracle.prefill(*(host64(inp[x]) for x in ("q", "k", "v", "g", "beta")))
+    eo, es = rel_err(host64(out32), o_ref), rel_err(host64(fin32), s_ref)
+    print(f"prefill_8k: err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+
+
+def test_varlen_packed_sampled_pairs():
+    w = synth.WORKLOADS["varlen_8seq"]
+    inp = synth.prefill_inputs(w, DEV)
+    out32, fin32 = _gpu(inp, torch.float32)
+    rng = np.random.default_rng(2024)
+    longest = int(np.argmax(w.lengths))
+    pairs = [(longest, 0), (longest, w.heads - 1)] + [
+        (int(rng.integers(w.num_seqs)), int(rng.integers(w.heads))) for _ in range(6)]
+    o_all, s_all = [], []
+    g_o, g_s = [], []
+    for n, sl, h, o, s in _oracle_pairs(inp, pairs):
+        o_all.append(o); s_all.append(s)
+        g_o.append(host64(out32[sl, h])); g_s.append(host64(fin32[n, h]))
+    eo = rel_err(np.concatenate(g_o), np.concatenate(o_all))
+    es = rel_err(np.stack(g_s), np.stack(s_all))
+    print(f"varlen_8seq (8 pairs): err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+
+
+def test_prefill_256k_sampled_heads():
+    w = synth.WORKLOADS["prefill_256k"]
+    inp = synth.prefill_inputs(w, DEV)
+    out32, fin32 = _gpu(inp, torch.float32)
+    pairs = [(0, 0), (0, 41), (0, 95)]
+    g_o, g_s, o_all, s_all = [], [], [], []
+    for n, sl, h, o, s in _oracle_pairs(inp, pairs):
+        o_all.append(o); s_all.append(s)
+        g_o.append(host64(out32[sl, h])); g_s.append(host64(fin32[n, h]))
+    eo = rel_err(np.concatenate(g_o), np.concatenate(o_all))
+    es = rel_err(np.stack(g_s), np.stack(s_all))
+    print(f"prefill_256k (3 heads): err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+    assert torch.isfinite(out32).all() and torch.isfinite(fin32).all()
+
+
+def test_decode_256x64_all_pairs():
+    w = synth.WORKLOADS["decode_256x64"]
+    x = synth.decode_inputs(w, DEV)
+    st = x["state"].clone()
+    ref = host64(x["state"])
+    outs, refs = [], []
+    for s in range(w.steps):
+        out = kda.kda_decode(x["q"][s], x["k"][s], x["v"][s], x["g"][s], x["beta"][s], st,
+                             out_dtype=torch.float32)
+        o_ref, ref = oracle.decode(*(host64(x[n][s]) for n in ("q", "k", "v", "g", "beta")), ref,
+                                   inplace=True)
+        outs.append(host64(out)); refs.append(o_ref)
+    eo = rel_err(np.stack(outs), np.stack(refs))
+    es = rel_err(host64(st), ref)
+    print(f"decode_256x64: err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
