@@ -305,11 +305,11 @@ def run_gpu(args):
     clocks = sampler.summary(t0, t1) if sampler else None
     value = T * world / (ms * 1e-3)
     achieved = PREFILL_BYTES_PER_TOKEN * T / (ms * 1e-3) / 1e9
-    kernel_src = "linear_attention_sequence_gb300/csrc/kda_prefill_fp32.cu"
+    kernel_src = "linear_attention_sequence_gb300/csrc/kda_prefill_tc.cu"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                 "frac": achieved / hbm_gbs, "peak_source": peak_src,
-                "kernel": "kda_prefill_fp32_kernel",
-                "traffic": profiled_traffic("kda_prefill_fp32_kernel", kernel_src, "prefill_8k"),
+                "kernel": "kda_prefill_tc_kernel",
+                "traffic": profiled_traffic("kda_prefill_tc_kernel", kernel_src, "prefill_8k"),
                 "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TOKEN * T}
 
     # ---------------- e2e through the public API, host buffers ----------------
@@ -375,7 +375,7 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "tf32", "data": "synthetic",
             "config": {"workload": "prefill_8k: B=1, T=8192, H=96, d_k=d_v=128, bf16 q/k/v/o, "
                                    "fp32 g/beta/state, zero initial state",
                        "l2": f"inputs {in_bytes / 1e9:.2f} GB > L2 {L2_BYTES / 2**20:.0f} MiB; "

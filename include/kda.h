@@ -129,6 +129,19 @@ kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const 
                       const float *g, const float *beta, float *state_inout, void *out,
                       kda_stream_t stream);
 
+/*
+ * kda_get_last_device_error -- report, then clear, the device-side status.
+ *
+ * The tensor-core prefill kernel waits on its own asynchronous copies and
+ * tensor-core operations with bounded waits; a wait that gives up makes the
+ * kernel stop early (outputs of the affected sequences are then incomplete)
+ * and records a status word on the device instead of trapping.  This call
+ * synchronises `stream`, returns KDA_ERR_TIMEOUT if any kernel recorded such
+ * an event since the previous call (else KDA_OK), and resets the word.
+ * KDA_ERR_CUDA if the synchronisation itself fails.
+ */
+kda_status kda_get_last_device_error(kda_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *kda_status_string(kda_status status);
 

@@ -63,6 +63,13 @@ const char *kda_last_cuda_error(void) { return g_last_cuda_error; }
 
 int32_t kda_version(void) { return 100; /* 0.1.0 */ }
 
+kda_status kda_get_last_device_error(kda_stream_t stream) {
+    unsigned status = 0;
+    cudaError_t e = kda_read_device_status((cudaStream_t)stream, &status);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_get_last_device_error");
+    return status ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
 kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const void *v,
                        const float *g, const float *beta, const float *init_state,
                        const int32_t *cu_seqlens, void *out, float *final_state,
@@ -82,11 +89,15 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
         const size_t bytes = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
         if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;
     }
-    if (P.variant == KDA_PREFILL_TC) return KDA_ERR_UNSUPPORTED;
+    const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, g);
+    if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens, out,
-                                            final_state, s);
+    const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
+    cudaError_t e = use_tc ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,
+                                                   out, final_state, s)
+                           : kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens,
+                                                     out, final_state, s);
     if (e != cudaSuccess) return cuda_fail(e, "kda_prefill");
     return KDA_OK;
 }
