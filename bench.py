@@ -287,6 +287,8 @@ def run_gpu(args):
 
     stream = torch.cuda.current_stream()
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    if args.profile:
+        return run_profile_case(args, kda, synth, dev, stream)
 
     # ---------------- prefill (headline) ----------------
     w = synth.WORKLOADS["prefill_8k"]
@@ -391,12 +393,50 @@ def run_gpu(args):
     return 0
 
 
+def run_profile_case(args, kda, synth, dev, stream):
+    """A reduced run for profilers: only one kernel family, a smaller prefill
+    (same recipe, --tokens tokens, all 96 heads) or fewer decode sequences;
+    W warm-up launches, then K launches.  Prints one short JSON line (not a
+    benchmark result)."""
+    import torch
+    if args.profile == "prefill":
+        w = synth.WORKLOADS["prefill_8k"]
+        inp = synth.prefill_inputs(w, dev, lengths=(args.tokens,))
+        out = torch.empty((args.tokens, w.heads, w.d), dtype=w.dtype, device=dev)
+        fin = torch.empty((1, w.heads, w.d, w.d), dtype=torch.float32, device=dev)
+
+        def step():
+            kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                            cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
+                            variant=args.variant, stream=stream)
+        units = args.tokens
+    else:
+        wd = synth.WORKLOADS["decode_256x64"]
+        dx = synth.decode_inputs(wd, dev, num_seqs=args.seqs, steps=1)
+        state = dx["state"]
+        dout = torch.empty((args.seqs, wd.heads, wd.d), dtype=wd.dtype, device=dev)
+
+        def step():
+            kda.kda_decode(dx["q"][0], dx["k"][0], dx["v"][0], dx["g"][0], dx["beta"][0], state,
+                           out=dout, stream=stream)
+        units = args.seqs
+    ms, _, _ = time_steps(step, args.steps, args.warmup, 1, stream)
+    print(json.dumps({"profile_case": args.profile, "units": units, "ms_per_launch": ms,
+                      "note": "profiling run, not a benchmark result"}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run only one kernel family on a reduced case (for ncu)")
+    ap.add_argument("--tokens", type=int, default=2048, help="--profile prefill: tokens")
+    ap.add_argument("--seqs", type=int, default=64, help="--profile decode: sequences")
+    ap.add_argument("--variant", type=int, default=0, help="prefill kernel variant (0 default)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
