@@ -5,8 +5,8 @@
 // between chunks; "Hybrid Attention", section "But isn't a recurrent update
 // sequential?": a triangular solve resolves the in-chunk dependencies):
 //
-//   T   = (I + Akk)^{-1},  W = T diag(beta)(gamma . K),  U' = T diag(beta) V
-//   U   = U' - W S0
+//   T   = (I + Akk)^{-1}
+//   U   = T diag(beta) V - T diag(beta) (gamma . K) S0        (= U' - ...)
 //   O   = (gamma . Q) S0 + Aqk U
 //   S_C = Diag(gamma_last) S0 + Kbar^T U,   Kbar_r = e^{Gamma_last - Gamma_r} . k_r
 //
@@ -19,11 +19,16 @@
 // readout GEMM straight from TMEM and accumulates its own update in place.
 //
 // Warp specialisation.  Warps 0-7 prepare chunk n (decay prefix, decay-
-// weighted operands, Gram MMA, triangular solve, W and U' MMAs) while warps
-// 8-15 run the state chain of chunk n-1 (readout MMA, U = U' - W S and the
-// state decay, intra-chunk readout and state-carry MMAs, output store).  The
-// two groups hand buffers to each other through mbarriers; every wait is
-// bounded.
+// weighted operands, Gram MMA, triangular solve, U' = T diag(beta) V) while
+// warps 8-11 run the state chain of chunk n-1: the readout MMA
+// X = S^T [gamma Q; gamma K]^T, the U MMA that subtracts (gamma K S) T diag(beta)
+// with the X accumulator itself as A operand, the state decay, and one MMA
+// group for the intra-chunk readout and the state carry together, then the
+// output store.  The two groups hand buffers to each other through mbarriers;
+// every wait is bounded.  A tcgen05.mma costs a roughly fixed time per
+// instruction on these shapes, so the formulation minimises the instruction
+// count: 16 for the Gram and 16 for the readout (K = d_k = 128), 4 each for
+// U', U and the readout + state-carry group.
 // tf32 (not bf16) operands: on these inputs the intermediate u_t and the
 // intra-chunk terms are several times larger than o_t, and bf16 operand
 // rounding alone costs more than the 2e-2 error budget; tf32 keeps it near
@@ -42,7 +47,7 @@
 //   rows  0..31 : k_r e^{Gamma_r - ref(r)}     rows 32..63: q_r e^{Gamma_r - ref(r)}
 //   cols  0..15 : k_i e^{0 - Gamma_i}          (i in sub-tile 0, reference 0)
 //   cols 16..47 : k_i e^{Gamma_15 - Gamma_i}   (i = 0..31,   reference Gamma_15)
-// (the A operand is 128 rows; rows 64..127 alias the next buffer and their
+// (the A operand sits in TMEM lanes 0-63; lanes 64-127 are not used and their
 // results are ignored).
 
 #include <mutex>
@@ -58,61 +63,92 @@ using namespace sm100;
 
 constexpr int C = 32;        // tokens per chunk
 constexpr int D = 128;       // d_k = d_v
-constexpr int kPrep = 256;   // threads of the chunk-preparation warps (warps 0-7)
-constexpr int kChain = 256;  // threads of the state-chain warps (warps 8-15)
+constexpr int kPrep = 256;   // chunk-preparation threads (warps 0-7)
+constexpr int kChain = 128;  // state-chain threads (warps 8-11; thread j <-> TMEM lane j)
 constexpr int kThreads = kPrep + kChain;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPollLimit = 1u << 23;  // about half a second of polling per wait
 
-// named barriers (0 is __syncthreads)
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_WG0 = 3;
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_SOLVE = 3;  // named barriers
 
 // tensor-memory columns
-constexpr uint32_t TM_S = 0;     // S^T (lanes = value index, columns = key channel), fp32 state
-constexpr uint32_t TM_X = 128;   // two buffers of 64: [(W S)^T | (gamma Q S)^T -> O^T]
-constexpr uint32_t TM_U = 256;   // two buffers of 32: U'^T, then U^T
-constexpr uint32_t TM_W = 320;   // W^T (lanes = key channel)
-constexpr uint32_t TM_G = 352;   // Gram, 48 columns
-constexpr uint32_t TM_BGK = 400; // (beta gamma k)^T: lanes = key channel, columns = token
-constexpr uint32_t TM_BV = 432;  // (beta v)^T: lanes = value index, columns = token
+constexpr uint32_t TM_S = 0;     // 128: S^T (lanes = value index, columns = key channel)
+constexpr uint32_t TM_X = 128;   // 64: [(gamma Q S)^T, then O^T | (gamma K S)^T]
+constexpr uint32_t TM_U = 192;   // 2 x 32: U'^T, then U^T, per chunk parity
+constexpr uint32_t TM_BV = 256;  // 32: V^T, A operand of the U' MMA
+constexpr uint32_t TM_G = 288;   // 48: Gram
+constexpr uint32_t TM_GA = 384;  // 128: Gram A operand, lanes 0-31 k~, 32-63 q~
 
-constexpr uint32_t kStageBytes = C * D * (2 + 2 + 2 + 4);
+constexpr uint32_t kTileBf16 = C * D * 2;
+constexpr uint32_t kTileF32 = C * D * 4;
+constexpr uint32_t kStageBytes = 3 * kTileBf16 + kTileF32;
+
+// Input tiles arrive by TMA with the 128-byte swizzle: a bf16 tile is two
+// 4 KB halves (32 rows x 64 elements), an fp32 tile four 4 KB quarters (32
+// rows x 32 elements); the 16-byte chunk ch of row r sits at chunk position
+// ch ^ (r % 8).  Rows of a warp then fall in distinct banks whether a warp
+// walks along a row, down a column, or over 4-element blocks.
+__device__ __forceinline__ uint32_t off_bf16(int r, int c) {
+    return (uint32_t)((c >> 6) * 4096 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1));
+}
+__device__ __forceinline__ uint32_t off_f32(int r, int c) {
+    return (uint32_t)((c >> 5) * 4096 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
+}
 
 struct Stage {
-    __nv_bfloat16 q[C * D];
-    __nv_bfloat16 k[C * D];
-    __nv_bfloat16 v[C * D];
-    float g[C * D];  // g, then Gamma in place
+    unsigned char q[kTileBf16];
+    unsigned char k[kTileBf16];
+    unsigned char v[kTileBf16];
+    unsigned char g[kTileF32];  // g, then Gamma in place
 };
 
 struct alignas(1024) TcSmem {
-    Stage in[2];               // TMA destinations, dense row-major [C][D], double-buffered
-    float gramA[4 * 64 * 32];  // Gram A operand (tf32, SW128): rows 0-31 k~, 32-63 q~;
-                               // also fp32 scratch of the triangular solve
-    float gramB[4 * 48 * 32];  // Gram B operand; its first 8 KB are read as rows 64-127 of gramA
-    float bX[4 * 64 * 32];     // readout B operand [W ; gamma q] (single buffer)
-    float kbT[2][D * 32];      // Kbar^T (state-carry B operand), per chunk parity
-    float aqk[2][32 * 32];     // Aqk (intra-chunk readout B operand), per chunk parity
-    float tmat[32 * 32];       // T = (I + Akk)^{-1} (B operand of the W / U' MMAs)
-    float akk[32][33];
-    float beta[C];
-    float gref[D], e01[D], glast[D];
-    float gamC[2][D];          // e^{Gamma_last}, per chunk parity (state decay of the chain)
-    uint64_t bar_tma[2], bar_gram, bar_wu, bar_bxfull, bar_bxempty, bar_x, bar_s;
-    uint64_t bar_akempty[2], bar_xfree[2];
+    Stage in[2];                // TMA destinations, double-buffered
+    float gramB[4 * 48 * 32];   // Gram B operand; after the Gram MMA, fp32 scratch of the solve
+    float e1t[C * D];           // e^{Gamma - ref}, fp32, laid out like an fp32 input tile
+    float bX[4 * 64 * 32];      // readout B operand [gamma q ; gamma k] (single buffer)
+    float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
+    float tmat[2][32 * 32];     // T diag(beta), B operand of the U' MMA
+    float tneg[2][32 * 32];     // -T diag(beta), B operand of the U MMA
+    float betaS[2][C];
+    float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
+    float gref[D], e01[D], e1l[D], glast[D];
+    uint64_t bar_tma[2], bar_gram, bar_bxfull, bar_bxempty, bar_x, bar_u, bar_s;
+    uint64_t bar_up[2];        // U' MMA of the chunk with that parity is complete
+    uint64_t bar_akempty[2];
     uint32_t tmem_base;
     int abort;
 };
 
+// Stores into K-major SW128 operand blocks (plain C++ stores, so the
+// compiler can schedule around them; fence.proxy.async orders them before the
+// MMAs that read them).
 __device__ __forceinline__ void st_op(float *blk, int row, int k, float x) {
     *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(blk) + sw128_off32(row, k)) =
         to_tf32(x);
 }
-// 16-byte store of the four consecutive-k elements k4*4 .. k4*4+3 of `row`.
+// 16-byte store of the elements 4*k4 .. 4*k4+3 of `row`.
 __device__ __forceinline__ void st_op4(float *blk, int row, int k4, float a, float b, float c,
                                        float d) {
-    const uint32_t addr = smem_u32(blk) + (uint32_t)(row * 128 + (((k4 ^ row) & 7) << 4));
-    st_shared_v4(addr, to_tf32(a), to_tf32(b), to_tf32(c), to_tf32(d));
+    *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(blk) + row * 128 +
+                                (((k4 ^ row) & 7) << 4)) =
+        make_float4(to_tf32(a), to_tf32(b), to_tf32(c), to_tf32(d));
+}
+__device__ __forceinline__ float4 ld_f32x4(const void *tile, int r, int c) {
+    return *reinterpret_cast<const float4 *>(reinterpret_cast<const unsigned char *>(tile) +
+                                             off_f32(r, c));
+}
+__device__ __forceinline__ void ld_bf16x4(const unsigned char *tile, int r, int c, float (&x)[4]) {
+    const uint2 raw = *reinterpret_cast<const uint2 *>(tile + off_bf16(r, c));
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+    x[0] = __low2float(a);
+    x[1] = __high2float(a);
+    x[2] = __low2float(b);
+    x[3] = __high2float(b);
+}
+__device__ __forceinline__ float ld_bf16(const unsigned char *tile, int r, int c) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off_bf16(r, c)));
 }
 
 __device__ __forceinline__ void issue_stage_loads(Stage &st, uint64_t *bar, const CUtensorMap *mq,
@@ -120,13 +156,16 @@ __device__ __forceinline__ void issue_stage_loads(Stage &st, uint64_t *bar, cons
                                                   const CUtensorMap *mg, int h, int64_t t0) {
     mbar_arrive_expect_tx(bar, kStageBytes);
     const int x = h * D, y = (int)t0;
-    tma_load_2d(st.q, mq, bar, x, y);
-    tma_load_2d(st.k, mk, bar, x, y);
-    tma_load_2d(st.v, mv, bar, x, y);
-    tma_load_2d(st.g, mg, bar, x, y);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        tma_load_2d(st.q + half * 4096, mq, bar, x + 64 * half, y);
+        tma_load_2d(st.k + half * 4096, mk, bar, x + 64 * half, y);
+        tma_load_2d(st.v + half * 4096, mv, bar, x + 64 * half, y);
+    }
+#pragma unroll
+    for (int qtr = 0; qtr < 4; ++qtr) tma_load_2d(st.g + qtr * 4096, mg, bar, x + 32 * qtr, y);
 }
 
-// Bounded wait; on timeout raise the CTA abort flag and the device status.
 __device__ __forceinline__ bool wait_phase(TcSmem &sm, uint64_t *bar, uint32_t parity,
                                            unsigned code) {
     if (!mbar_wait_bounded(bar, parity, kPollLimit)) {
@@ -142,27 +181,30 @@ __device__ __forceinline__ bool aborted(TcSmem &sm) {
 
 // ---------------------------------------------------------------------------
 // Preparation warps (0-7): everything of chunk n that does not depend on the
-// state -- decay prefix, decay-weighted operands, Gram matrices, the
-// triangular solve, W and U' -- done while the chain warps run chunk n-1.
+// state, done while the chain warps run chunk n-1.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mg,
                                           const float *__restrict__ beta, int H, int h, int64_t a,
                                           int64_t b, int nchunks, uint32_t tb) {
-    const int p = threadIdx.x;            // 0..255
-    const int warp = p >> 5, lane = p & 31;
-    const bool wg0 = p < 128;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0};
-    uint32_t gram_par = 0, wu_par = 0, bxe_par = 0;
-    // in-flight bookkeeping for the abort path (valid in the thread that gave up)
-    bool pend_tma[2] = {false, false}, pend_gram = false, pend_wu = false;
+    const int P = threadIdx.x;  // 0..255
+    const int warp = P >> 5, lane = P & 31, qd = warp & 3, wg = warp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, up_par[2] = {0, 0}, gram_par = 0, bxe_par = 0;
+    bool pend_tma[2] = {false, false}, pend_gram = false;
     uint32_t pend_tma_par[2] = {0, 0};
+    const bool beta_thread = P >= 128 && P < 128 + C;
 
-    if (p == 0) {
+    // beta of chunk 0 (asynchronous 4-byte copies; rows past the end are 0)
+    if (beta_thread) {
+        const int r = P - 128;
+        if (nchunks > 0 && a + r < b) cp_async4(&sm.betaS[0][r], beta + (a + r) * H + h);
+        else sm.betaS[0][r] = 0.f;
+        cp_async_commit();
+    }
+    if (P == 0)
         for (int s = 0; s < 2 && s < nchunks; ++s)
             issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C);
-    }
     __syncwarp();
     for (int s = 0; s < 2; ++s) pend_tma[s] = s < nchunks;
 
@@ -172,147 +214,219 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         const int L = (int)((b - t0) < C ? (b - t0) : C);
         Stage &in = sm.in[st];
 
-        // chunk n-2 (same parity) must be finished by the chain before its
-        // aqk / kbT / gamC / U buffers are overwritten
+        // the chain must be done with chunk n-2 (same parity) before its
+        // buffers (kbaq, tmat, tneg, gamC, TMEM U) are overwritten
         if (n >= 2) {
             wait_phase(sm, &sm.bar_akempty[st], ake_par[st], 32u);
             ake_par[st] ^= 1u;
         }
         if (wait_phase(sm, &sm.bar_tma[st], tma_par[st], 1u)) pend_tma[st] = false;
         tma_par[st] ^= 1u;
+        if (beta_thread) {
+            cp_async_wait_all();   // beta of chunk n has landed
+            const int r = P - 128;
+            const int64_t tn = t0 + C + r;
+            if (n + 1 < nchunks && tn < b) cp_async4(&sm.betaS[st ^ 1][r], beta + tn * H + h);
+            else sm.betaS[st ^ 1][r] = 0.f;
+            cp_async_commit();
+        }
         if (named_sync_or(BAR_PREP, kPrep, aborted(sm))) break;
 
-        // ---- a1: Gamma (running sum of g per key channel), beta ----
-        if (wg0) {
-            const int c = p;
-            float run = 0.f, g15 = 0.f;
+        // ---- a1: Gamma = running sum of g per key channel (all loads first) ----
+        if (P < D) {
+            const int c = P;
+            float *g = reinterpret_cast<float *>(in.g);
+            float gv[C];
+#pragma unroll
+            for (int r = 0; r < C; ++r) gv[r] = g[off_f32(r, c) >> 2];
+            float run = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                run += r < L ? in.g[r * D + c] : 0.f;
-                in.g[r * D + c] = run;
-                if (r == 15) g15 = run;
+                run += r < L ? gv[r] : 0.f;
+                gv[r] = run;
             }
+#pragma unroll
+            for (int r = 0; r < C; ++r) g[off_f32(r, c) >> 2] = gv[r];
+            const float g15 = gv[15], gl = gv[C - 1];
             sm.gref[c] = g15;
             sm.e01[c] = __expf(g15);
-            sm.glast[c] = run;
-            sm.gamC[st][c] = __expf(run);
-        } else if (p < 128 + C) {
-            const int r = p - 128;
-            sm.beta[r] = r < L ? beta[(t0 + r) * H + h] : 0.f;
+            sm.e1l[c] = __expf(gl - g15);
+            sm.glast[c] = gl;
+            sm.gamC[st][c] = __expf(gl);
         }
         named_sync(BAR_PREP, kPrep);
 
-        // ---- a2: Gram operands, 4 tokens x 4 channels per thread ----
-        // (warp w: tokens 4w..4w+3; lane: channels 4*lane..4*lane+3)
+        // ---- a2: e^{Gamma - ref} once per element, the key variants of the Gram, V^T ----
         {
-            const int cb = lane, c0 = 4 * cb, kb = cb >> 3, k4 = cb & 7;
-            const float4 gref4 = *reinterpret_cast<const float4 *>(&sm.gref[c0]);
-            const float4 e014 = *reinterpret_cast<const float4 *>(&sm.e01[c0]);
-            float *gA = sm.gramA + kb * 64 * 32;
-            float *gB = sm.gramB + kb * 48 * 32;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = 4 * warp + i;
+            for (int it = 0; it < 4; ++it) {
+                const int u = P + 256 * it, r = u >> 5, cb = u & 31, c = 4 * cb;
                 const bool live = r < L, sub1 = r >= 16;
-                const float4 G = *reinterpret_cast<const float4 *>(&in.g[r * D + c0]);
-                const uint2 kraw = *reinterpret_cast<const uint2 *>(&in.k[r * D + c0]);
-                const uint2 qraw = *reinterpret_cast<const uint2 *>(&in.q[r * D + c0]);
-                const __nv_bfloat162 k01 = *reinterpret_cast<const __nv_bfloat162 *>(&kraw.x);
-                const __nv_bfloat162 k23 = *reinterpret_cast<const __nv_bfloat162 *>(&kraw.y);
-                const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162 *>(&qraw.x);
-                const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162 *>(&qraw.y);
-                float kv[4] = {__low2float(k01), __high2float(k01), __low2float(k23), __high2float(k23)};
-                float qv[4] = {__low2float(q01), __high2float(q01), __low2float(q23), __high2float(q23)};
-                const float gv[4] = {G.x, G.y, G.z, G.w};
-                const float rf[4] = {gref4.x, gref4.y, gref4.z, gref4.w};
-                const float ef[4] = {e014.x, e014.y, e014.z, e014.w};
-                float ka[4], qa[4], kinv[4], kinv1[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (!live) { kv[j] = 0.f; qv[j] = 0.f; }
-                    const float e1 = __expf(gv[j] - (sub1 ? rf[j] : 0.f));  // [e^-80, 1]
-                    const float inv = __frcp_rn(e1);                         // [1, e^80]
-                    ka[j] = kv[j] * e1;
-                    qa[j] = qv[j] * e1;
-                    kinv[j] = kv[j] * inv;
-                    kinv1[j] = kinv[j] * ef[j];
-                }
-                st_op4(gA, r, k4, ka[0], ka[1], ka[2], ka[3]);
-                st_op4(gA, 32 + r, k4, qa[0], qa[1], qa[2], qa[3]);
+                const float4 G = ld_f32x4(in.g, r, c);
+                const float4 ref = sub1 ? *reinterpret_cast<const float4 *>(&sm.gref[c])
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 e1 = make_float4(__expf(G.x - ref.x), __expf(G.y - ref.y),
+                                              __expf(G.z - ref.z), __expf(G.w - ref.w));
+                *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(sm.e1t) +
+                                            off_f32(r, c)) = e1;
+                float x[4];
+                ld_bf16x4(in.k, r, c, x);
+                const float s = live ? 1.f : 0.f;
+                const float k0 = s * __fdividef(x[0], e1.x), k1 = s * __fdividef(x[1], e1.y),
+                            k2 = s * __fdividef(x[2], e1.z),
+                            k3 = s * __fdividef(x[3], e1.w);   // k e^{ref - Gamma}
+                float *blk = sm.gramB + (cb >> 3) * 48 * 32;
                 if (!sub1) {
-                    st_op4(gB, r, k4, kinv[0], kinv[1], kinv[2], kinv[3]);
-                    st_op4(gB, 16 + r, k4, kinv1[0], kinv1[1], kinv1[2], kinv1[3]);
+                    const float4 e = *reinterpret_cast<const float4 *>(&sm.e01[c]);
+                    st_op4(blk, r, cb & 7, k0, k1, k2, k3);
+                    st_op4(blk, 16 + r, cb & 7, k0 * e.x, k1 * e.y, k2 * e.z, k3 * e.w);
                 } else {
-                    st_op4(gB, 16 + r, k4, kinv[0], kinv[1], kinv[2], kinv[3]);
+                    st_op4(blk, 16 + r, cb & 7, k0, k1, k2, k3);
                 }
             }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-        named_sync(BAR_PREP, kPrep);
-        if (p == 0) {
-            tc_fence_after();
-            const uint32_t aA = smem_u32(sm.gramA), aB = smem_u32(sm.gramB);
-#pragma unroll 1
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t da = sdesc_sw128(aA + (kk >> 2) * (64 * 128) + (kk & 3) * 32);
-                const uint64_t db = sdesc_sw128(aB + (kk >> 2) * (48 * 128) + (kk & 3) * 32);
-                mma_tf32_ss(tb + TM_G, da, db, idesc_tf32(128, 48), kk > 0);
+        if (wg == 1) {
+            // V^T into TMEM (thread = value index); the U' MMA of chunk n-1 must be done with it
+            if (n >= 1) {
+                wait_phase(sm, &sm.bar_up[st ^ 1], up_par[st ^ 1], 8u);
+                up_par[st ^ 1] ^= 1u;
             }
-            mma_commit(&sm.bar_gram);
-        }
-        __syncwarp();   // reconverge warp 0 before its warp-collective tcgen05 operations
-        pend_gram = true;
-
-        if (wg0) {
-            // ---- (beta gamma k)^T into TMEM: thread = key channel, 32 tokens ----
-            const int c = p;
+            const int j = P - 128;
             float v0[16], v1[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                const float kv = r < L ? __bfloat162float(in.k[r * D + c]) : 0.f;
-                v0[r] = to_tf32(sm.beta[r] * __expf(in.g[r * D + c]) * kv);
-                const int r1 = 16 + r;
-                const float kv1 = r1 < L ? __bfloat162float(in.k[r1 * D + c]) : 0.f;
-                v1[r] = to_tf32(sm.beta[r1] * __expf(in.g[r1 * D + c]) * kv1);
+                v0[r] = r < L ? ld_bf16(in.v, r, j) : 0.f;
+                v1[r] = 16 + r < L ? ld_bf16(in.v, 16 + r, j) : 0.f;
             }
-            tmem_st16(tb + lane_off + TM_BGK, v0);
-            tmem_st16(tb + lane_off + TM_BGK + 16, v1);
+            tmem_st16(tb + lane_off + TM_BV, v0);
+            tmem_st16(tb + lane_off + TM_BV + 16, v1);
             tmem_wait_st();
             tc_fence_before();
+        }
+        named_sync(BAR_PREP, kPrep);
 
-            // ---- Gram -> Akk (strict, beta rows) and Aqk (inclusive) ----
+        // ---- a3: Gram A operand into TMEM (quadrants 0,1); Kbar^T (quadrants 2,3) ----
+        if (qd < 2) {
+            const int r = lane;
+            const bool live = r < L;
+            const unsigned char *src = qd == 0 ? in.k : in.q;
+            const int c_lo = 64 * wg, nblk = 4;
+            for (int blk = 0; blk < nblk; ++blk) {
+                const int c0 = c_lo + 16 * blk;
+                float vals[16];
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const int c = c0 + 4 * j4;
+                    const float4 E = ld_f32x4(sm.e1t, r, c);
+                    float x[4];
+                    ld_bf16x4(src, r, c, x);
+                    vals[4 * j4 + 0] = to_tf32(live ? x[0] * E.x : 0.f);
+                    vals[4 * j4 + 1] = to_tf32(live ? x[1] * E.y : 0.f);
+                    vals[4 * j4 + 2] = to_tf32(live ? x[2] * E.z : 0.f);
+                    vals[4 * j4 + 3] = to_tf32(live ? x[3] * E.w : 0.f);
+                }
+                tmem_st16(tb + lane_off + TM_GA + c0, vals);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+        } else {
+            const int kt = (wg * 2 + (qd - 2)) * 32 + lane;   // 0..127
+            {
+                const int c = kt;
+                const float gl = sm.glast[c];
+                const float *g = reinterpret_cast<const float *>(in.g);
+                float *kb = sm.kbaq[st];
+#pragma unroll
+                for (int r4 = 0; r4 < 8; ++r4) {
+                    float kbar[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int r = 4 * r4 + m;
+                        kbar[m] = r < L ? ld_bf16(in.k, r, c) * __expf(gl - g[off_f32(r, c) >> 2]) : 0.f;
+                    }
+                    st_op4(kb, c, r4, kbar[0], kbar[1], kbar[2], kbar[3]);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        named_sync(BAR_PREP, kPrep);
+        if (P == 0) {
+            tc_fence_after();
+            const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_tf32_ts(tb + TM_G, tb + TM_GA + kk * 8,
+                            dB + (uint64_t)(((kk >> 2) * (48 * 128) + (kk & 3) * 32) >> 4),
+                            idesc_tf32(128, 48), kk > 0);
+            mma_commit(&sm.bar_gram);
+        }
+        __syncwarp();
+        pend_gram = true;
+
+        // ---- readout operand [gamma q ; gamma k] (warps 4-11), while the Gram runs ----
+        {
+            if (n >= 1) {   // single buffer: the readout MMA of chunk n-1 must be done with it
+                wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
+                bxe_par ^= 1u;
+            }
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int u = P + 256 * it, r = u >> 5, cb = u & 31, c = 4 * cb;
+                const float s = r < L ? 1.f : 0.f;
+                float4 gm = ld_f32x4(sm.e1t, r, c);   // e^{Gamma}: e1 times e^{ref}
+                if (r >= 16) {
+                    const float4 e = *reinterpret_cast<const float4 *>(&sm.e01[c]);
+                    gm.x *= e.x; gm.y *= e.y; gm.z *= e.z; gm.w *= e.w;
+                }
+                float kx[4], qx[4];
+                ld_bf16x4(in.k, r, c, kx);
+                ld_bf16x4(in.q, r, c, qx);
+                float *blk = sm.bX + (cb >> 3) * 64 * 32;
+                st_op4(blk, r, cb & 7, s * qx[0] * gm.x, s * qx[1] * gm.y, s * qx[2] * gm.z,
+                       s * qx[3] * gm.w);
+                st_op4(blk, 32 + r, cb & 7, s * kx[0] * gm.x, s * kx[1] * gm.y, s * kx[2] * gm.z,
+                       s * kx[3] * gm.w);
+            }
+            fence_proxy_async_smem();
+        }
+
+        // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram ----
+        float(*akk)[33] = reinterpret_cast<float(*)[33]>(sm.gramB);
+        if (warp < 2) {
             if (wait_phase(sm, &sm.bar_gram, gram_par, 2u)) pend_gram = false;
             gram_par ^= 1u;
             tc_fence_after();
-            if (warp < 2) {
-                float d0[16], d1[16], d2[16];
-                tmem_ld16x2(tb + lane_off + TM_G, tb + lane_off + TM_G + 16, d0, d1);
-                tmem_ld16(tb + lane_off + TM_G + 32, d2);
-                const int r = lane;
-                if (warp == 0) {
-                    const float br = sm.beta[r];
+            float d0[16], d1[16], d2[16];
+            tmem_ld16x2(tb + lane_off + TM_G, tb + lane_off + TM_G + 16, d0, d1);
+            tmem_ld16(tb + lane_off + TM_G + 32, d2);
+            const int r = lane;
+            if (warp == 0) {
+                const float br = sm.betaS[st][r];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
-                        sm.akk[r][i] = i < r ? br * val : 0.f;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
-                        st_op(sm.aqk[st], r, i, i <= r ? val : 0.f);
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
+                    akk[r][i] = i < r ? br * val : 0.f;
                 }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
+                    st_op(sm.kbaq[st], 128 + r, i, i <= r ? val : 0.f);
+                }
+                fence_proxy_async_smem();
             }
             tc_fence_before();
-            named_sync(BAR_WG0, 128);
+        }
+        named_sync(BAR_PREP, kPrep);
 
-            // ---- T = (I + Akk)^{-1}, blocked 2 x 2 over 16-token sub-tiles ----
-            float(*Tm)[33] = reinterpret_cast<float(*)[33]>(sm.gramA);           // fp32 T
-            float(*Y)[17] = reinterpret_cast<float(*)[17]>(sm.gramA + 32 * 33);   // A10 T00
-            if (warp == 0) {
-                // diagonal blocks: lanes 0-15 -> columns of T00, lanes 16-31 -> columns of T11
-                const int base = lane < 16 ? 0 : 16, col = lane & 15;
+        // ---- T = (I + Akk)^{-1}, blocked 2 x 2 over 16-token sub-tiles (warps 0-3) ----
+        if (wg == 0) {
+            float(*Tm)[33] = reinterpret_cast<float(*)[33]>(sm.gramB + 32 * 33);
+            float(*Y)[17] = reinterpret_cast<float(*)[17]>(sm.gramB + 2 * 32 * 33);
+            if (warp < 2) {
+                // diagonal blocks by forward substitution: warp 0 -> T00, warp 1 -> T11
+                const int base = 16 * warp, col = lane & 15;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) x[r] = r == col ? 1.f : 0.f;
@@ -320,135 +434,58 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 for (int m = 0; m < 15; ++m) {
                     const float xm = x[m];
 #pragma unroll
-                    for (int r = m + 1; r < 16; ++r) x[r] -= sm.akk[base + r][base + m] * xm;
+                    for (int r = m + 1; r < 16; ++r) x[r] -= akk[base + r][base + m] * xm;
                 }
+                if (lane < 16) {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    Tm[base + r][base + col] = x[r];
-                    Tm[base + r][16 - base + col] = 0.f;   // upper off-diagonal block / placeholder
-                }
-            }
-            named_sync(BAR_WG0, 128);
-            {   // Y = A10 T00   (A10 = Akk[16..31][0..15]); 256 entries, 2 per thread
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int idx = p + 128 * e, i = idx >> 4, j = idx & 15;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) acc += sm.akk[16 + i][m] * Tm[m][j];
-                    Y[i][j] = acc;
+                    for (int r = 0; r < 16; ++r) {
+                        Tm[base + r][base + col] = x[r];
+                        if (warp == 0) Tm[r][16 + col] = 0.f;
+                    }
                 }
             }
-            named_sync(BAR_WG0, 128);
-            {   // T10 = -T11 Y
+            named_sync(BAR_SOLVE, 128);
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int idx = p + 128 * e, i = idx >> 4, j = idx & 15;
-                    float acc = 0.f;
+            for (int e = 0; e < 2; ++e) {   // Y = A10 T00
+                const int idx = P + 128 * e, i = idx >> 4, j = idx & 15;
+                float acc = 0.f;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) acc += Tm[16 + i][16 + m] * Y[m][j];
-                    Tm[16 + i][j] = -acc;
-                }
+                for (int m = 0; m < 16; ++m) acc += akk[16 + i][m] * Tm[m][j];
+                Y[i][j] = acc;
             }
-            named_sync(BAR_WG0, 128);
-            {   // T into its tf32 operand: thread -> row p / 4, 8 consecutive columns
-                const int r = p >> 2, c0 = (p & 3) * 8;
-                st_op4(sm.tmat, r, c0 >> 2, Tm[r][c0], Tm[r][c0 + 1], Tm[r][c0 + 2], Tm[r][c0 + 3]);
-                st_op4(sm.tmat, r, (c0 >> 2) + 1, Tm[r][c0 + 4], Tm[r][c0 + 5], Tm[r][c0 + 6],
-                       Tm[r][c0 + 7]);
+            named_sync(BAR_SOLVE, 128);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {   // T10 = -T11 Y
+                const int idx = P + 128 * e, i = idx >> 4, j = idx & 15;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc += Tm[16 + i][16 + m] * Y[m][j];
+                Tm[16 + i][j] = -acc;
+            }
+            named_sync(BAR_SOLVE, 128);
+            {   // T diag(beta) and its negative, as tf32 operands
+                const int r = P >> 2, c0 = (P & 3) * 8;
+                float tb8[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * sm.betaS[st][c0 + m];
+                st_op4(sm.tmat[st], r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
+                st_op4(sm.tmat[st], r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
+                st_op4(sm.tneg[st], r, c0 >> 2, -tb8[0], -tb8[1], -tb8[2], -tb8[3]);
+                st_op4(sm.tneg[st], r, (c0 >> 2) + 1, -tb8[4], -tb8[5], -tb8[6], -tb8[7]);
             }
             fence_proxy_async_smem();
-        } else {
-            // ---- (beta v)^T into TMEM and Kbar^T into smem: thread = channel ----
-            const int c = p - 128;
-            float v0[16], v1[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                v0[r] = to_tf32(r < L ? sm.beta[r] * __bfloat162float(in.v[r * D + c]) : 0.f);
-                const int r1 = 16 + r;
-                v1[r] = to_tf32(r1 < L ? sm.beta[r1] * __bfloat162float(in.v[r1 * D + c]) : 0.f);
-            }
-            tmem_st16(tb + lane_off + TM_BV, v0);
-            tmem_st16(tb + lane_off + TM_BV + 16, v1);
-            const float gl = sm.glast[c];
-            float *kb = sm.kbT[st];
-#pragma unroll
-            for (int r4 = 0; r4 < 8; ++r4) {
-                float kbar[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = 4 * r4 + j;
-                    const float kv = r < L ? __bfloat162float(in.k[r * D + c]) : 0.f;
-                    kbar[j] = kv * __expf(gl - in.g[r * D + c]);   // e^{Gamma_last - Gamma_r} <= 1
-                }
-                st_op4(kb, c, r4, kbar[0], kbar[1], kbar[2], kbar[3]);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            // gamma q rows of the readout operand: bX is single-buffered, so wait
-            // for the readout MMA of chunk n-1 to have consumed it
-            if (n >= 1) {
-                wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
-                bxe_par ^= 1u;
-            }
-            const int q_ = c, cb = q_ & 31, c0 = 4 * cb, kb4 = cb >> 3, k4 = cb & 7;
-            float *blk = sm.bX + kb4 * 64 * 32;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * (q_ >> 5) + i;
-                const bool live = r < L;
-                const float4 G = *reinterpret_cast<const float4 *>(&in.g[r * D + c0]);
-                const uint2 qraw = *reinterpret_cast<const uint2 *>(&in.q[r * D + c0]);
-                const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162 *>(&qraw.x);
-                const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162 *>(&qraw.y);
-                const float s = live ? 1.f : 0.f;
-                st_op4(blk, 32 + r, k4, s * __low2float(q01) * __expf(G.x),
-                       s * __high2float(q01) * __expf(G.y), s * __low2float(q23) * __expf(G.z),
-                       s * __high2float(q23) * __expf(G.w));
-            }
-            fence_proxy_async_smem();
-        }
-        named_sync(BAR_PREP, kPrep);
-
-        // ---- W^T = (beta gamma K)^T T^T ; U'^T = (beta V)^T T^T (A operands in TMEM) ----
-        if (p == 0) {
-            tc_fence_after();
-            const uint32_t aT = smem_u32(sm.tmat);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                mma_tf32_ts(tb + TM_W, tb + TM_BGK + kk * 8, sdesc_sw128(aT + kk * 32),
-                            idesc_tf32(128, 32), kk > 0);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                mma_tf32_ts(tb + TM_U + 32 * st, tb + TM_BV + kk * 8, sdesc_sw128(aT + kk * 32),
-                            idesc_tf32(128, 32), kk > 0);
-            mma_commit(&sm.bar_wu);
-        }
-        __syncwarp();
-        pend_wu = true;
-        if (wg0) {
-            if (wait_phase(sm, &sm.bar_wu, wu_par, 8u)) pend_wu = false;
-            wu_par ^= 1u;
-            tc_fence_after();
-            if (n >= 1) {   // bX single-buffered (see above)
-                wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
-                bxe_par ^= 1u;
-            }
-            // W rows (token r, key channel c) of the readout operand
-            float w0[16], w1[16];
-            tmem_ld16x2(tb + lane_off + TM_W, tb + lane_off + TM_W + 16, w0, w1);
-            const int c = p;
-            float *blk = sm.bX + (c >> 5) * 64 * 32;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) st_op(blk, r, c & 31, w0[r]);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) st_op(blk, 16 + r, c & 31, w1[r]);
-            fence_proxy_async_smem();
-            tc_fence_before();
         }
         const bool stop = named_sync_or(BAR_PREP, kPrep, aborted(sm));
-        if (p == 0 && !stop) {
-            mbar_arrive(&sm.bar_bxfull);   // chunk n ready for the chain
+        if (P == 0 && !stop) {
+            // U'^T = V^T (T diag(beta))^T into TMEM U[st]; the chain adds -X_K (T diag(beta))^T
+            tc_fence_after();
+            const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_tf32_ts(tb + TM_U + 32 * st, tb + TM_BV + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
+                            idesc_tf32(128, 32), kk > 0);
+            mma_commit(&sm.bar_up[st]);
+            mbar_arrive(&sm.bar_bxfull);   // chunk n is ready for the chain
             if (n + 2 < nchunks) {
                 issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
                 pend_tma_par[st] = tma_par[st];
@@ -458,107 +495,98 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         if (n + 2 < nchunks) pend_tma[st] = true;
         if (stop) break;
     }
+    if (beta_thread) cp_async_wait_all();
     if (aborted(sm)) {   // drain what this thread saw in flight
         for (int s = 0; s < 2; ++s)
-            if (pend_tma[s] && p == 0) mbar_wait_bounded(&sm.bar_tma[s], pend_tma_par[s], kPollLimit);
-        if (pend_gram) mbar_wait_bounded(&sm.bar_gram, gram_par, kPollLimit);
-        if (pend_wu) mbar_wait_bounded(&sm.bar_wu, wu_par, kPollLimit);
+            if (pend_tma[s] && P == 0) mbar_wait_bounded(&sm.bar_tma[s], pend_tma_par[s], kPollLimit);
+        if (pend_gram && warp < 2) mbar_wait_bounded(&sm.bar_gram, gram_par ^ 1u, kPollLimit);
     }
 }
 
 // ---------------------------------------------------------------------------
-// Chain warps (8-15): the state-dependent part of chunk n.
+// Chain warps (8-11): the state-dependent part of chunk n.  Thread j owns
+// TMEM lane j = value index j.
 // ---------------------------------------------------------------------------
 template <typename OUT_T>
 __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, int H, int h,
                                            int64_t a, int64_t b, int nchunks, uint32_t tb) {
-    const int ct = threadIdx.x - kPrep;   // 0..255
-    const int warp = threadIdx.x >> 5;    // 8..15
-    const bool wg2 = ct < 128;
+    const int j = threadIdx.x - kPrep;   // 0..127
+    const int warp = threadIdx.x >> 5;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int j = ct & 127;               // value index = TMEM lane
-    const bool issuer = ct == 0;
-    uint32_t bxf_par = 0, x_par = 0, s_par = 0, xfree_par[2] = {0, 0};
-    bool pend_x = false, pend_s = false;
+    const bool issuer = j == 0;
+    uint32_t bxf_par = 0, x_par = 0, u_par = 0, s_par = 0, up_par[2] = {0, 0};
+    bool pend_x = false, pend_u = false, pend_s = false;
+    const uint64_t dX = sdesc_sw128(smem_u32(sm.bX));
 
     for (int n = 0; n < nchunks; ++n) {
         const int st = n & 1;
         const int64_t t0 = a + (int64_t)n * C;
         const int L = (int)((b - t0) < C ? (b - t0) : C);
-        const uint32_t tx = TM_X + 64 * st, tu = TM_U + 32 * st;
+        const uint32_t tu = TM_U + 32 * st;
 
+        // ---- a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
         if (issuer) {
-            bool ok = wait_phase(sm, &sm.bar_bxfull, bxf_par, 64u);
-            bxf_par ^= 1u;
-            if (ok && n >= 2) {
-                ok = wait_phase(sm, &sm.bar_xfree[st], xfree_par[st], 128u);
-                xfree_par[st] ^= 1u;
-            }
-            if (ok) {
+            if (wait_phase(sm, &sm.bar_bxfull, bxf_par, 64u)) {
                 tc_fence_after();
-                // X^T = S^T [W ; gamma Q]^T, A operand = the state in TMEM
-                const uint32_t aX = smem_u32(sm.bX);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < 16; ++kk)
-                    mma_tf32_ts(tb + tx, tb + TM_S + kk * 8,
-                                sdesc_sw128(aX + (kk >> 2) * (64 * 128) + (kk & 3) * 32),
+                    mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
+                                dX + (uint64_t)(((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4),
                                 idesc_tf32(128, 64), kk > 0);
                 mma_commit(&sm.bar_x);
                 mma_commit(&sm.bar_bxempty);
             }
         }
         __syncwarp();
+        bxf_par ^= 1u;
         pend_x = true;
         if (wait_phase(sm, &sm.bar_x, x_par, 16u)) pend_x = false;
         x_par ^= 1u;
         tc_fence_after();
         if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
 
-        // U^T = U'^T - (W S)^T ; S^T <- S^T Diag(e^{Gamma_last})
-        if (wg2) {
-            float u0[16], u1[16], x0[16], x1[16];
-            tmem_ld16x2(tb + lane_off + tu, tb + lane_off + tu + 16, u0, u1);
-            tmem_ld16x2(tb + lane_off + tx, tb + lane_off + tx + 16, x0, x1);
+        // ---- a4 (state side): U^T = U'^T - (gamma K S)^T (T diag(beta))^T ----
+        if (issuer) {
+            if (wait_phase(sm, &sm.bar_up[st], up_par[st], 16u)) {
+                tc_fence_after();
+                const uint64_t dN = sdesc_sw128(smem_u32(sm.tneg[st]));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32_ts(tb + tu, tb + TM_X + 32 + kk * 8, dN + (uint64_t)((kk * 32) >> 4),
+                                idesc_tf32(128, 32), 1u);
+                mma_commit(&sm.bar_u);
+            }
+        }
+        __syncwarp();
+        up_par[st] ^= 1u;
+        pend_u = true;
+        // S^T <- S^T Diag(e^{Gamma_last}), overlapping the U MMA
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float s0[16], s1[16];
+            tmem_ld16x2(tb + lane_off + TM_S + c0, tb + lane_off + TM_S + c0 + 16, s0, s1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                u0[i] = to_tf32(u0[i] - x0[i]);
-                u1[i] = to_tf32(u1[i] - x1[i]);
+                s0[i] *= sm.gamC[st][c0 + i];
+                s1[i] *= sm.gamC[st][c0 + 16 + i];
             }
-            tmem_st16(tb + lane_off + tu, u0);
-            tmem_st16(tb + lane_off + tu + 16, u1);
-        }
-        {
-            const int cbase = wg2 ? 0 : 64;
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float s0[16], s1[16];
-                const uint32_t col = TM_S + cbase + c0;
-                tmem_ld16x2(tb + lane_off + col, tb + lane_off + col + 16, s0, s1);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    s0[i] *= sm.gamC[st][cbase + c0 + i];
-                    s1[i] *= sm.gamC[st][cbase + c0 + 16 + i];
-                }
-                tmem_st16(tb + lane_off + col, s0);
-                tmem_st16(tb + lane_off + col + 16, s1);
-            }
+            tmem_st16(tb + lane_off + TM_S + c0, s0);
+            tmem_st16(tb + lane_off + TM_S + c0 + 16, s1);
         }
         tmem_wait_st();
         tc_fence_before();
+        if (wait_phase(sm, &sm.bar_u, u_par, 16u)) pend_u = false;
+        u_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
 
-        // O^T += U^T Aqk^T (into the gamma-Q-S half of X) ; S^T += U^T Kbar
+        // ---- a5/a6: [S^T | O^T] += U^T [Kbar^T ; Aqk]^T, one N = 160 MMA group ----
         if (issuer) {
             tc_fence_after();
-            const uint32_t aQ = smem_u32(sm.aqk[st]), aK = smem_u32(sm.kbT[st]);
-#pragma unroll 1
+            const uint64_t dK = sdesc_sw128(smem_u32(sm.kbaq[st]));
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_tf32_ts(tb + tx + 32, tb + tu + kk * 8, sdesc_sw128(aQ + kk * 32),
-                            idesc_tf32(128, 32), 1u);
-#pragma unroll 1
-            for (int kk = 0; kk < 4; ++kk)
-                mma_tf32_ts(tb + TM_S, tb + tu + kk * 8, sdesc_sw128(aK + kk * 32),
-                            idesc_tf32(128, 128), 1u);
+                mma_tf32_ts(tb + TM_S, tb + tu + kk * 8, dK + (uint64_t)((kk * 32) >> 4),
+                            idesc_tf32(128, 160), 1u);
             mma_commit(&sm.bar_s);
             mma_commit(&sm.bar_akempty[st]);
         }
@@ -568,25 +596,24 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         s_par ^= 1u;
         tc_fence_after();
 
-        // ---- output rows of chunk n (warpgroup 3), then release X[st] ----
-        if (!wg2) {
-            float o0[16], o1[16];
-            tmem_ld16x2(tb + lane_off + tx + 32, tb + lane_off + tx + 48, o0, o1);
-            OUT_T *dst = out + (t0 * H + h) * (int64_t)D + j;
-            const int64_t row = (int64_t)H * D;
+        // ---- a7: output rows ----
+        float o0[16], o1[16];
+        tmem_ld16x2(tb + lane_off + TM_X, tb + lane_off + TM_X + 16, o0, o1);
+        tc_fence_before();
+        named_sync(BAR_CHAIN, kChain);   // X may now be overwritten by the next readout MMA
+        OUT_T *dst = out + (t0 * H + h) * (int64_t)D + j;
+        const int64_t row = (int64_t)H * D;
 #pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (r < L) kda::st_elem(dst + r * row, o0[r]);
+        for (int r = 0; r < 16; ++r)
+            if (r < L) kda::st_elem(dst + r * row, o0[r]);
 #pragma unroll
-            for (int r = 0; r < 16; ++r)
-                if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
-            tc_fence_before();
-            mbar_arrive(&sm.bar_xfree[st]);
-        }
+        for (int r = 0; r < 16; ++r)
+            if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
     }
     if (aborted(sm)) {
-        if (pend_x) mbar_wait_bounded(&sm.bar_x, x_par, kPollLimit);
-        if (pend_s) mbar_wait_bounded(&sm.bar_s, s_par, kPollLimit);
+        if (pend_x) mbar_wait_bounded(&sm.bar_x, x_par ^ 1u, kPollLimit);
+        if (pend_u) mbar_wait_bounded(&sm.bar_u, u_par ^ 1u, kPollLimit);
+        if (pend_s) mbar_wait_bounded(&sm.bar_s, s_par ^ 1u, kPollLimit);
     }
 }
 
@@ -599,9 +626,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const float *__restrict__ init_state, const int32_t *__restrict__ cu,
                       OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
                       int64_t total, int64_t seq_len) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    TcSmem &sm = *reinterpret_cast<TcSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // Round up to 1024 bytes by pointer arithmetic on the shared array itself
+    // (an integer round trip would lose the shared address space and turn
+    // every access through `sm` into a generic one).
+    TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
 
     const int t = threadIdx.x, warp = t >> 5;
     const int h = blockIdx.x % H, n = blockIdx.x / H;
@@ -613,13 +642,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.bar_tma[s], 1);
             mbar_init(&sm.bar_akempty[s], 1);
-            mbar_init(&sm.bar_xfree[s], 128);
+            mbar_init(&sm.bar_up[s], 1);
         }
         mbar_init(&sm.bar_gram, 1);
-        mbar_init(&sm.bar_wu, 1);
         mbar_init(&sm.bar_bxfull, 1);
         mbar_init(&sm.bar_bxempty, 1);
         mbar_init(&sm.bar_x, 1);
+        mbar_init(&sm.bar_u, 1);
         mbar_init(&sm.bar_s, 1);
         fence_mbar_init();
         sm.abort = 0;
@@ -638,10 +667,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tb = sm.tmem_base;
     const int64_t state_off = ((int64_t)n * H + h) * D * D;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const bool state_wg = t >= kPrep && t < kPrep + 128;   // warpgroup 2: lanes = value index
+    const bool chain = t >= kPrep;
 
-    // initial state into TMEM: thread j holds column j of S (row j of S^T)
-    if (state_wg) {
+    // initial state into TMEM: chain thread j holds column j of S (row j of S^T)
+    if (chain) {
         const int j = t - kPrep;
         for (int c0 = 0; c0 < D; c0 += 16) {
             float v[16];
@@ -656,7 +685,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     tc_fence_after();
 
-    if (t < kPrep)
+    if (!chain)
         prep_loop(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb);
     else
         chain_loop<OUT_T>(sm, out, H, h, a, b, nchunks, tb);
@@ -664,7 +693,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (!aborted(sm) && final_state && state_wg) {
+    if (!aborted(sm) && final_state && chain) {
         const int j = t - kPrep;
         for (int c0 = 0; c0 < D; c0 += 16) {
             float s[16];
@@ -699,17 +728,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D view [T rows, H*D columns] of a [T, H, D] tensor, box = C rows x D columns.
+// 2-D view [T rows, H*D columns] of a [T, H, D] tensor; box = C rows x 128
+// bytes (64 bf16 or 32 fp32 elements), 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int64_t T,
               int H) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)H * D * esize};
-    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)C};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -69,6 +69,19 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- cp.async (4-byte)
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -147,7 +160,10 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32 lanes x 32-bit, 16 consecutive columns per thread (its own lane).  The
 // load and its tcgen05.wait::ld sit in one asm statement, so no use of the
-// destination registers can be scheduled before the data has arrived.
+// destination registers can be scheduled before the data has arrived.  These
+// touch only tensor memory and registers, so they carry no "memory" clobber:
+// ordinary loads and stores may be scheduled around them, while their order
+// relative to the tcgen05 fences (volatile asm) is kept.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -157,8 +173,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
+        : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -178,8 +193,7 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t taddr2, flo
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
-        : "r"(taddr), "r"(taddr2)
-        : "memory");
+        : "r"(taddr), "r"(taddr2));
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         v[i] = __uint_as_float(r[i]);
@@ -195,8 +209,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
         "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
         "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
+        "r"(__float_as_uint(v[15])));
 }
 // 16-byte store of four values into shared memory (already tf32-rounded by the caller).
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, float a, float b, float c, float d) {
@@ -229,11 +242,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Round an fp32 value to tf32 (nearest, ties away), low 13 bits cleared.
+// Round a finite fp32 value to tf32: nearest, ties away from zero, low 13
+// bits cleared.  Adding half a tf32 ulp (bit 12) to the magnitude bits and
+// truncating rounds the magnitude; the sign bit is untouched.  Two integer
+// operations (the result equals cvt.rna.tf32.f32 for finite inputs).
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 }  // namespace sm100
