@@ -142,6 +142,16 @@ kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const 
  */
 kda_status kda_get_last_device_error(kda_stream_t stream);
 
+/*
+ * kda_selftest_timeout -- diagnostic of the bounded-wait path (not part of
+ * the method).  Enqueues a one-warp kernel on `stream` that waits, with the
+ * same bounded wait the prefill kernel uses, on a barrier nothing arrives on;
+ * the wait gives up after a few milliseconds and records the device status
+ * word, so that the next kda_get_last_device_error() returns KDA_ERR_TIMEOUT.
+ * Nothing traps or hangs and the CUDA context stays usable.
+ */
+kda_status kda_selftest_timeout(kda_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *kda_status_string(kda_status status);
 

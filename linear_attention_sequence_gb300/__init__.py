@@ -17,6 +17,7 @@ import os
 import torch
 
 __all__ = ["KdaError", "kda_prefill", "kda_decode", "kda_status_string", "lib", "library_path",
+           "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,8 +68,23 @@ def lib():
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_last_cuda_error.restype = ctypes.c_char_p
         L.kda_version.restype = ctypes.c_int32
+        L.kda_get_last_device_error.argtypes = [vp]
+        L.kda_get_last_device_error.restype = ctypes.c_int
+        L.kda_selftest_timeout.argtypes = [vp]
+        L.kda_selftest_timeout.restype = ctypes.c_int
         _lib = L
     return _lib
+
+
+def kda_get_last_device_error(stream=None) -> int:
+    """Synchronise `stream` and return (then clear) the device status: 0 or
+    4 (KDA_ERR_TIMEOUT) if a bounded device-side wait gave up."""
+    return int(lib().kda_get_last_device_error(_stream(stream)))
+
+
+def kda_selftest_timeout(stream=None) -> None:
+    """Enqueue the diagnostic kernel whose bounded wait is made to give up."""
+    _check(lib().kda_selftest_timeout(_stream(stream)), "kda_selftest_timeout")
 
 
 def kda_status_string(status: int) -> str:

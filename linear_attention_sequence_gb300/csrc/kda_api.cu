@@ -63,6 +63,12 @@ const char *kda_last_cuda_error(void) { return g_last_cuda_error; }
 
 int32_t kda_version(void) { return 100; /* 0.1.0 */ }
 
+kda_status kda_selftest_timeout(kda_stream_t stream) {
+    cudaError_t e = kda_launch_selftest_timeout((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_selftest_timeout");
+    return KDA_OK;
+}
+
 kda_status kda_get_last_device_error(kda_stream_t stream) {
     unsigned status = 0;
     cudaError_t e = kda_read_device_status((cudaStream_t)stream, &status);

@@ -52,6 +52,7 @@ cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const vo
                                   const float *init_state, const int32_t *cu, void *out,
                                   float *final_state, cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
+cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
                                     const void *v, const float *g, const float *beta,
                                     const float *init_state, const int32_t *cu, void *out,

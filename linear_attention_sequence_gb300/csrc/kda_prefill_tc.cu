@@ -783,6 +783,26 @@ cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const vo
     return launch<float>(P, q, k, v, g, beta, init_state, cu, out, final_state, stream);
 }
 
+// Diagnostic of the bounded-wait path: one warp waits on an mbarrier that
+// nothing arrives on; the wait gives up after `polls` polls (a few
+// milliseconds) and records the status word exactly as the prefill kernel
+// does when one of its waits gives up.  Nothing traps or hangs.
+__global__ void kda_selftest_timeout_kernel(uint32_t polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&bar, 1);
+        sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    if (!sm100::mbar_wait_bounded(&bar, 0, polls) && threadIdx.x == 0)
+        atomicOr(&g_kda_device_status, 0x100u);
+}
+
+cudaError_t kda_launch_selftest_timeout(cudaStream_t stream) {
+    kda_selftest_timeout_kernel<<<1, 32, 0, stream>>>(1u << 16);
+    return cudaGetLastError();
+}
+
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return e;
