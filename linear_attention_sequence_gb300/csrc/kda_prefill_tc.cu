@@ -104,17 +104,17 @@ struct Stage {
 
 struct alignas(1024) TcSmem {
     Stage in[2];                // TMA destinations, double-buffered
+    float gramA[4 * 64 * 32];   // staging of the Gram A operand [k~ ; q~] (tf32), copied to TMEM
     float gramB[4 * 48 * 32];   // Gram B operand; after the Gram MMA, fp32 scratch of the solve
-    float e1t[C * D];           // e^{Gamma - ref}, fp32, laid out like an fp32 input tile
     float bX[4 * 64 * 32];      // readout B operand [gamma q ; gamma k] (single buffer)
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
-    float tmat[2][32 * 32];     // T diag(beta), B operand of the U' MMA
+    float tmat[32 * 32];        // T diag(beta), B operand of the U' MMA
     float tneg[2][32 * 32];     // -T diag(beta), B operand of the U MMA
     float betaS[2][C];
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
-    float gref[D], e01[D], e1l[D], glast[D];
+    float gref[D], e01[D], e1l[D];
     uint64_t bar_tma[2], bar_gram, bar_bxfull, bar_bxempty, bar_x, bar_u, bar_s;
-    uint64_t bar_up[2];        // U' MMA of the chunk with that parity is complete
+    uint64_t bar_up[2];         // U' MMA of the chunk with that parity is complete
     uint64_t bar_akempty[2];
     uint32_t tmem_base;
     int abort;
@@ -251,43 +251,93 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             sm.gref[c] = g15;
             sm.e01[c] = __expf(g15);
             sm.e1l[c] = __expf(gl - g15);
-            sm.glast[c] = gl;
             sm.gamC[st][c] = __expf(gl);
         }
         named_sync(BAR_PREP, kPrep);
 
-        // ---- a2: e^{Gamma - ref} once per element, the key variants of the Gram, V^T ----
+        // ---- a2: one pass over (token, 4-channel) blocks: Gram operands, Kbar^T, and
+        // the readout operand values (stored once the previous readout is done).
+        // Thread P handles tokens (P % 8) + 8 it, channels 4 (P / 8) .. +3. ----
+        float gq[4][4], gk[4][4];
         {
+            const int cb = P >> 3, c = 4 * cb, kb = cb >> 3, k4 = cb & 7;
+            float4 G[4];
+            float kx[4][4], qx[4][4];
 #pragma unroll
             for (int it = 0; it < 4; ++it) {
-                const int u = P + 256 * it, r = u >> 5, cb = u & 31, c = 4 * cb;
-                const bool live = r < L, sub1 = r >= 16;
-                const float4 G = ld_f32x4(in.g, r, c);
-                const float4 ref = sub1 ? *reinterpret_cast<const float4 *>(&sm.gref[c])
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float4 e1 = make_float4(__expf(G.x - ref.x), __expf(G.y - ref.y),
-                                              __expf(G.z - ref.z), __expf(G.w - ref.w));
-                *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(sm.e1t) +
-                                            off_f32(r, c)) = e1;
-                float x[4];
-                ld_bf16x4(in.k, r, c, x);
-                const float s = live ? 1.f : 0.f;
-                const float k0 = s * __fdividef(x[0], e1.x), k1 = s * __fdividef(x[1], e1.y),
-                            k2 = s * __fdividef(x[2], e1.z),
-                            k3 = s * __fdividef(x[3], e1.w);   // k e^{ref - Gamma}
-                float *blk = sm.gramB + (cb >> 3) * 48 * 32;
-                if (!sub1) {
-                    const float4 e = *reinterpret_cast<const float4 *>(&sm.e01[c]);
-                    st_op4(blk, r, cb & 7, k0, k1, k2, k3);
-                    st_op4(blk, 16 + r, cb & 7, k0 * e.x, k1 * e.y, k2 * e.z, k3 * e.w);
-                } else {
-                    st_op4(blk, 16 + r, cb & 7, k0, k1, k2, k3);
-                }
+                const int r = (P & 7) + 8 * it;
+                G[it] = ld_f32x4(in.g, r, c);
+                ld_bf16x4(in.k, r, c, kx[it]);
+                ld_bf16x4(in.q, r, c, qx[it]);
             }
-            fence_proxy_async_smem();
+            const float4 gr4 = *reinterpret_cast<const float4 *>(&sm.gref[c]);
+            const float4 e4 = *reinterpret_cast<const float4 *>(&sm.e01[c]);
+            const float4 l4 = *reinterpret_cast<const float4 *>(&sm.e1l[c]);
+            const float gref[4] = {gr4.x, gr4.y, gr4.z, gr4.w};
+            const float e01[4] = {e4.x, e4.y, e4.z, e4.w};
+            const float e1l[4] = {l4.x, l4.y, l4.z, l4.w};
+            float *gA = sm.gramA + kb * 64 * 32;
+            float *gB = sm.gramB + kb * 48 * 32;
+            float *kbq = sm.kbaq[st];
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int r = (P & 7) + 8 * it;
+                const bool sub1 = it >= 2;            // tokens 16..31
+                const float sc = r < L ? 1.f : 0.f;
+                const float gv[4] = {G[it].x, G[it].y, G[it].z, G[it].w};
+                float ka[4], qa[4], kv[4], kv1[4], kbar[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float e1 = __expf(gv[m] - (sub1 ? gref[m] : 0.f));   // [e^-80, 1]
+                    const float inv = __fdividef(1.f, e1);                        // [1, e^80]
+                    const float kk = sc * kx[it][m], qq = sc * qx[it][m];
+                    ka[m] = kk * e1;
+                    qa[m] = qq * e1;
+                    kv[m] = kk * inv;              // k e^{ref - Gamma}
+                    kv1[m] = kv[m] * e01[m];       // k e^{Gamma_15 - Gamma}   (sub-tile 0 keys)
+                    const float gam = sub1 ? e1 * e01[m] : e1;                    // e^{Gamma}
+                    gq[it][m] = qq * gam;
+                    gk[it][m] = kk * gam;
+                    kbar[m] = (sub1 ? kv[m] : kv1[m]) * e1l[m];                  // k e^{Gamma_last - Gamma}
+                }
+                st_op4(gA, r, k4, ka[0], ka[1], ka[2], ka[3]);
+                st_op4(gA, 32 + r, k4, qa[0], qa[1], qa[2], qa[3]);
+                if (!sub1) {
+                    st_op4(gB, r, k4, kv[0], kv[1], kv[2], kv[3]);
+                    st_op4(gB, 16 + r, k4, kv1[0], kv1[1], kv1[2], kv1[3]);
+                } else {
+                    st_op4(gB, 16 + r, k4, kv[0], kv[1], kv[2], kv[3]);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) st_op(kbq, c + m, r, kbar[m]);
+            }
         }
-        if (wg == 1) {
-            // V^T into TMEM (thread = value index); the U' MMA of chunk n-1 must be done with it
+        fence_proxy_async_smem();
+        named_sync(BAR_PREP, kPrep);
+
+        // ---- a3: Gram A operand staging -> TMEM (warps 0, 1); V^T -> TMEM (warps 4-7) ----
+        if (warp < 2) {
+            const int r = lane, row = 32 * warp + r;     // warp 0: k~ rows, warp 1: q~ rows
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                const float *blk = sm.gramA + (c0 >> 5) * 64 * 32;
+                float vals[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int k4 = ((c0 & 31) >> 2) + j;
+                    const float4 x = *reinterpret_cast<const float4 *>(
+                        reinterpret_cast<const unsigned char *>(blk) + row * 128 + (((k4 ^ row) & 7) << 4));
+                    vals[4 * j + 0] = x.x;
+                    vals[4 * j + 1] = x.y;
+                    vals[4 * j + 2] = x.z;
+                    vals[4 * j + 3] = x.w;
+                }
+                tmem_st16(tb + lane_off + TM_GA + c0, vals);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+        } else if (wg == 1) {
+            // V^T (thread = value index); the U' MMA of chunk n-1 must be done with it
             if (n >= 1) {
                 wait_phase(sm, &sm.bar_up[st ^ 1], up_par[st ^ 1], 8u);
                 up_par[st ^ 1] ^= 1u;
@@ -305,52 +355,6 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             tc_fence_before();
         }
         named_sync(BAR_PREP, kPrep);
-
-        // ---- a3: Gram A operand into TMEM (quadrants 0,1); Kbar^T (quadrants 2,3) ----
-        if (qd < 2) {
-            const int r = lane;
-            const bool live = r < L;
-            const unsigned char *src = qd == 0 ? in.k : in.q;
-            const int c_lo = 64 * wg, nblk = 4;
-            for (int blk = 0; blk < nblk; ++blk) {
-                const int c0 = c_lo + 16 * blk;
-                float vals[16];
-#pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                    const int c = c0 + 4 * j4;
-                    const float4 E = ld_f32x4(sm.e1t, r, c);
-                    float x[4];
-                    ld_bf16x4(src, r, c, x);
-                    vals[4 * j4 + 0] = to_tf32(live ? x[0] * E.x : 0.f);
-                    vals[4 * j4 + 1] = to_tf32(live ? x[1] * E.y : 0.f);
-                    vals[4 * j4 + 2] = to_tf32(live ? x[2] * E.z : 0.f);
-                    vals[4 * j4 + 3] = to_tf32(live ? x[3] * E.w : 0.f);
-                }
-                tmem_st16(tb + lane_off + TM_GA + c0, vals);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-        } else {
-            const int kt = (wg * 2 + (qd - 2)) * 32 + lane;   // 0..127
-            {
-                const int c = kt;
-                const float gl = sm.glast[c];
-                const float *g = reinterpret_cast<const float *>(in.g);
-                float *kb = sm.kbaq[st];
-#pragma unroll
-                for (int r4 = 0; r4 < 8; ++r4) {
-                    float kbar[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int r = 4 * r4 + m;
-                        kbar[m] = r < L ? ld_bf16(in.k, r, c) * __expf(gl - g[off_f32(r, c) >> 2]) : 0.f;
-                    }
-                    st_op4(kb, c, r4, kbar[0], kbar[1], kbar[2], kbar[3]);
-                }
-            }
-            fence_proxy_async_smem();
-        }
-        named_sync(BAR_PREP, kPrep);
         if (P == 0) {
             tc_fence_after();
             const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
@@ -364,32 +368,23 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         __syncwarp();
         pend_gram = true;
 
-        // ---- readout operand [gamma q ; gamma k] (warps 4-11), while the Gram runs ----
+        // ---- readout operand [gamma q ; gamma k], while the Gram runs (single buffer:
+        // the readout MMA of chunk n-1 must have consumed it) ----
+        if (n >= 1) {
+            wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
+            bxe_par ^= 1u;
+        }
         {
-            if (n >= 1) {   // single buffer: the readout MMA of chunk n-1 must be done with it
-                wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
-                bxe_par ^= 1u;
-            }
+            const int cb = P >> 3, k4 = cb & 7;
+            float *blk = sm.bX + (cb >> 3) * 64 * 32;
 #pragma unroll
             for (int it = 0; it < 4; ++it) {
-                const int u = P + 256 * it, r = u >> 5, cb = u & 31, c = 4 * cb;
-                const float s = r < L ? 1.f : 0.f;
-                float4 gm = ld_f32x4(sm.e1t, r, c);   // e^{Gamma}: e1 times e^{ref}
-                if (r >= 16) {
-                    const float4 e = *reinterpret_cast<const float4 *>(&sm.e01[c]);
-                    gm.x *= e.x; gm.y *= e.y; gm.z *= e.z; gm.w *= e.w;
-                }
-                float kx[4], qx[4];
-                ld_bf16x4(in.k, r, c, kx);
-                ld_bf16x4(in.q, r, c, qx);
-                float *blk = sm.bX + (cb >> 3) * 64 * 32;
-                st_op4(blk, r, cb & 7, s * qx[0] * gm.x, s * qx[1] * gm.y, s * qx[2] * gm.z,
-                       s * qx[3] * gm.w);
-                st_op4(blk, 32 + r, cb & 7, s * kx[0] * gm.x, s * kx[1] * gm.y, s * kx[2] * gm.z,
-                       s * kx[3] * gm.w);
+                const int r = (P & 7) + 8 * it;
+                st_op4(blk, r, k4, gq[it][0], gq[it][1], gq[it][2], gq[it][3]);
+                st_op4(blk, 32 + r, k4, gk[it][0], gk[it][1], gk[it][2], gk[it][3]);
             }
-            fence_proxy_async_smem();
         }
+        fence_proxy_async_smem();
 
         // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram ----
         float(*akk)[33] = reinterpret_cast<float(*)[33]>(sm.gramB);
@@ -409,11 +404,15 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                     akk[r][i] = i < r ? br * val : 0.f;
                 }
             } else {
+                float a[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
-                    st_op(sm.kbaq[st], 128 + r, i, i <= r ? val : 0.f);
+                    a[i] = i <= r ? val : 0.f;
                 }
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4)
+                    st_op4(sm.kbaq[st], 128 + r, i4, a[4 * i4], a[4 * i4 + 1], a[4 * i4 + 2], a[4 * i4 + 3]);
                 fence_proxy_async_smem();
             }
             tc_fence_before();
@@ -468,8 +467,8 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 float tb8[8];
 #pragma unroll
                 for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * sm.betaS[st][c0 + m];
-                st_op4(sm.tmat[st], r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
-                st_op4(sm.tmat[st], r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
+                st_op4(sm.tmat, r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
+                st_op4(sm.tmat, r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
                 st_op4(sm.tneg[st], r, c0 >> 2, -tb8[0], -tb8[1], -tb8[2], -tb8[3]);
                 st_op4(sm.tneg[st], r, (c0 >> 2) + 1, -tb8[4], -tb8[5], -tb8[6], -tb8[7]);
             }
@@ -479,7 +478,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         if (P == 0 && !stop) {
             // U'^T = V^T (T diag(beta))^T into TMEM U[st]; the chain adds -X_K (T diag(beta))^T
             tc_fence_after();
-            const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
+            const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_tf32_ts(tb + TM_U + 32 * st, tb + TM_BV + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
