@@ -19,12 +19,14 @@
 // readout GEMM straight from TMEM and accumulates its own update in place.
 //
 // Warp specialisation.  Warps 0-7 prepare chunk n (decay prefix, decay-
-// weighted operands, Gram MMA, triangular solve, U' = T diag(beta) V) while
-// warps 8-11 run the state chain of chunk n-1: the readout MMA
+// weighted operands, Gram MMA, triangular solve) while warps 8-11 run the
+// state chain of chunk n-1: U' = T diag(beta) V and the readout MMA
 // X = S^T [gamma Q; gamma K]^T, the U MMA that subtracts (gamma K S) T diag(beta)
 // with the X accumulator itself as A operand, the state decay, and one MMA
 // group for the intra-chunk readout and the state carry together, then the
-// output store.  The two groups hand buffers to each other through mbarriers;
+// output store.  The thread that issues a tcgen05.mma or a TMA load is held
+// for roughly the time the unit needs to accept it, so each issue is given
+// to a warp that has nothing else to do at that point.  The two groups hand buffers to each other through mbarriers;
 // every wait is bounded.  A tcgen05.mma costs a roughly fixed time per
 // instruction on these shapes, so the formulation minimises the instruction
 // count: 16 for the Gram and 16 for the readout (K = d_k = 128), 4 each for
@@ -69,7 +71,12 @@ constexpr int kThreads = kPrep + kChain;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPollLimit = 1u << 23;  // about half a second of polling per wait
 
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_SOLVE = 3;  // named barriers
+// Named barriers.  A phase of an mbarrier is awaited by one thread, and a named
+// barrier releases the threads that depend on it: hundreds of threads polling
+// mbarriers slow every other mbarrier and tensor-core operation of the SM.
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_SOLVE = 3, BAR_WG1 = 4, BAR_E1 = 5;
+constexpr int kGramIssuer = 96;   // warp 3: idle until the solve
+constexpr int kTmaIssuer = 224;   // warp 7: idle after the V^T copy
 
 // tensor-memory columns
 constexpr uint32_t TM_S = 0;     // 128: S^T (lanes = value index, columns = key channel)
@@ -108,8 +115,7 @@ struct alignas(1024) TcSmem {
     float gramB[4 * 48 * 32];   // Gram B operand; after the Gram MMA, fp32 scratch of the solve
     float bX[4 * 64 * 32];      // readout B operand [gamma q ; gamma k] (single buffer)
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
-    float tmat[32 * 32];        // T diag(beta), B operand of the U' MMA
-    float tneg[2][32 * 32];     // -T diag(beta), B operand of the U MMA
+    float tmat[2][32 * 32];     // T diag(beta): B operand of the U' MMA and, negated, of the U MMA
     float betaS[2][C];
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
@@ -154,26 +160,30 @@ __device__ __forceinline__ float ld_bf16(const unsigned char *tile, int r, int c
 __device__ __forceinline__ void issue_stage_loads(Stage &st, uint64_t *bar, const CUtensorMap *mq,
                                                   const CUtensorMap *mk, const CUtensorMap *mv,
                                                   const CUtensorMap *mg, int h, int64_t t0) {
+    // one box per tensor: {128-byte segment, C tokens, the head's segments}
     mbar_arrive_expect_tx(bar, kStageBytes);
-    const int x = h * D, y = (int)t0;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        tma_load_2d(st.q + half * 4096, mq, bar, x + 64 * half, y);
-        tma_load_2d(st.k + half * 4096, mk, bar, x + 64 * half, y);
-        tma_load_2d(st.v + half * 4096, mv, bar, x + 64 * half, y);
-    }
-#pragma unroll
-    for (int qtr = 0; qtr < 4; ++qtr) tma_load_2d(st.g + qtr * 4096, mg, bar, x + 32 * qtr, y);
+    const int y = (int)t0;
+    tma_load_3d(st.q, mq, bar, 0, y, 2 * h);
+    tma_load_3d(st.k, mk, bar, 0, y, 2 * h);
+    tma_load_3d(st.v, mv, bar, 0, y, 2 * h);
+    tma_load_3d(st.g, mg, bar, 0, y, 4 * h);
 }
 
-__device__ __forceinline__ bool wait_phase(TcSmem &sm, uint64_t *bar, uint32_t parity,
-                                           unsigned code) {
+// Bounded wait for a phase.  The first poll is inline; the polling loop (and
+// the error path) is a single out-of-line copy, which keeps the loop bodies of
+// the kernel small enough for the instruction caches.
+__device__ __noinline__ bool wait_phase_slow(TcSmem &sm, uint64_t *bar, uint32_t parity,
+                                             unsigned code) {
     if (!mbar_wait_bounded(bar, parity, kPollLimit)) {
         *reinterpret_cast<volatile int *>(&sm.abort) = 1;
         atomicOr(&g_kda_device_status, code);
         return false;
     }
     return true;
+}
+__device__ __forceinline__ bool wait_phase(TcSmem &sm, uint64_t *bar, uint32_t parity,
+                                           unsigned code) {
+    return mbar_try_wait(bar, parity) || wait_phase_slow(sm, bar, parity, code);
 }
 __device__ __forceinline__ bool aborted(TcSmem &sm) {
     return *reinterpret_cast<volatile int *>(&sm.abort) != 0;
@@ -202,7 +212,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         else sm.betaS[0][r] = 0.f;
         cp_async_commit();
     }
-    if (P == 0)
+    if (P == kTmaIssuer)
         for (int s = 0; s < 2 && s < nchunks; ++s)
             issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C);
     __syncwarp();
@@ -215,12 +225,15 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         Stage &in = sm.in[st];
 
         // the chain must be done with chunk n-2 (same parity) before its
-        // buffers (kbaq, tmat, tneg, gamC, TMEM U) are overwritten
-        if (n >= 2) {
-            wait_phase(sm, &sm.bar_akempty[st], ake_par[st], 32u);
-            ake_par[st] ^= 1u;
+        // buffers (kbaq, tmat, gamC, TMEM U) are overwritten, and the inputs
+        // of chunk n must have landed.  One thread waits; the barrier below
+        // releases the others (and orders their reads after the TMA writes).
+        if (P == 0) {
+            if (n >= 2) wait_phase(sm, &sm.bar_akempty[st], ake_par[st], 32u);
+            pend_tma[st] = !wait_phase(sm, &sm.bar_tma[st], tma_par[st], 1u);
+            pend_tma_par[st] = tma_par[st];   // drained with this parity if still pending
         }
-        if (wait_phase(sm, &sm.bar_tma[st], tma_par[st], 1u)) pend_tma[st] = false;
+        if (n >= 2) ake_par[st] ^= 1u;
         tma_par[st] ^= 1u;
         if (beta_thread) {
             cp_async_wait_all();   // beta of chunk n has landed
@@ -339,8 +352,10 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         } else if (wg == 1) {
             // V^T (thread = value index); the U' MMA of chunk n-1 must be done with it
             if (n >= 1) {
-                wait_phase(sm, &sm.bar_up[st ^ 1], up_par[st ^ 1], 8u);
+                if (P == 128) wait_phase(sm, &sm.bar_up[st ^ 1], up_par[st ^ 1], 8u);
                 up_par[st ^ 1] ^= 1u;
+                named_sync(BAR_WG1, 128);
+                tc_fence_after();
             }
             const int j = P - 128;
             float v0[16], v1[16];
@@ -355,7 +370,14 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             tc_fence_before();
         }
         named_sync(BAR_PREP, kPrep);
-        if (P == 0) {
+        // the inputs of chunk n are consumed: refill the stage with chunk n+2
+        if (P == kTmaIssuer && n + 2 < nchunks)
+            issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
+        if (n + 2 < nchunks) {   // tracked by thread 0, which waits on (and drains) bar_tma
+            pend_tma[st] = true;
+            pend_tma_par[st] = tma_par[st];
+        }
+        if (P == kGramIssuer) {
             tc_fence_after();
             const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
 #pragma unroll
@@ -366,13 +388,14 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             mma_commit(&sm.bar_gram);
         }
         __syncwarp();
-        pend_gram = true;
+        if (P == 0) pend_gram = true;
 
         // ---- readout operand [gamma q ; gamma k], while the Gram runs (single buffer:
         // the readout MMA of chunk n-1 must have consumed it) ----
-        if (n >= 1) {
-            wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
+        if (n >= 1) {   // generic stores after the MMA's reads: lane 0 waits, the warp follows
+            if (lane == 0) wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
             bxe_par ^= 1u;
+            __syncwarp();
         }
         {
             const int cb = P >> 3, k4 = cb & 7;
@@ -389,8 +412,9 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram ----
         float(*akk)[33] = reinterpret_cast<float(*)[33]>(sm.gramB);
         if (warp < 2) {
-            if (wait_phase(sm, &sm.bar_gram, gram_par, 2u)) pend_gram = false;
+            if (P == 0) pend_gram = !wait_phase(sm, &sm.bar_gram, gram_par, 2u);
             gram_par ^= 1u;
+            named_sync(BAR_E1, 64);
             tc_fence_after();
             float d0[16], d1[16], d2[16];
             tmem_ld16x2(tb + lane_off + TM_G, tb + lane_off + TM_G + 16, d0, d1);
@@ -467,38 +491,20 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 float tb8[8];
 #pragma unroll
                 for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * sm.betaS[st][c0 + m];
-                st_op4(sm.tmat, r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
-                st_op4(sm.tmat, r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
-                st_op4(sm.tneg[st], r, c0 >> 2, -tb8[0], -tb8[1], -tb8[2], -tb8[3]);
-                st_op4(sm.tneg[st], r, (c0 >> 2) + 1, -tb8[4], -tb8[5], -tb8[6], -tb8[7]);
+                st_op4(sm.tmat[st], r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
+                st_op4(sm.tmat[st], r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
             }
             fence_proxy_async_smem();
         }
         const bool stop = named_sync_or(BAR_PREP, kPrep, aborted(sm));
-        if (P == 0 && !stop) {
-            // U'^T = V^T (T diag(beta))^T into TMEM U[st]; the chain adds -X_K (T diag(beta))^T
-            tc_fence_after();
-            const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_tf32_ts(tb + TM_U + 32 * st, tb + TM_BV + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
-                            idesc_tf32(128, 32), kk > 0);
-            mma_commit(&sm.bar_up[st]);
-            mbar_arrive(&sm.bar_bxfull);   // chunk n is ready for the chain
-            if (n + 2 < nchunks) {
-                issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
-                pend_tma_par[st] = tma_par[st];
-            }
-        }
-        __syncwarp();
-        if (n + 2 < nchunks) pend_tma[st] = true;
+        if (P == 0 && !stop) mbar_arrive(&sm.bar_bxfull);   // chunk n is ready for the chain
         if (stop) break;
     }
     if (beta_thread) cp_async_wait_all();
     if (aborted(sm)) {   // drain what this thread saw in flight
         for (int s = 0; s < 2; ++s)
             if (pend_tma[s] && P == 0) mbar_wait_bounded(&sm.bar_tma[s], pend_tma_par[s], kPollLimit);
-        if (pend_gram && warp < 2) mbar_wait_bounded(&sm.bar_gram, gram_par ^ 1u, kPollLimit);
+        if (pend_gram && P == 0) mbar_wait_bounded(&sm.bar_gram, gram_par ^ 1u, kPollLimit);
     }
 }
 
@@ -513,7 +519,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
     const int warp = threadIdx.x >> 5;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const bool issuer = j == 0;
-    uint32_t bxf_par = 0, x_par = 0, u_par = 0, s_par = 0, up_par[2] = {0, 0};
+    uint32_t bxf_par = 0, x_par = 0, u_par = 0, s_par = 0;
     bool pend_x = false, pend_u = false, pend_s = false;
     const uint64_t dX = sdesc_sw128(smem_u32(sm.bX));
 
@@ -523,10 +529,19 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         const int L = (int)((b - t0) < C ? (b - t0) : C);
         const uint32_t tu = TM_U + 32 * st;
 
-        // ---- a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
+        // ---- U'^T = V^T (T diag(beta))^T into TMEM U[st], then
+        // a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
+        bool issued = false;
         if (issuer) {
             if (wait_phase(sm, &sm.bar_bxfull, bxf_par, 64u)) {
+                issued = true;
                 tc_fence_after();
+                const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32_ts(tb + tu, tb + TM_BV + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
+                                idesc_tf32(128, 32), kk > 0);
+                mma_commit(&sm.bar_up[st]);   // V^T may be overwritten once this completes
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk)
                     mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
@@ -538,27 +553,23 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         }
         __syncwarp();
         bxf_par ^= 1u;
-        pend_x = true;
-        if (wait_phase(sm, &sm.bar_x, x_par, 16u)) pend_x = false;
+        if (issued) pend_x = !wait_phase(sm, &sm.bar_x, x_par, 16u);
         x_par ^= 1u;
-        tc_fence_after();
         if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
+        tc_fence_after();
 
-        // ---- a4 (state side): U^T = U'^T - (gamma K S)^T (T diag(beta))^T ----
+        // ---- a4 (state side): U^T = U'^T - (gamma K S)^T (T diag(beta))^T, accumulated
+        // onto U' (same accumulator and issuing thread, so it follows the U' MMA) ----
         if (issuer) {
-            if (wait_phase(sm, &sm.bar_up[st], up_par[st], 16u)) {
-                tc_fence_after();
-                const uint64_t dN = sdesc_sw128(smem_u32(sm.tneg[st]));
+            tc_fence_after();
+            const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32_ts(tb + tu, tb + TM_X + 32 + kk * 8, dN + (uint64_t)((kk * 32) >> 4),
-                                idesc_tf32(128, 32), 1u);
-                mma_commit(&sm.bar_u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                mma_tf32_ts(tb + tu, tb + TM_X + 32 + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
+                            idesc_tf32_negb(128, 32), 1u);
+            mma_commit(&sm.bar_u);
         }
         __syncwarp();
-        up_par[st] ^= 1u;
-        pend_u = true;
         // S^T <- S^T Diag(e^{Gamma_last}), overlapping the U MMA
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -574,7 +585,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         }
         tmem_wait_st();
         tc_fence_before();
-        if (wait_phase(sm, &sm.bar_u, u_par, 16u)) pend_u = false;
+        if (issuer) pend_u = !wait_phase(sm, &sm.bar_u, u_par, 16u);
         u_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
 
@@ -590,9 +601,9 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
             mma_commit(&sm.bar_akempty[st]);
         }
         __syncwarp();
-        pend_s = true;
-        if (wait_phase(sm, &sm.bar_s, s_par, 16u)) pend_s = false;
+        if (issuer) pend_s = !wait_phase(sm, &sm.bar_s, s_par, 16u);
         s_par ^= 1u;
+        named_sync(BAR_CHAIN, kChain);
         tc_fence_after();
 
         // ---- a7: output rows ----
@@ -609,7 +620,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         for (int r = 0; r < 16; ++r)
             if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
     }
-    if (aborted(sm)) {
+    if (aborted(sm) && issuer) {   // the issuer alone tracks (and drains) the MMA groups
         if (pend_x) mbar_wait_bounded(&sm.bar_x, x_par ^ 1u, kPollLimit);
         if (pend_u) mbar_wait_bounded(&sm.bar_u, u_par ^ 1u, kPollLimit);
         if (pend_s) mbar_wait_bounded(&sm.bar_s, s_par ^ 1u, kPollLimit);
@@ -727,17 +738,19 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D view [T rows, H*D columns] of a [T, H, D] tensor; box = C rows x 128
-// bytes (64 bf16 or 32 fp32 elements), 128-byte swizzle.
+// 3-D view of a [T, H, D] tensor: (element within a 128-byte segment, token,
+// segment index along the H*D row); box = one head's segments for C tokens,
+// stored segment by segment (C rows of 128 bytes each), 128-byte swizzle.
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int64_t T,
               int H) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)H * D, (cuuint64_t)T};
-    const cuuint64_t strides[1] = {(cuuint64_t)H * D * esize};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)C};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+    const int seg = 128 / esize, nseg = D / seg;
+    const cuuint64_t dims[3] = {(cuuint64_t)seg, (cuuint64_t)T, (cuuint64_t)H * nseg};
+    const cuuint64_t strides[2] = {(cuuint64_t)H * D * esize, 128};
+    const cuuint32_t box[3] = {(cuuint32_t)seg, (cuuint32_t)C, (cuuint32_t)nseg};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

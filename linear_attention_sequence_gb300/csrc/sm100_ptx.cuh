@@ -49,6 +49,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // `max_polls` polls (each poll backs off a little after the first few).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint32_t max_polls) {
+#pragma unroll 1
     for (uint32_t i = 0; i < max_polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 64) __nanosleep(64);
@@ -63,6 +64,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -116,6 +125,10 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            | (2u << 10)                         // B format: tf32
            | ((uint32_t)(N >> 3) << 17)         // N / 8
            | ((uint32_t)(M >> 4) << 24);        // M / 16
+}
+// The same with the B operand negated (D = A (-B) [+ D]).
+__host__ __device__ constexpr uint32_t idesc_tf32_negb(int M, int N) {
+    return idesc_tf32(M, N) | (1u << 14);
 }
 // Shared-memory matrix descriptor for a K-major SW128 operand starting at
 // shared address `saddr` (see the layout note at the top of this file).
