@@ -18,16 +18,17 @@
 // key channel) lives in TMEM for the whole sequence, is the A operand of the
 // readout GEMM straight from TMEM and accumulates its own update in place.
 //
-// Warp specialisation.  Warps 0-7 prepare chunk n (decay prefix, decay-
-// weighted operands, Gram MMA, triangular solve) while warps 8-11 run the
-// state chain of chunk n-1: U' = T diag(beta) V and the readout MMA
-// X = S^T [gamma Q; gamma K]^T, the U MMA that subtracts (gamma K S) T diag(beta)
-// with the X accumulator itself as A operand, the state decay, and one MMA
-// group for the intra-chunk readout and the state carry together, then the
-// output store.  The thread that issues a tcgen05.mma or a TMA load is held
-// for roughly the time the unit needs to accept it, so each issue is given
-// to a warp that has nothing else to do at that point.  The two groups hand buffers to each other through mbarriers;
-// every wait is bounded.  A tcgen05.mma costs a roughly fixed time per
+// Warp specialisation.  Warps 0-7 prepare chunk n: decay prefix,
+// decay-weighted operands, the Gram MMA.  Warps 8-11 run the rest of a chunk:
+// extraction of the intra-chunk matrices from the Gram, the triangular solve,
+// U' = T diag(beta) V and the readout MMA X = S^T [gamma Q; gamma K]^T, the U
+// MMA that subtracts (gamma K S) T diag(beta) with the X accumulator itself as
+// A operand, the state decay, and one MMA group for the intra-chunk readout
+// and the state carry together, then the output store.  The two groups hand
+// buffers to each other through mbarriers; every wait is bounded.  The thread
+// that issues a tcgen05.mma or a TMA load is held for roughly the time the
+// unit needs to accept it, so each issue is given to a warp that has nothing
+// else to do at that point.  A tcgen05.mma costs a roughly fixed time per
 // instruction on these shapes, so the formulation minimises the instruction
 // count: 16 for the Gram and 16 for the readout (K = d_k = 128), 4 each for
 // U', U and the readout + state-carry group.
@@ -38,17 +39,15 @@
 // is processed.
 //
 // Decay factoring.  Products e^{Gamma_r - Gamma_i} (i <= r) are split into
-// two bounded factors around a reference inside the chunk.  The chunk is two
-// 16-token sub-tiles; with the log-decay bounded below by g_min = -5 the
-// cumulative decay over one sub-tile stays above e^{-80} ("Understanding Kimi
-// K3's Attention", log-decay bound; "Kimi K3.1 and the Road ...", section 5),
-// so e^{Gamma_r - Gamma_s} and its inverse stay inside fp32 range when r and s
-// are in the same sub-tile.  Rows use the start of their own sub-tile as the
-// reference; columns come in two variants (reference = start of sub-tile 0 or
-// of sub-tile 1), so the Gram matrices are one 128 x 48 x 128 MMA:
-//   rows  0..31 : k_r e^{Gamma_r - ref(r)}     rows 32..63: q_r e^{Gamma_r - ref(r)}
-//   cols  0..15 : k_i e^{0 - Gamma_i}          (i in sub-tile 0, reference 0)
-//   cols 16..47 : k_i e^{Gamma_15 - Gamma_i}   (i = 0..31,   reference Gamma_15)
+// two bounded factors around the reference Gamma_15 (the running sum after
+// the 16th token of the chunk).  With the log-decay bounded below by
+// g_min = -5, |Gamma_r - Gamma_15| <= 16 * 5 = 80 for every token r of a
+// 32-token chunk ("Understanding Kimi K3's Attention", log-decay bound;
+// "Kimi K3.1 and the Road ...", section 5), so e^{Gamma_r - Gamma_15} and its
+// inverse stay inside the fp32 (and tf32) normal range.  The Gram matrices
+// are then one 128 x 32 x 128 MMA group:
+//   A rows  0..31 : k_r e^{Gamma_r - Gamma_15}     rows 32..63: q_r e^{Gamma_r - Gamma_15}
+//   B rows  0..31 : k_i e^{Gamma_15 - Gamma_i}
 // (the A operand sits in TMEM lanes 0-63; lanes 64-127 are not used and their
 // results are ignored).
 
@@ -74,16 +73,17 @@ constexpr uint32_t kPollLimit = 1u << 23;  // about half a second of polling per
 // Named barriers.  A phase of an mbarrier is awaited by one thread, and a named
 // barrier releases the threads that depend on it: hundreds of threads polling
 // mbarriers slow every other mbarrier and tensor-core operation of the SM.
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_SOLVE = 3, BAR_WG1 = 4, BAR_E1 = 5;
-constexpr int kGramIssuer = 96;   // warp 3: idle until the solve
-constexpr int kTmaIssuer = 224;   // warp 7: idle after the V^T copy
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_E1 = 3, BAR_WG1 = 4;
+constexpr int kGramIssuer = 96;   // warp 3: idle after the element-wise pass
+constexpr int kTmaIssuer = 224;   // warp 7: issues the first two stage loads
+constexpr int kBetaRing = 4;      // beta of chunk n sits in slot n % 4 (the prep runs <= 2 chunks ahead)
 
 // tensor-memory columns
 constexpr uint32_t TM_S = 0;     // 128: S^T (lanes = value index, columns = key channel)
 constexpr uint32_t TM_X = 128;   // 64: [(gamma Q S)^T, then O^T | (gamma K S)^T]
 constexpr uint32_t TM_U = 192;   // 2 x 32: U'^T, then U^T, per chunk parity
 constexpr uint32_t TM_BV = 256;  // 32: V^T, A operand of the U' MMA
-constexpr uint32_t TM_G = 288;   // 48: Gram
+constexpr uint32_t TM_G = 288;   // 2 x 32: Gram, per chunk parity
 constexpr uint32_t TM_GA = 384;  // 128: Gram A operand, lanes 0-31 k~, 32-63 q~
 
 constexpr uint32_t kTileBf16 = C * D * 2;
@@ -102,26 +102,34 @@ __device__ __forceinline__ uint32_t off_f32(int r, int c) {
     return (uint32_t)((c >> 5) * 4096 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
 }
 
+// A stage holds the TMA-loaded inputs of one chunk and then, once they are
+// consumed, that chunk's readout B operand [gamma q ; gamma k] (32 KB, SW128
+// K-major, over the q, k, v tiles and the first quarter of g) until the
+// readout MMA has read it.
 struct Stage {
     unsigned char q[kTileBf16];
     unsigned char k[kTileBf16];
     unsigned char v[kTileBf16];
     unsigned char g[kTileF32];  // g, then Gamma in place
 };
+static_assert(4 * 64 * 32 * 4 <= sizeof(Stage), "readout operand fits in a stage");
 
 struct alignas(1024) TcSmem {
     Stage in[2];                // TMA destinations, double-buffered
     float gramA[4 * 64 * 32];   // staging of the Gram A operand [k~ ; q~] (tf32), copied to TMEM
-    float gramB[4 * 48 * 32];   // Gram B operand; after the Gram MMA, fp32 scratch of the solve
-    float bX[4 * 64 * 32];      // readout B operand [gamma q ; gamma k] (single buffer)
+    float gramB[4 * 32 * 32];   // Gram B operand k e^{Gamma_15 - Gamma}
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
     float tmat[2][32 * 32];     // T diag(beta): B operand of the U' MMA and, negated, of the U MMA
-    float betaS[2][C];
+    float akk[32][33];          // solve scratch: beta-scaled strict lower Akk
+    float tsol[32][33];         //   T = (I + Akk)^{-1}
+    float ysol[16][17];         //   A10 T00
+    float betaS[kBetaRing][C];
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
-    uint64_t bar_tma[2], bar_gram, bar_bxfull, bar_bxempty, bar_x, bar_u, bar_s;
-    uint64_t bar_up[2];         // U' MMA of the chunk with that parity is complete
-    uint64_t bar_akempty[2];
+    uint64_t bar_tma[2], bar_gram[2], bar_bxfull[2], bar_up[2], bar_akempty[2];
+    uint64_t bar_x, bar_u, bar_s, bar_fin[2];
+    uint32_t tma_issued[2];     // stage loads issued / awaited (for the drain after a stop)
+    uint32_t tma_awaited[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -190,8 +198,8 @@ __device__ __forceinline__ bool aborted(TcSmem &sm) {
 }
 
 // ---------------------------------------------------------------------------
-// Preparation warps (0-7): everything of chunk n that does not depend on the
-// state, done while the chain warps run chunk n-1.
+// Preparation warps (0-7): the decay prefix and decay-weighted operands of
+// chunk n and its Gram MMA, done while the chain warps run chunk n-1.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mg,
@@ -200,9 +208,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
     const int P = threadIdx.x;  // 0..255
     const int warp = P >> 5, lane = P & 31, qd = warp & 3, wg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, up_par[2] = {0, 0}, gram_par = 0, bxe_par = 0;
-    bool pend_tma[2] = {false, false}, pend_gram = false;
-    uint32_t pend_tma_par[2] = {0, 0};
+    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, up_par[2] = {0, 0}, gram_par[2] = {0, 0};
     const bool beta_thread = P >= 128 && P < 128 + C;
 
     // beta of chunk 0 (asynchronous 4-byte copies; rows past the end are 0)
@@ -213,10 +219,11 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         cp_async_commit();
     }
     if (P == kTmaIssuer)
-        for (int s = 0; s < 2 && s < nchunks; ++s)
+        for (int s = 0; s < 2 && s < nchunks; ++s) {
             issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C);
+            sm.tma_issued[s] = 1;
+        }
     __syncwarp();
-    for (int s = 0; s < 2; ++s) pend_tma[s] = s < nchunks;
 
     for (int n = 0; n < nchunks; ++n) {
         const int st = n & 1;
@@ -224,14 +231,13 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         const int L = (int)((b - t0) < C ? (b - t0) : C);
         Stage &in = sm.in[st];
 
-        // the chain must be done with chunk n-2 (same parity) before its
-        // buffers (kbaq, tmat, gamC, TMEM U) are overwritten, and the inputs
-        // of chunk n must have landed.  One thread waits; the barrier below
+        // The chain must be done with chunk n-2 (same parity) before its
+        // buffers (kbaq, gamC, Gram TMEM) are overwritten, and the inputs of
+        // chunk n must have landed.  One thread waits; the barrier below
         // releases the others (and orders their reads after the TMA writes).
         if (P == 0) {
             if (n >= 2) wait_phase(sm, &sm.bar_akempty[st], ake_par[st], 32u);
-            pend_tma[st] = !wait_phase(sm, &sm.bar_tma[st], tma_par[st], 1u);
-            pend_tma_par[st] = tma_par[st];   // drained with this parity if still pending
+            if (wait_phase(sm, &sm.bar_tma[st], tma_par[st], 1u)) sm.tma_awaited[st] += 1;
         }
         if (n >= 2) ake_par[st] ^= 1u;
         tma_par[st] ^= 1u;
@@ -239,8 +245,9 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             cp_async_wait_all();   // beta of chunk n has landed
             const int r = P - 128;
             const int64_t tn = t0 + C + r;
-            if (n + 1 < nchunks && tn < b) cp_async4(&sm.betaS[st ^ 1][r], beta + tn * H + h);
-            else sm.betaS[st ^ 1][r] = 0.f;
+            float *dst = &sm.betaS[(n + 1) % kBetaRing][r];
+            if (n + 1 < nchunks && tn < b) cp_async4(dst, beta + tn * H + h);
+            else *dst = 0.f;
             cp_async_commit();
         }
         if (named_sync_or(BAR_PREP, kPrep, aborted(sm))) break;
@@ -266,6 +273,10 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             sm.e1l[c] = __expf(gl - g15);
             sm.gamC[st][c] = __expf(gl);
         }
+        // the Gram MMA of chunk n-1 must be done with its operands (gramB in
+        // shared memory, the A operand in TMEM) before they are rewritten
+        if (P == 0 && n >= 1) wait_phase(sm, &sm.bar_gram[st ^ 1], gram_par[st ^ 1], 2u);
+        if (n >= 1) gram_par[st ^ 1] ^= 1u;
         named_sync(BAR_PREP, kPrep);
 
         // ---- a2: one pass over (token, 4-channel) blocks: Gram operands, Kbar^T, and
@@ -290,37 +301,29 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             const float e01[4] = {e4.x, e4.y, e4.z, e4.w};
             const float e1l[4] = {l4.x, l4.y, l4.z, l4.w};
             float *gA = sm.gramA + kb * 64 * 32;
-            float *gB = sm.gramB + kb * 48 * 32;
+            float *gB = sm.gramB + kb * 32 * 32;
             float *kbq = sm.kbaq[st];
 #pragma unroll
             for (int it = 0; it < 4; ++it) {
                 const int r = (P & 7) + 8 * it;
-                const bool sub1 = it >= 2;            // tokens 16..31
                 const float sc = r < L ? 1.f : 0.f;
                 const float gv[4] = {G[it].x, G[it].y, G[it].z, G[it].w};
-                float ka[4], qa[4], kv[4], kv1[4], kbar[4];
+                float ka[4], qa[4], kv[4], kbar[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const float e1 = __expf(gv[m] - (sub1 ? gref[m] : 0.f));   // [e^-80, 1]
-                    const float inv = __fdividef(1.f, e1);                        // [1, e^80]
+                    const float e1 = __expf(gv[m] - gref[m]);      // e^{Gamma_r - Gamma_15}, [e^-80, e^75]
+                    const float inv = __fdividef(1.f, e1);
                     const float kk = sc * kx[it][m], qq = sc * qx[it][m];
                     ka[m] = kk * e1;
                     qa[m] = qq * e1;
-                    kv[m] = kk * inv;              // k e^{ref - Gamma}
-                    kv1[m] = kv[m] * e01[m];       // k e^{Gamma_15 - Gamma}   (sub-tile 0 keys)
-                    const float gam = sub1 ? e1 * e01[m] : e1;                    // e^{Gamma}
-                    gq[it][m] = qq * gam;
-                    gk[it][m] = kk * gam;
-                    kbar[m] = (sub1 ? kv[m] : kv1[m]) * e1l[m];                  // k e^{Gamma_last - Gamma}
+                    kv[m] = kk * inv;                               // k e^{Gamma_15 - Gamma_r}
+                    gq[it][m] = qa[m] * e01[m];                     // q e^{Gamma_r}
+                    gk[it][m] = ka[m] * e01[m];                     // k e^{Gamma_r}
+                    kbar[m] = kv[m] * e1l[m];                       // k e^{Gamma_last - Gamma_r}
                 }
                 st_op4(gA, r, k4, ka[0], ka[1], ka[2], ka[3]);
                 st_op4(gA, 32 + r, k4, qa[0], qa[1], qa[2], qa[3]);
-                if (!sub1) {
-                    st_op4(gB, r, k4, kv[0], kv[1], kv[2], kv[3]);
-                    st_op4(gB, 16 + r, k4, kv1[0], kv1[1], kv1[2], kv1[3]);
-                } else {
-                    st_op4(gB, 16 + r, k4, kv[0], kv[1], kv[2], kv[3]);
-                }
+                st_op4(gB, r, k4, kv[0], kv[1], kv[2], kv[3]);
 #pragma unroll
                 for (int m = 0; m < 4; ++m) st_op(kbq, c + m, r, kbar[m]);
             }
@@ -330,6 +333,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
 
         // ---- a3: Gram A operand staging -> TMEM (warps 0, 1); V^T -> TMEM (warps 4-7) ----
         if (warp < 2) {
+            tc_fence_after();   // after the Gram MMA of chunk n-1 (awaited above)
             const int r = lane, row = 32 * warp + r;     // warp 0: k~ rows, warp 1: q~ rows
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 16) {
@@ -369,37 +373,12 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             tmem_wait_st();
             tc_fence_before();
         }
-        named_sync(BAR_PREP, kPrep);
-        // the inputs of chunk n are consumed: refill the stage with chunk n+2
-        if (P == kTmaIssuer && n + 2 < nchunks)
-            issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
-        if (n + 2 < nchunks) {   // tracked by thread 0, which waits on (and drains) bar_tma
-            pend_tma[st] = true;
-            pend_tma_par[st] = tma_par[st];
-        }
-        if (P == kGramIssuer) {
-            tc_fence_after();
-            const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                mma_tf32_ts(tb + TM_G, tb + TM_GA + kk * 8,
-                            dB + (uint64_t)(((kk >> 2) * (48 * 128) + (kk & 3) * 32) >> 4),
-                            idesc_tf32(128, 48), kk > 0);
-            mma_commit(&sm.bar_gram);
-        }
-        __syncwarp();
-        if (P == 0) pend_gram = true;
+        named_sync(BAR_PREP, kPrep);   // the inputs of chunk n are consumed
 
-        // ---- readout operand [gamma q ; gamma k], while the Gram runs (single buffer:
-        // the readout MMA of chunk n-1 must have consumed it) ----
-        if (n >= 1) {   // generic stores after the MMA's reads: lane 0 waits, the warp follows
-            if (lane == 0) wait_phase(sm, &sm.bar_bxempty, bxe_par, 4u);
-            bxe_par ^= 1u;
-            __syncwarp();
-        }
+        // ---- readout operand [gamma q ; gamma k] into the chunk's own stage ----
         {
             const int cb = P >> 3, k4 = cb & 7;
-            float *blk = sm.bX + (cb >> 3) * 64 * 32;
+            float *blk = reinterpret_cast<float *>(&in) + (cb >> 3) * 64 * 32;
 #pragma unroll
             for (int it = 0; it < 4; ++it) {
                 const int r = (P & 7) + 8 * it;
@@ -407,49 +386,93 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 st_op4(blk, 32 + r, k4, gk[it][0], gk[it][1], gk[it][2], gk[it][3]);
             }
         }
+        // End of chunk n.  After the barrier thread 0 hands the chunk to the
+        // chain, and the warp that issues the Gram MMA (the issue holds it for
+        // about a microsecond) does so without holding anyone up.
         fence_proxy_async_smem();
+        named_sync(BAR_PREP, kPrep);
+        if (P == 0) mbar_arrive(&sm.bar_bxfull[st]);   // chunk n is ready for the chain
+        if (P == kGramIssuer) {
+            tc_fence_after();
+            const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_tf32_ts(tb + TM_G + 32 * st, tb + TM_GA + kk * 8,
+                            dB + (uint64_t)(((kk >> 2) * (32 * 128) + (kk & 3) * 32) >> 4),
+                            idesc_tf32(128, 32), kk > 0);
+            mma_commit(&sm.bar_gram[st]);
+        }
+        __syncwarp();
+        // (a stop is agreed on by the vote at the top of the next chunk)
+    }
+    if (beta_thread) cp_async_wait_all();
+    if (P == kGramIssuer) {      // every Gram MMA issued here has completed
+        mma_commit(&sm.bar_fin[0]);
+        mbar_wait_bounded(&sm.bar_fin[0], 0, kPollLimit);
+    }
+}
 
-        // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram ----
-        float(*akk)[33] = reinterpret_cast<float(*)[33]>(sm.gramB);
-        if (warp < 2) {
-            if (P == 0) pend_gram = !wait_phase(sm, &sm.bar_gram, gram_par, 2u);
-            gram_par ^= 1u;
+// ---------------------------------------------------------------------------
+// Chain warps (8-11): everything of chunk n from its Gram on.  Thread j owns
+// TMEM lane j = value index j; warps 8 and 9 read the Gram rows (lanes 0-63).
+// ---------------------------------------------------------------------------
+template <typename OUT_T>
+__device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
+                                           const CUtensorMap *mv, const CUtensorMap *mg,
+                                           OUT_T *__restrict__ out, int H, int h,
+                                           int64_t a, int64_t b, int nchunks, uint32_t tb) {
+    const int j = threadIdx.x - kPrep;   // 0..127
+    const int warp = threadIdx.x >> 5, cw = j >> 5, lane = j & 31;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const bool issuer = j == 0;
+    uint32_t bxf_par[2] = {0, 0}, gram_par[2] = {0, 0}, x_par = 0, u_par = 0, s_par = 0;
+
+    for (int n = 0; n < nchunks; ++n) {
+        const int st = n & 1;
+        const int64_t t0 = a + (int64_t)n * C;
+        const int L = (int)((b - t0) < C ? (b - t0) : C);
+        const uint32_t tu = TM_U + 32 * st;
+        const float *betaN = sm.betaS[n % kBetaRing];
+
+        // Chunk n handed over by the preparation warps (its beta, gamma_last,
+        // readout operand, Kbar^T and V^T are in place; the Gram MMA is issued).
+        // The issuer waits; the barriers below release the other threads.
+        if (issuer) wait_phase(sm, &sm.bar_bxfull[st], bxf_par[st], 64u);
+        bxf_par[st] ^= 1u;
+
+        // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram (warps 8, 9) ----
+        if (cw < 2) {
+            if (issuer) wait_phase(sm, &sm.bar_gram[st], gram_par[st], 2u);
+            gram_par[st] ^= 1u;
             named_sync(BAR_E1, 64);
             tc_fence_after();
-            float d0[16], d1[16], d2[16];
-            tmem_ld16x2(tb + lane_off + TM_G, tb + lane_off + TM_G + 16, d0, d1);
-            tmem_ld16(tb + lane_off + TM_G + 32, d2);
+            float d0[16], d1[16];
+            tmem_ld16x2(tb + lane_off + TM_G + 32 * st, tb + lane_off + TM_G + 32 * st + 16, d0, d1);
+            tc_fence_before();
             const int r = lane;
-            if (warp == 0) {
-                const float br = sm.betaS[st][r];
+            if (cw == 0) {
+                const float br = betaN[r];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
-                    akk[r][i] = i < r ? br * val : 0.f;
-                }
+                for (int i = 0; i < 32; ++i) sm.akk[r][i] = i < r ? br * (i < 16 ? d0[i] : d1[i - 16]) : 0.f;
             } else {
-                float a[32];
+                float av[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float val = r < 16 ? (i < 16 ? d0[i] : 0.f) : (i < 16 ? d1[i] : d2[i - 16]);
-                    a[i] = i <= r ? val : 0.f;
-                }
+                for (int i = 0; i < 32; ++i) av[i] = i <= r ? (i < 16 ? d0[i] : d1[i - 16]) : 0.f;
 #pragma unroll
                 for (int i4 = 0; i4 < 8; ++i4)
-                    st_op4(sm.kbaq[st], 128 + r, i4, a[4 * i4], a[4 * i4 + 1], a[4 * i4 + 2], a[4 * i4 + 3]);
+                    st_op4(sm.kbaq[st], 128 + r, i4, av[4 * i4], av[4 * i4 + 1], av[4 * i4 + 2], av[4 * i4 + 3]);
                 fence_proxy_async_smem();
             }
-            tc_fence_before();
         }
-        named_sync(BAR_PREP, kPrep);
+        if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
 
-        // ---- T = (I + Akk)^{-1}, blocked 2 x 2 over 16-token sub-tiles (warps 0-3) ----
-        if (wg == 0) {
-            float(*Tm)[33] = reinterpret_cast<float(*)[33]>(sm.gramB + 32 * 33);
-            float(*Y)[17] = reinterpret_cast<float(*)[17]>(sm.gramB + 2 * 32 * 33);
-            if (warp < 2) {
-                // diagonal blocks by forward substitution: warp 0 -> T00, warp 1 -> T11
-                const int base = 16 * warp, col = lane & 15;
+        // ---- T = (I + Akk)^{-1}, blocked 2 x 2 over 16-token sub-tiles ----
+        {
+            float(*Tm)[33] = sm.tsol;
+            float(*Y)[17] = sm.ysol;
+            if (cw < 2) {
+                // diagonal blocks by forward substitution: warp 8 -> T00, warp 9 -> T11
+                const int base = 16 * cw, col = lane & 15;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) x[r] = r == col ? 1.f : 0.f;
@@ -457,84 +480,51 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 for (int m = 0; m < 15; ++m) {
                     const float xm = x[m];
 #pragma unroll
-                    for (int r = m + 1; r < 16; ++r) x[r] -= akk[base + r][base + m] * xm;
+                    for (int r = m + 1; r < 16; ++r) x[r] -= sm.akk[base + r][base + m] * xm;
                 }
                 if (lane < 16) {
 #pragma unroll
                     for (int r = 0; r < 16; ++r) {
                         Tm[base + r][base + col] = x[r];
-                        if (warp == 0) Tm[r][16 + col] = 0.f;
+                        if (cw == 0) Tm[r][16 + col] = 0.f;
                     }
                 }
             }
-            named_sync(BAR_SOLVE, 128);
+            named_sync(BAR_CHAIN, kChain);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {   // Y = A10 T00
-                const int idx = P + 128 * e, i = idx >> 4, j = idx & 15;
+                const int idx = j + 128 * e, i = idx >> 4, jj = idx & 15;
                 float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc += akk[16 + i][m] * Tm[m][j];
-                Y[i][j] = acc;
+                for (int m = 0; m < 16; ++m) acc += sm.akk[16 + i][m] * Tm[m][jj];
+                Y[i][jj] = acc;
             }
-            named_sync(BAR_SOLVE, 128);
+            named_sync(BAR_CHAIN, kChain);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {   // T10 = -T11 Y
-                const int idx = P + 128 * e, i = idx >> 4, j = idx & 15;
+                const int idx = j + 128 * e, i = idx >> 4, jj = idx & 15;
                 float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc += Tm[16 + i][16 + m] * Y[m][j];
-                Tm[16 + i][j] = -acc;
+                for (int m = 0; m < 16; ++m) acc += Tm[16 + i][16 + m] * Y[m][jj];
+                Tm[16 + i][jj] = -acc;
             }
-            named_sync(BAR_SOLVE, 128);
-            {   // T diag(beta) and its negative, as tf32 operands
-                const int r = P >> 2, c0 = (P & 3) * 8;
+            named_sync(BAR_CHAIN, kChain);
+            {   // T diag(beta) as a tf32 operand
+                const int r = j >> 2, c0 = (j & 3) * 8;
                 float tb8[8];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * sm.betaS[st][c0 + m];
+                for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * betaN[c0 + m];
                 st_op4(sm.tmat[st], r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
                 st_op4(sm.tmat[st], r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
             }
             fence_proxy_async_smem();
         }
-        const bool stop = named_sync_or(BAR_PREP, kPrep, aborted(sm));
-        if (P == 0 && !stop) mbar_arrive(&sm.bar_bxfull);   // chunk n is ready for the chain
-        if (stop) break;
-    }
-    if (beta_thread) cp_async_wait_all();
-    if (aborted(sm)) {   // drain what this thread saw in flight
-        for (int s = 0; s < 2; ++s)
-            if (pend_tma[s] && P == 0) mbar_wait_bounded(&sm.bar_tma[s], pend_tma_par[s], kPollLimit);
-        if (pend_gram && P == 0) mbar_wait_bounded(&sm.bar_gram, gram_par ^ 1u, kPollLimit);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Chain warps (8-11): the state-dependent part of chunk n.  Thread j owns
-// TMEM lane j = value index j.
-// ---------------------------------------------------------------------------
-template <typename OUT_T>
-__device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, int H, int h,
-                                           int64_t a, int64_t b, int nchunks, uint32_t tb) {
-    const int j = threadIdx.x - kPrep;   // 0..127
-    const int warp = threadIdx.x >> 5;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const bool issuer = j == 0;
-    uint32_t bxf_par = 0, x_par = 0, u_par = 0, s_par = 0;
-    bool pend_x = false, pend_u = false, pend_s = false;
-    const uint64_t dX = sdesc_sw128(smem_u32(sm.bX));
-
-    for (int n = 0; n < nchunks; ++n) {
-        const int st = n & 1;
-        const int64_t t0 = a + (int64_t)n * C;
-        const int L = (int)((b - t0) < C ? (b - t0) : C);
-        const uint32_t tu = TM_U + 32 * st;
+        named_sync(BAR_CHAIN, kChain);
 
         // ---- U'^T = V^T (T diag(beta))^T into TMEM U[st], then
         // a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
-        bool issued = false;
         if (issuer) {
-            if (wait_phase(sm, &sm.bar_bxfull, bxf_par, 64u)) {
-                issued = true;
+            if (!aborted(sm)) {
                 tc_fence_after();
                 const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
 #pragma unroll
@@ -543,17 +533,20 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
                                 idesc_tf32(128, 32), kk > 0);
                 mma_commit(&sm.bar_up[st]);   // V^T may be overwritten once this completes
 #pragma unroll
+                const uint64_t dX = sdesc_sw128(smem_u32(&sm.in[st]));   // the chunk's stage
                 for (int kk = 0; kk < 16; ++kk)
                     mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
                                 dX + (uint64_t)(((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4),
                                 idesc_tf32(128, 64), kk > 0);
                 mma_commit(&sm.bar_x);
-                mma_commit(&sm.bar_bxempty);
+                if (wait_phase(sm, &sm.bar_x, x_par, 16u) && n + 2 < nchunks) {
+                    // the stage is free again: refill it with chunk n+2
+                    issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
+                    sm.tma_issued[st] += 1;
+                }
             }
         }
         __syncwarp();
-        bxf_par ^= 1u;
-        if (issued) pend_x = !wait_phase(sm, &sm.bar_x, x_par, 16u);
         x_par ^= 1u;
         if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
         tc_fence_after();
@@ -561,7 +554,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         // ---- a4 (state side): U^T = U'^T - (gamma K S)^T (T diag(beta))^T, accumulated
         // onto U' (same accumulator and issuing thread, so it follows the U' MMA) ----
         if (issuer) {
-            tc_fence_after();
             const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -575,17 +567,19 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         for (int c0 = 0; c0 < D; c0 += 32) {
             float s0[16], s1[16];
             tmem_ld16x2(tb + lane_off + TM_S + c0, tb + lane_off + TM_S + c0 + 16, s0, s1);
+            const float4 *gc = reinterpret_cast<const float4 *>(&sm.gamC[st][c0]);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s0[i] *= sm.gamC[st][c0 + i];
-                s1[i] *= sm.gamC[st][c0 + 16 + i];
+            for (int i4 = 0; i4 < 4; ++i4) {
+                const float4 a4 = gc[i4], b4 = gc[4 + i4];
+                s0[4 * i4] *= a4.x; s0[4 * i4 + 1] *= a4.y; s0[4 * i4 + 2] *= a4.z; s0[4 * i4 + 3] *= a4.w;
+                s1[4 * i4] *= b4.x; s1[4 * i4 + 1] *= b4.y; s1[4 * i4 + 2] *= b4.z; s1[4 * i4 + 3] *= b4.w;
             }
             tmem_st16(tb + lane_off + TM_S + c0, s0);
             tmem_st16(tb + lane_off + TM_S + c0 + 16, s1);
         }
         tmem_wait_st();
         tc_fence_before();
-        if (issuer) pend_u = !wait_phase(sm, &sm.bar_u, u_par, 16u);
+        if (issuer) wait_phase(sm, &sm.bar_u, u_par, 16u);
         u_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
 
@@ -599,9 +593,9 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
                             idesc_tf32(128, 160), 1u);
             mma_commit(&sm.bar_s);
             mma_commit(&sm.bar_akempty[st]);
+            wait_phase(sm, &sm.bar_s, s_par, 16u);
         }
         __syncwarp();
-        if (issuer) pend_s = !wait_phase(sm, &sm.bar_s, s_par, 16u);
         s_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
         tc_fence_after();
@@ -610,7 +604,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         float o0[16], o1[16];
         tmem_ld16x2(tb + lane_off + TM_X, tb + lane_off + TM_X + 16, o0, o1);
         tc_fence_before();
-        named_sync(BAR_CHAIN, kChain);   // X may now be overwritten by the next readout MMA
         OUT_T *dst = out + (t0 * H + h) * (int64_t)D + j;
         const int64_t row = (int64_t)H * D;
 #pragma unroll
@@ -620,10 +613,9 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, OUT_T *__restrict__ out, 
         for (int r = 0; r < 16; ++r)
             if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
     }
-    if (aborted(sm) && issuer) {   // the issuer alone tracks (and drains) the MMA groups
-        if (pend_x) mbar_wait_bounded(&sm.bar_x, x_par ^ 1u, kPollLimit);
-        if (pend_u) mbar_wait_bounded(&sm.bar_u, u_par ^ 1u, kPollLimit);
-        if (pend_s) mbar_wait_bounded(&sm.bar_s, s_par ^ 1u, kPollLimit);
+    if (issuer) {   // every MMA issued here has completed
+        mma_commit(&sm.bar_fin[1]);
+        mbar_wait_bounded(&sm.bar_fin[1], 0, kPollLimit);
     }
 }
 
@@ -653,15 +645,17 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&sm.bar_tma[s], 1);
             mbar_init(&sm.bar_akempty[s], 1);
             mbar_init(&sm.bar_up[s], 1);
+            mbar_init(&sm.bar_gram[s], 1);
+            mbar_init(&sm.bar_bxfull[s], 1);
+            mbar_init(&sm.bar_fin[s], 1);
         }
-        mbar_init(&sm.bar_gram, 1);
-        mbar_init(&sm.bar_bxfull, 1);
-        mbar_init(&sm.bar_bxempty, 1);
         mbar_init(&sm.bar_x, 1);
         mbar_init(&sm.bar_u, 1);
         mbar_init(&sm.bar_s, 1);
         fence_mbar_init();
         sm.abort = 0;
+        sm.tma_issued[0] = sm.tma_issued[1] = 0;
+        sm.tma_awaited[0] = sm.tma_awaited[1] = 0;
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
@@ -698,11 +692,15 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (!chain)
         prep_loop(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb);
     else
-        chain_loop<OUT_T>(sm, out, H, h, a, b, nchunks, tb);
+        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, out, H, h, a, b, nchunks, tb);
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (t == 0)   // after a stop, wait for stage loads still in flight
+        for (int s = 0; s < 2; ++s)
+            if (sm.tma_issued[s] > sm.tma_awaited[s])
+                mbar_wait_bounded(&sm.bar_tma[s], (sm.tma_issued[s] - 1) & 1u, kPollLimit);
     if (!aborted(sm) && final_state && chain) {
         const int j = t - kPrep;
         for (int c0 = 0; c0 < D; c0 += 16) {

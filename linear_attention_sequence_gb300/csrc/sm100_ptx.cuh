@@ -239,6 +239,11 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on a named barrier without waiting (the producer side of a
+// producer/consumer hand-off; the consumers bar.sync with the same count).
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Barrier that also ORs a predicate over the participating threads, so that a
 // decision taken after it is uniform across them.
 __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
