@@ -314,6 +314,30 @@ def run_gpu(args):
                 "traffic": profiled_traffic("kda_prefill_tc_kernel", kernel_src, "prefill_8k"),
                 "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TOKEN * T}
 
+    # ---------------- the same layer with state checkpoints every 1024 tokens ----------------
+    interval = 1024
+    ck = torch.empty((kda.checkpoint_count(T, interval, inp["cu_seqlens"]), w.heads, w.d, w.d),
+                     dtype=torch.float32, device=dev)
+
+    def checkpointed_step():
+        kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     cu_seqlens=inp["cu_seqlens"], interval=interval,
+                                     checkpoints=ck, out=out, final_state=fin, stream=stream)
+
+    ck_steps = max(3, min(args.steps, 20))
+    ms_ck, _, _ = time_steps(checkpointed_step, ck_steps, max(args.warmup, 3), world, stream)
+    ck_bytes = ck.numel() * ck.element_size()
+    ck_ach = (PREFILL_BYTES_PER_TOKEN * T + ck_bytes) / (ms_ck * 1e-3) / 1e9
+    checkpointed = {"value": T * world / (ms_ck * 1e-3), "unit": UNIT, "ms_per_step": ms_ck,
+                    "steps": ck_steps, "interval_tokens": interval,
+                    "checkpoint_bytes_per_step": ck_bytes,
+                    "roofline": {"bound": "hbm", "achieved": ck_ach, "peak": hbm_gbs,
+                                 "unit": "GB/s", "frac": ck_ach / hbm_gbs,
+                                 "peak_source": peak_src, "kernel": "kda_prefill_tc_kernel",
+                                 "algorithmic_bytes_per_launch":
+                                     PREFILL_BYTES_PER_TOKEN * T + ck_bytes}}
+    del ck
+
     # ---------------- e2e through the public API, host buffers ----------------
     host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
     dbuf = {x: torch.empty_like(inp[x]) for x in host}
@@ -387,6 +411,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
+            "checkpointed": checkpointed,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

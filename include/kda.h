@@ -110,6 +110,40 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                        const int32_t *cu_seqlens, void *out, float *final_state,
                        kda_stream_t stream);
 
+/* Chunk length of the prefill kernels; checkpoint intervals are multiples of it. */
+#define KDA_CHUNK 32
+
+/*
+ * kda_prefill_checkpointed -- kda_prefill that also writes state checkpoints.
+ *
+ * Prefix reuse restores the recurrent state at a token boundary from sparse
+ * state checkpoints ("Inside Kimi K3", section "Sequence mixing: fixed-state
+ * KDA alongside global MLA").  Besides everything kda_prefill does, this call
+ * writes the state of every sequence after each `interval` tokens:
+ * checkpoint j (j = 1 .. floor(len_n / interval)) of sequence n is the state
+ * after its first j * interval tokens, i.e. the final_state a prefill over
+ * that prefix alone would return.
+ *
+ *   checkpoints device fp32 [capacity, H, d_k, d_v], 4-byte aligned.  Sequence n
+ *               uses rows base_n .. base_n + floor(len_n / interval) - 1 with
+ *               base_n = sum over m < n of floor(len_m / interval).  Rows at
+ *               or beyond `capacity` are not written; checkpoints may be NULL
+ *               only with capacity 0 (then this is kda_prefill).
+ *   interval    tokens between checkpoints: a positive multiple of KDA_CHUNK.
+ *   capacity    number of rows the caller allocated (>= 0).
+ *
+ * Every other argument, and every other error, is as in kda_prefill;
+ * KDA_ERR_INVALID_ARGUMENT if interval is not a positive multiple of
+ * KDA_CHUNK, capacity < 0, or checkpoints is NULL or misaligned while
+ * capacity > 0.  The checkpoint stores add 4 d_k d_v bytes per checkpoint
+ * and head to the prefill's traffic.
+ */
+kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, float *checkpoints,
+                                    int64_t interval, int64_t capacity, kda_stream_t stream);
+
 /*
  * kda_decode -- one single-token update of N independent fixed-size states.
  *

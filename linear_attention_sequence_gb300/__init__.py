@@ -7,6 +7,7 @@ same names and raises on a non-OK status.  It performs no arithmetic of the
 method and has no fallback: if the library is missing, every call raises.
 
     kda_prefill(q, k, v, g, beta, ...)  chunk-parallel prefill, packed batch
+    kda_prefill_checkpointed(...)       the same, plus state checkpoints every `interval` tokens
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -16,7 +17,7 @@ import os
 
 import torch
 
-__all__ = ["KdaError", "kda_prefill", "kda_decode", "kda_status_string", "lib", "library_path",
+__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -26,6 +27,7 @@ _LIB_PATH = os.path.join(_HERE, "libkda.so")
 KDA_OK = 0
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PREFILL_DEFAULT, PREFILL_FP32, PREFILL_TC = 0, 1, 2
+CHUNK = 32   # chunk length of the prefill kernels (KDA_CHUNK)
 _DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
 
 
@@ -62,6 +64,9 @@ def lib():
         vp, fp = ctypes.c_void_p, ctypes.c_void_p
         L.kda_prefill.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp, fp, vp]
         L.kda_prefill.restype = ctypes.c_int
+        L.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp,
+                                               fp, fp, ctypes.c_int64, ctypes.c_int64, vp]
+        L.kda_prefill_checkpointed.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -120,16 +125,8 @@ def _require(t, name, dtype=None, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims")
 
 
-def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,
-                out=None, final_state=None, out_dtype=None, variant=PREFILL_DEFAULT,
-                return_final_state=True, stream=None):
-    """Chunked KDA prefill (C entry point ``kda_prefill``).
-
-    q, k [T, H, d_k] and v [T, H, d_v] in fp32 or bf16; g [T, H, d_k] fp32;
-    beta [T, H] fp32; init_state [N, H, d_k, d_v] fp32 or None; cu_seqlens
-    int32 [N+1] (device) or None (``num_seqs`` equal-length sequences,
-    default 1).  Returns ``(out, final_state)``.
-    """
+def _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs, out, final_state,
+                  out_dtype, variant, return_final_state):
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _require(t, n, ndim=3)
     _require(g, "g", torch.float32, 3)
@@ -154,6 +151,56 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     _require(final_state, "final_state", torch.float32, 4)
     dims = Dims(N, T, H, dk, dv, _DTYPES[q.dtype], _DTYPES[out_dtype], int(variant))
+    return dims, out, final_state
+
+
+def checkpoint_count(total_tokens, interval, cu_seqlens=None, num_seqs=1):
+    """Rows kda_prefill_checkpointed writes: sum over sequences of
+    floor(length / interval) (cu_seqlens is copied to the host to count)."""
+    if cu_seqlens is not None:
+        cu = cu_seqlens.detach().to("cpu").tolist()
+        return sum(max(0, b - a) // interval for a, b in zip(cu[:-1], cu[1:]))
+    return int(num_seqs) * ((total_tokens // max(1, int(num_seqs))) // interval)
+
+
+def kda_prefill_checkpointed(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, interval,
+                             num_seqs=None, checkpoints=None, out=None, final_state=None,
+                             out_dtype=None, variant=PREFILL_DEFAULT, return_final_state=True,
+                             stream=None):
+    """Prefill that also writes the state after every `interval` tokens of each
+    sequence (C entry point ``kda_prefill_checkpointed``).  Returns
+    ``(out, final_state, checkpoints)``; checkpoints [rows, H, d_k, d_v] fp32,
+    sequence by sequence (see include/kda.h)."""
+    dims, out, final_state = _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs,
+                                           out, final_state, out_dtype, variant,
+                                           return_final_state)
+    if checkpoints is None:
+        rows = checkpoint_count(q.shape[0], int(interval), cu_seqlens, dims.num_seqs)
+        checkpoints = torch.empty((rows, q.shape[1], q.shape[2], v.shape[2]),
+                                  dtype=torch.float32, device=q.device)
+    _require(checkpoints, "checkpoints", torch.float32, 4)
+    st = lib().kda_prefill_checkpointed(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                                        _ptr(out), _ptr(final_state),
+                                        _ptr(checkpoints) if checkpoints.numel() else None,
+                                        int(interval), int(checkpoints.shape[0]), _stream(stream))
+    _check(st, "kda_prefill_checkpointed")
+    return out, final_state, checkpoints
+
+
+def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,
+                out=None, final_state=None, out_dtype=None, variant=PREFILL_DEFAULT,
+                return_final_state=True, stream=None):
+    """Chunked KDA prefill (C entry point ``kda_prefill``).
+
+    q, k [T, H, d_k] and v [T, H, d_v] in fp32 or bf16; g [T, H, d_k] fp32;
+    beta [T, H] fp32; init_state [N, H, d_k, d_v] fp32 or None; cu_seqlens
+    int32 [N+1] (device) or None (``num_seqs`` equal-length sequences,
+    default 1).  Returns ``(out, final_state)``.
+    """
+    dims, out, final_state = _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs,
+                                           out, final_state, out_dtype, variant,
+                                           return_final_state)
     st = lib().kda_prefill(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                            _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                            _stream(stream))

@@ -76,10 +76,13 @@ kda_status kda_get_last_device_error(kda_stream_t stream) {
     return status ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
-kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const void *v,
-                       const float *g, const float *beta, const float *init_state,
-                       const int32_t *cu_seqlens, void *out, float *final_state,
-                       kda_stream_t stream) {
+namespace {
+
+kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, const float *init_state,
+                          const int32_t *cu_seqlens, void *out, float *final_state,
+                          float *ckpt, int64_t ckpt_interval, int64_t ckpt_capacity,
+                          kda_stream_t stream, const char *where) {
     kda::Problem P;
     kda_status st = check_dims(dims, P);
     if (st != KDA_OK) return st;
@@ -95,6 +98,9 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
         const size_t bytes = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
         if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;
     }
+    P.ckpt = ckpt_capacity > 0 ? ckpt : nullptr;
+    P.ckpt_interval = ckpt_interval;
+    P.ckpt_capacity = ckpt_capacity;
     const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, g);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
@@ -104,8 +110,30 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                                                    out, final_state, s)
                            : kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                      out, final_state, s);
-    if (e != cudaSuccess) return cuda_fail(e, "kda_prefill");
+    if (e != cudaSuccess) return cuda_fail(e, where);
     return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const float *init_state,
+                       const int32_t *cu_seqlens, void *out, float *final_state,
+                       kda_stream_t stream) {
+    return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                          nullptr, 0, 0, stream, "kda_prefill");
+}
+
+kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, float *checkpoints,
+                                    int64_t interval, int64_t capacity, kda_stream_t stream) {
+    if (interval <= 0 || interval % KDA_CHUNK != 0 || capacity < 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (capacity > 0 && (!checkpoints || ((uintptr_t)checkpoints & 3u)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                          checkpoints, interval, capacity, stream, "kda_prefill_checkpointed");
 }
 
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,

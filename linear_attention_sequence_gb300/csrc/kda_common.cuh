@@ -37,7 +37,25 @@ struct Problem {
     int32_t N, T, H, dk, dv;
     int32_t in_dtype, out_dtype, variant;
     int64_t seq_len;  // used when cu_seqlens == NULL
+    // state checkpoints (kda_prefill_checkpointed); ckpt == nullptr: none
+    float *ckpt = nullptr;
+    int64_t ckpt_interval = 0;  // tokens between checkpoints, a multiple of the chunk length
+    int64_t ckpt_capacity = 0;  // rows of [capacity, H, d_k, d_v] that may be written
 };
+
+// Row of the first checkpoint of sequence n: the checkpoints of the earlier
+// sequences come first, floor(length / interval) of them each.
+__device__ __forceinline__ int64_t ckpt_first_row(const int32_t *cu, int n, int64_t total,
+                                                  int64_t seq_len, int64_t interval) {
+    if (!cu) return (int64_t)n * (seq_len / interval);
+    int64_t row = 0;
+    for (int m = 0; m < n; ++m) {
+        int64_t a, b;
+        seq_bounds(cu, m, total, seq_len, a, b);
+        row += (b - a) / interval;
+    }
+    return row;
+}
 
 }  // namespace kda
 

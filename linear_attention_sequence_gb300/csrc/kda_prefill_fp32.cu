@@ -57,7 +57,8 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                         const float *__restrict__ beta, const float *__restrict__ init_state,
                         const int32_t *__restrict__ cu, OUT_T *__restrict__ out,
                         float *__restrict__ final_state, int H, int DV, int64_t total,
-                        int64_t seq_len) {
+                        int64_t seq_len, float *__restrict__ ckpt, int64_t ckpt_every,
+                        int64_t ckpt_cap) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<DK, C> &sm = *reinterpret_cast<Smem<DK, C> *>(smem_raw);
 
@@ -75,7 +76,10 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     }
 
     const int64_t rowK = (int64_t)H * DK, rowV = (int64_t)H * DV;
-    for (int64_t t0 = a; t0 < b; t0 += C) {
+    // state checkpoints: after every ckpt_every chunks that end inside the sequence
+    const int64_t ck_row0 = ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0;
+    int64_t chunk = 0;
+    for (int64_t t0 = a; t0 < b; t0 += C, ++chunk) {
         const int L = (int)((b - t0) < C ? (b - t0) : C);
         __syncthreads();  // previous chunk done with every buffer
         // ---- load the chunk (rows >= L are zeros) ----
@@ -198,6 +202,17 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             for (int r = 0; r < C; ++r) acc += sm.K[r][c] * sm.U[r][lane];
             sm.S[c][lane] = acc;
         }
+        if (ckpt && (chunk + 1) % ckpt_every == 0 && t0 + C <= b) {
+            const int64_t row = ck_row0 + (chunk + 1) / ckpt_every - 1;
+            if (row < ckpt_cap) {
+                __syncthreads();
+                const int64_t off = (row * H + h) * DK * (int64_t)DV;
+                for (int idx = t; idx < DK * BV; idx += kThreads) {
+                    const int c = idx / BV, j = idx % BV;
+                    ckpt[off + (int64_t)c * DV + j0 + j] = sm.S[c][j];
+                }
+            }
+        }
     }
     __syncthreads();
     if (final_state) {
@@ -220,7 +235,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     dim3 grid(P.dv / BV, P.H, P.N);
     kern<<<grid, kThreads, smem, stream>>>((const IN_T *)q, (const IN_T *)k, (const IN_T *)v, g,
                                            beta, init_state, cu, (OUT_T *)out, final_state, P.H,
-                                           P.dv, (int64_t)P.T, P.seq_len);
+                                           P.dv, (int64_t)P.T, P.seq_len, P.ckpt,
+                                           P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity);
     return cudaGetLastError();
 }
 

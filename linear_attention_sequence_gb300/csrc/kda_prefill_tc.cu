@@ -120,9 +120,7 @@ struct alignas(1024) TcSmem {
     float gramB[4 * 32 * 32];   // Gram B operand k e^{Gamma_15 - Gamma}
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
     float tmat[2][32 * 32];     // T diag(beta): B operand of the U' MMA and, negated, of the U MMA
-    float akk[32][33];          // solve scratch: beta-scaled strict lower Akk
-    float tsol[32][33];         //   T = (I + Akk)^{-1}
-    float ysol[16][17];         //   A10 T00
+    float akkT[32][32];         // solve scratch: (beta-scaled strict lower Akk)^T
     float betaS[kBetaRing][C];
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
@@ -420,7 +418,9 @@ template <typename OUT_T>
 __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                            const CUtensorMap *mv, const CUtensorMap *mg,
                                            OUT_T *__restrict__ out, int H, int h,
-                                           int64_t a, int64_t b, int nchunks, uint32_t tb) {
+                                           int64_t a, int64_t b, int nchunks, uint32_t tb,
+                                           float *__restrict__ ckpt, int64_t ckpt_every,
+                                           int64_t ckpt_cap, int64_t ck_row0) {
     const int j = threadIdx.x - kPrep;   // 0..127
     const int warp = threadIdx.x >> 5, cw = j >> 5, lane = j & 31;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -451,9 +451,36 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             tc_fence_before();
             const int r = lane;
             if (cw == 0) {
+                // Akk^T[m][r] = beta_r Gram[r][m] for m < r (row m of Akk^T is contiguous)
                 const float br = betaN[r];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sm.akk[r][i] = i < r ? br * (i < 16 ? d0[i] : d1[i - 16]) : 0.f;
+                for (int m = 0; m < 32; ++m)
+                    sm.akkT[m][r] = m < r ? br * (m < 16 ? d0[m] : d1[m - 16]) : 0.f;
+                __syncwarp();
+                // T = (I + Akk)^{-1}: lane j computes column j by forward
+                // substitution, one row of Akk^T (a broadcast) per step
+                const int jc = lane;
+                float x[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = i == jc ? 1.f : 0.f;
+#pragma unroll
+                for (int m = 0; m < 31; ++m) {
+                    const float xm = x[m];
+                    const float4 *row = reinterpret_cast<const float4 *>(sm.akkT[m]);
+#pragma unroll
+                    for (int q4 = (m + 1) >> 2; q4 < 8; ++q4) {
+                        const float4 a4 = row[q4];
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * q4 + e > m) x[4 * q4 + e] -= av[e] * xm;
+                    }
+                }
+                // T diag(beta) as a tf32 operand: row i, column jc
+                const float bj = betaN[jc];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) st_op(sm.tmat[st], i, jc, x[i] * bj);
+                fence_proxy_async_smem();
             } else {
                 float av[32];
 #pragma unroll
@@ -465,61 +492,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             }
         }
         if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
-
-        // ---- T = (I + Akk)^{-1}, blocked 2 x 2 over 16-token sub-tiles ----
-        {
-            float(*Tm)[33] = sm.tsol;
-            float(*Y)[17] = sm.ysol;
-            if (cw < 2) {
-                // diagonal blocks by forward substitution: warp 8 -> T00, warp 9 -> T11
-                const int base = 16 * cw, col = lane & 15;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = r == col ? 1.f : 0.f;
-#pragma unroll
-                for (int m = 0; m < 15; ++m) {
-                    const float xm = x[m];
-#pragma unroll
-                    for (int r = m + 1; r < 16; ++r) x[r] -= sm.akk[base + r][base + m] * xm;
-                }
-                if (lane < 16) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        Tm[base + r][base + col] = x[r];
-                        if (cw == 0) Tm[r][16 + col] = 0.f;
-                    }
-                }
-            }
-            named_sync(BAR_CHAIN, kChain);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {   // Y = A10 T00
-                const int idx = j + 128 * e, i = idx >> 4, jj = idx & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc += sm.akk[16 + i][m] * Tm[m][jj];
-                Y[i][jj] = acc;
-            }
-            named_sync(BAR_CHAIN, kChain);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {   // T10 = -T11 Y
-                const int idx = j + 128 * e, i = idx >> 4, jj = idx & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc += Tm[16 + i][16 + m] * Y[m][jj];
-                Tm[16 + i][jj] = -acc;
-            }
-            named_sync(BAR_CHAIN, kChain);
-            {   // T diag(beta) as a tf32 operand
-                const int r = j >> 2, c0 = (j & 3) * 8;
-                float tb8[8];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) tb8[m] = Tm[r][c0 + m] * betaN[c0 + m];
-                st_op4(sm.tmat[st], r, c0 >> 2, tb8[0], tb8[1], tb8[2], tb8[3]);
-                st_op4(sm.tmat[st], r, (c0 >> 2) + 1, tb8[4], tb8[5], tb8[6], tb8[7]);
-            }
-            fence_proxy_async_smem();
-        }
-        named_sync(BAR_CHAIN, kChain);
 
         // ---- U'^T = V^T (T diag(beta))^T into TMEM U[st], then
         // a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
@@ -612,6 +584,22 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
 #pragma unroll
         for (int r = 0; r < 16; ++r)
             if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
+
+        // ---- state checkpoint after every ckpt_every chunks that end inside the
+        // sequence: S (after this chunk's carry) from TMEM, thread j writes column j ----
+        if (ckpt && (n + 1) % ckpt_every == 0 && L == C) {
+            const int64_t ck = ck_row0 + (n + 1) / ckpt_every - 1;
+            if (ck < ckpt_cap) {
+                float *dstS = ckpt + (ck * H + h) * (int64_t)D * D + j;
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float sv[16];
+                    tmem_ld16(tb + lane_off + TM_S + c0, sv);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dstS[(int64_t)(c0 + i) * D] = sv[i];
+                }
+                tc_fence_before();
+            }
+        }
     }
     if (issuer) {   // every MMA issued here has completed
         mma_commit(&sm.bar_fin[1]);
@@ -627,7 +615,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_g, const float *__restrict__ beta,
                       const float *__restrict__ init_state, const int32_t *__restrict__ cu,
                       OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
-                      int64_t total, int64_t seq_len) {
+                      int64_t total, int64_t seq_len, float *__restrict__ ckpt,
+                      int64_t ckpt_every, int64_t ckpt_cap) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Round up to 1024 bytes by pointer arithmetic on the shared array itself
     // (an integer round trip would lose the shared address space and turn
@@ -692,7 +681,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (!chain)
         prep_loop(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb);
     else
-        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, out, H, h, a, b, nchunks, tb);
+        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, out, H, h, a, b, nchunks, tb, ckpt,
+                          ckpt_every, ckpt_cap,
+                          ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0);
 
     tc_fence_before();
     __syncthreads();
@@ -770,7 +761,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((int64_t)P.N * P.H);
     kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, beta, init_state, cu, (OUT_T *)out,
-                                             final_state, P.H, (int64_t)P.T, P.seq_len);
+                                             final_state, P.H, (int64_t)P.T, P.seq_len, P.ckpt,
+                                             P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity);
     return cudaGetLastError();
 }
 

@@ -109,6 +109,49 @@ def test_prefill_rejects(L, dims, over, want):
     assert prefill(L, dims, **over) == want
 
 
+def prefill_ckpt(L, dims, interval=64, capacity=2, ckpt=ctypes.c_void_p(0x50000), **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, init=None, cu=None,
+                out=ctypes.c_void_p(0x20000), fin=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_prefill_checkpointed(d, args["q"], args["k"], args["v"], args["g"], args["beta"],
+                                      args["init"], args["cu"], args["out"], args["fin"], ckpt,
+                                      interval, capacity, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(interval=0), INVALID),
+    (dict(interval=-32), INVALID),
+    (dict(interval=48), INVALID),                 # not a multiple of the chunk length
+    (dict(interval=1), INVALID),
+    (dict(capacity=-1), INVALID),
+    (dict(ckpt=None), INVALID),                   # rows requested but no buffer
+    (dict(ckpt=ctypes.c_void_p(0x50002)), INVALID),   # misaligned
+])
+def test_prefill_checkpointed_rejects(L, kw, want):
+    assert prefill_ckpt(L, D(), **kw) == want
+
+
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(), {"q": None}), (D(num_seqs=3, total_tokens=16), {}),
+])
+def test_prefill_checkpointed_validates_like_prefill(L, dims, over):
+    assert prefill_ckpt(L, dims, **over) == INVALID
+
+
+def test_prefill_checkpointed_empty_batch_is_ok(L):
+    assert prefill_ckpt(L, D(num_seqs=0, total_tokens=0), capacity=0, ckpt=None, q=None, k=None,
+                        v=None, g=None, beta=None, out=None) == OK
+
+
+def test_checkpoint_count():
+    cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
+    assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6
+    assert kda.checkpoint_count(364, 64, cu) == 1 + 1 + 0 + 3
+    assert kda.checkpoint_count(256, 64, None, num_seqs=2) == 4
+    assert kda.checkpoint_count(0, 32, None, num_seqs=0) == 0
+
+
 def test_prefill_empty_batch_is_ok(L):
     # nothing to do: no sequences, no tokens -> OK without touching the device
     assert prefill(L, D(num_seqs=0, total_tokens=0), q=None, k=None, v=None, g=None,

@@ -101,3 +101,23 @@ def test_decode_256x64_all_pairs():
     es = rel_err(host64(st), ref)
     print(f"decode_256x64: err_o {eo:.3e} err_S {es:.3e}")
     assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+
+
+def test_prefill_8k_checkpoints_match_prefix_runs():
+    """Full-size layer with a checkpoint every 1024 tokens: the outputs equal
+    the plain prefill's, and checkpoints 1, 4 and 8 equal (bitwise) the final
+    states of prefills over the first 1024, 4096 and 8192 tokens."""
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, "cuda")
+    out, fin, ck = kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"],
+                                                inp["beta"], cu_seqlens=inp["cu_seqlens"],
+                                                interval=1024)
+    assert ck.shape == (8, w.heads, w.d, w.d)
+    out0, fin0 = kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                 cu_seqlens=inp["cu_seqlens"])
+    assert torch.equal(out, out0) and torch.equal(fin, fin0)
+    assert torch.equal(ck[7], fin0[0])
+    for j in (1, 4):
+        n = 1024 * j
+        _, fin_p = kda.kda_prefill(*(inp[x][:n].contiguous() for x in ("q", "k", "v", "g", "beta")))
+        assert torch.equal(ck[j - 1], fin_p[0]), f"checkpoint {j}"

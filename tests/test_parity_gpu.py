@@ -218,3 +218,83 @@ def test_prefill_equals_decode_steps(variant):
     tol = TOL[dtype]
     assert rel_err(host64(out), host64(dec)) <= tol
     assert rel_err(host64(fin), host64(st)) <= tol
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("split", [97, 128])
+def test_split_sequence_carries_state(variant, split):
+    """Prefill over [0, T) equals prefill over [0, T1) followed by prefill over
+    [T1, T) started from the first call's final state (chunk-aligned and
+    ragged split points)."""
+    T, H, d = 300, 2, 128
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=31, device=DEV, init_std=0.05)
+    out, fin = run_gpu(inp, variant)
+    a = {x: inp[x][:split].contiguous() for x in ("q", "k", "v", "g", "beta")}
+    b = {x: inp[x][split:].contiguous() for x in ("q", "k", "v", "g", "beta")}
+    a["init_state"] = inp["init_state"]
+    out_a, fin_a = run_gpu(a, variant)
+    b["init_state"] = fin_a
+    out_b, fin_b = run_gpu(b, variant)
+    tol = TOL[dtype]
+    assert rel_err(host64(torch.cat([out_a, out_b])), host64(out)) <= tol
+    assert rel_err(host64(fin_b), host64(fin)) <= tol
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_packed_batch_equals_sequences_run_alone(variant):
+    """A packed batch gives, for every sequence, exactly what that sequence
+    gives alone: each (sequence, head) is computed independently and the same
+    way whatever its position in the packed batch."""
+    H, d = 2, 128
+    lens = [45, 96, 1, 130]
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=41, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    out, fin = run_gpu(inp, variant, cu=cu)
+    for n, (t0, t1) in enumerate(zip(cu[:-1].tolist(), cu[1:].tolist())):
+        one = {x: inp[x][t0:t1].contiguous() for x in ("q", "k", "v", "g", "beta")}
+        one["init_state"] = inp["init_state"][n:n + 1].contiguous()
+        o1, f1 = run_gpu(one, variant)
+        assert torch.equal(o1, out[t0:t1]), f"sequence {n}: outputs differ"
+        assert torch.equal(f1, fin[n:n + 1]), f"sequence {n}: final states differ"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("interval", [32, 64])
+def test_checkpoints_equal_prefix_final_states(variant, interval):
+    """kda_prefill_checkpointed: outputs and final states are those of
+    kda_prefill, and checkpoint j of a sequence is exactly the final state of a
+    prefill over its first j * interval tokens (checked bitwise against the
+    GPU and within the bound against the oracle)."""
+    H, d = 2, 128
+    lens = [100, 64, 0, 161]
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    inp = synth.random_inputs(sum(lens), H, d, dtype=dtype, seed=51, device=DEV,
+                              num_seqs=len(lens), init_std=0.05)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    try:
+        out, fin, ck = kda.kda_prefill_checkpointed(
+            inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], init_state=inp["init_state"],
+            cu_seqlens=cu, interval=interval, out_dtype=torch.float32, variant=variant)
+    except kda.KdaError as e:
+        if e.status == 2:
+            pytest.skip("variant does not take this shape/dtype (KDA_ERR_UNSUPPORTED)")
+        raise
+    out0, fin0 = run_gpu(inp, variant, cu=cu)
+    assert torch.equal(out, out0) and torch.equal(fin, fin0)
+    row = 0
+    for n, (t0, t1) in enumerate(zip(cu[:-1].tolist(), cu[1:].tolist())):
+        for j in range(1, (t1 - t0) // interval + 1):
+            pre = {x: inp[x][t0:t0 + j * interval].contiguous()
+                   for x in ("q", "k", "v", "g", "beta")}
+            pre["init_state"] = inp["init_state"][n:n + 1].contiguous()
+            _, fin_p = run_gpu(pre, variant)
+            assert torch.equal(ck[row], fin_p[0]), f"sequence {n}, checkpoint {j}"
+            if j == (t1 - t0) // interval:
+                _, s_ref = run_oracle(pre)
+                assert rel_err(host64(ck[row]), s_ref[0]) <= TOL[dtype]
+            row += 1
+    assert row == ck.shape[0]
