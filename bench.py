@@ -76,7 +76,7 @@ def barrier(world: int):
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms in the background; samples are tagged
+    """nvidia-smi sampled every 50 ms in the background; samples are tagged
     with wall time so that those inside the timed region can be picked."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -93,7 +93,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -124,7 +124,7 @@ class ClockSampler:
         note = None
         if not inside:  # region shorter than the sampling period: take the nearest
             near = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
-            inside, note = [near[1]], "nearest sample (timed region shorter than 100 ms)"
+            inside, note = [near[1]], "nearest sample (timed region shorter than 50 ms)"
 
         def num(x):
             try:
@@ -456,7 +456,7 @@ def run_profile_case(args, kda, synth, dev, stream):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
