@@ -55,6 +55,8 @@ class Oracle:
         lib.kda_oracle_decode.argtypes = [i32, i32, i32, i32, dp, dp, dp, dp, dp, dp, dp, i32]
         lib.kda_oracle_decode.restype = ctypes.c_int
         lib.kda_oracle_num_cpus.restype = ctypes.c_int
+        lib.kda_oracle_gate.argtypes = [i32, i32, i32, dp, dp, dp, dp, dp]
+        lib.kda_oracle_gate.restype = ctypes.c_int
         self.lib = lib
 
     def num_cpus(self) -> int:
@@ -88,6 +90,18 @@ class Oracle:
             raise ValueError("kda_oracle_prefill rejected its arguments (shapes, "
                              "cu_seqlens, or gates outside g in [-5,0], beta in [0,1])")
         return out, fin
+
+    def gate(self, z, a_log, beta_logit):
+        """g [T, H, d_k] and beta [T, H] (fp64) from the decay logits z
+        [T, H, d_k], the per-head log-scales a_log [H] and the beta logits
+        [T, H] (C function ``kda_oracle_gate``)."""
+        z, a_log, bl = _f64(z), _f64(a_log), _f64(beta_logit)
+        T, H, dk = z.shape
+        assert a_log.shape == (H,) and bl.shape == (T, H)
+        g = np.empty_like(z)
+        beta = np.empty_like(bl)
+        self.lib.kda_oracle_gate(T, H, dk, _ptr(z), _ptr(a_log), _ptr(bl), _ptr(g), _ptr(beta))
+        return g, beta
 
     def decode(self, q, k, v, g, beta, state, num_threads: int = 0, inplace: bool = False):
         """One decode step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
@@ -138,6 +152,10 @@ def _ptr(a, ctype=ctypes.c_double):
 def prefill(*args, **kwargs):
     """Module-level form of :meth:`Oracle.prefill` on the default build."""
     return _load().prefill(*args, **kwargs)
+
+
+def gate(*args, **kwargs):
+    return _load().gate(*args, **kwargs)
 
 
 def decode(*args, **kwargs):

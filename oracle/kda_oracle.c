@@ -190,6 +190,28 @@ int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads
     return rc;
 }
 
+/* Gate prologue.  "Understanding Kimi K3's Attention": the log-decay bound
+ * equation g_t = g_min Sigmoid(e^{A_h} z_t) (per key channel; A_h the
+ * per-head log-scale of the symbol table, z_t the decay logit), and the
+ * write strength beta_t = Sigmoid(W_beta x_t) of the symbol table, here from
+ * its logit.  Sigmoid(x) = 1 / (1 + e^{-x}); for very negative x, e^{-x}
+ * overflows to infinity and the quotient is 0, its limit. */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+int kda_oracle_gate(int32_t total_tokens, int32_t num_heads, int32_t d_k, const double *z,
+                    const double *a_log, const double *beta_logit, double *g, double *beta) {
+    for (int64_t t = 0; t < total_tokens; ++t)
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const double scale = exp(a_log[h]);
+            for (int32_t c = 0; c < d_k; ++c) {
+                const int64_t i = (t * num_heads + h) * (int64_t)d_k + c;
+                g[i] = KDA_ORACLE_G_MIN * sigmoid(scale * z[i]);
+            }
+            beta[t * num_heads + h] = sigmoid(beta_logit[t * num_heads + h]);
+        }
+    return 0;
+}
+
 int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                       const double *q, const double *k, const double *v,
                       const double *g, const double *beta, double *state_inout,

@@ -33,6 +33,12 @@ int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t 
                       const double *g, const double *beta, double *state_inout,
                       double *out, int32_t num_threads);
 
+/* Gate prologue: for every token t, head h and key channel c,
+ * g[t,h,c] = g_min Sigmoid(e^{a_log[h]} z[t,h,c]) with g_min = -5, and
+ * beta[t,h] = Sigmoid(beta_logit[t,h]).  Returns 0. */
+int kda_oracle_gate(int32_t total_tokens, int32_t num_heads, int32_t d_k, const double *z,
+                    const double *a_log, const double *beta_logit, double *g, double *beta);
+
 #ifdef __cplusplus
 }
 #endif

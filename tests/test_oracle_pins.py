@@ -192,8 +192,38 @@ def pin_norm_bound(orc):
         S = S_next
 
 
+def pin_gate_closed_forms(orc):
+    """Gate prologue, g = g_min Sigmoid(e^{A_h} z) and beta = Sigmoid(logit)
+    ("Understanding Kimi K3's Attention", log-decay bound and symbol table):
+    - z = 0 gives g_min / 2 exactly, and a zero logit gives beta = 1/2;
+    - with A_h = ln 2 and z = ln(3) / 2, Sigmoid(ln 3) = 3/4, so g = -3.75;
+    - g tends to g_min as z grows and to 0 as z falls (alpha -> 1);
+    - g(z) + g(-z) = g_min for any A_h;
+    - a logit of ln 3 gives beta = 3/4."""
+    T, H, dk = 3, 2, 4
+    z = np.zeros((T, H, dk))
+    z[1, 0, :] = np.log(3.0) / 2
+    z[2, 1, 0], z[2, 1, 1] = 60.0, -800.0
+    a_log = np.array([np.log(2.0), 0.0])
+    bl = np.zeros((T, H))
+    bl[1, 1] = np.log(3.0)
+    g, beta = orc.gate(z, a_log, bl)
+    assert np.all(g[0] == -2.5) and beta[0, 0] == 0.5
+    assert abs(g[1, 0, 0] - (-3.75)) < 1e-14
+    assert abs(beta[1, 1] - 0.75) < 1e-15
+    assert abs(g[2, 1, 0] - (-5.0)) < 1e-14 and g[2, 1, 1] == 0.0
+    rng = np.random.default_rng(5)
+    zr = rng.normal(0.0, 3.0, (5, H, dk))
+    a2 = rng.normal(0.0, 0.5, H)
+    gp, _ = orc.gate(zr, a2, np.zeros((5, H)))
+    gm, _ = orc.gate(-zr, a2, np.zeros((5, H)))
+    assert np.allclose(gp + gm, -5.0, rtol=0, atol=1e-14)
+    assert np.all((gp > -5.0) & (gp < 0.0))
+
+
 PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
-        pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound]
+        pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound,
+        pin_gate_closed_forms]
 
 
 def _run_pin(pin, orc, golden):
@@ -300,6 +330,12 @@ MUTANTS = {
     "read_before_write": ("ot[j] += S[i * dv + j] * qt[i];",
                           "ot[j] += (S[i * dv + j] - kt[i] * u[j]) * qt[i];"),
     "write_with_q": ("S[i * dv + j] += kt[i] * u[j];", "S[i * dv + j] += qt[i] * u[j];"),
+    "gate_scale_dropped": ("g[i] = KDA_ORACLE_G_MIN * sigmoid(scale * z[i]);",
+                           "g[i] = KDA_ORACLE_G_MIN * sigmoid(z[i]);"),
+    "gate_sign": ("g[i] = KDA_ORACLE_G_MIN * sigmoid(scale * z[i]);",
+                  "g[i] = KDA_ORACLE_G_MIN * sigmoid(-scale * z[i]);"),
+    "gate_beta_raw": ("beta[t * num_heads + h] = sigmoid(beta_logit[t * num_heads + h]);",
+                      "beta[t * num_heads + h] = beta_logit[t * num_heads + h];"),
 }
 
 
