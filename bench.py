@@ -36,6 +36,8 @@ UNIT = "tokens/s"
 # Algorithmic bytes per token of one 96-head layer (prefill): q, k, v, o bf16
 # (4 x 96 x 128 x 2) + g fp32 (96 x 128 x 4) + beta fp32 (96 x 4).
 PREFILL_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 96 * 128 * 4 + 96 * 4  # 147840
+# the gated call reads bf16 decay logits z instead of fp32 g, and beta logits
+GATED_BYTES_PER_TOKEN = 5 * 96 * 128 * 2 + 96 * 4  # 123264
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -338,6 +340,26 @@ def run_gpu(args):
                                      PREFILL_BYTES_PER_TOKEN * T + ck_bytes}}
     del ck
 
+    # ---------------- the same layer through the fused gate prologue ----------------
+    gl = synth.gate_logits(T, w.heads, w.d, dtype=w.dtype, seed=81, device=dev)
+
+    def gated_step():
+        kda.kda_prefill_gated(inp["q"], inp["k"], inp["v"], gl["z"], gl["a_log"],
+                              gl["beta_logit"], cu_seqlens=inp["cu_seqlens"], out=out,
+                              final_state=fin, stream=stream)
+
+    ms_gt, _, _ = time_steps(gated_step, ck_steps, max(args.warmup, 3), world, stream)
+    gt_ach = GATED_BYTES_PER_TOKEN * T / (ms_gt * 1e-3) / 1e9
+    gated = {"value": T * world / (ms_gt * 1e-3), "unit": UNIT, "ms_per_step": ms_gt,
+             "steps": ck_steps,
+             "config": {"workload": "prefill_8k inputs with gate logits: bf16 z ~ N(-3.6, 1), "
+                                    "A_h ~ 0.1 N(0, 1), beta logits ~ N(0, 1)"},
+             "roofline": {"bound": "hbm", "achieved": gt_ach, "peak": hbm_gbs, "unit": "GB/s",
+                          "frac": gt_ach / hbm_gbs, "peak_source": peak_src,
+                          "kernel": "kda_prefill_tc_kernel",
+                          "algorithmic_bytes_per_launch": GATED_BYTES_PER_TOKEN * T}}
+    del gl
+
     # ---------------- e2e through the public API, host buffers ----------------
     host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
     dbuf = {x: torch.empty_like(inp[x]) for x in host}
@@ -411,7 +433,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-            "checkpointed": checkpointed,
+            "checkpointed": checkpointed, "gated": gated,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -145,6 +145,32 @@ kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const v
                                     int64_t interval, int64_t capacity, kda_stream_t stream);
 
 /*
+ * kda_prefill_gated -- kda_prefill with the gate prologue fused into the load
+ * stage: the call takes the decay logits and the write-strength logits and
+ * forms, per token t, head h and key channel c,
+ *
+ *   g[t,h,c] = g_min Sigmoid(e^{A_h} z[t,h,c]),  g_min = -5,
+ *   beta[t,h] = Sigmoid(beta_logit[t,h])
+ *
+ * ("Understanding Kimi K3's Attention": the log-decay bound equation, and the
+ * symbol table for z_t, A_h and beta_t), then evaluates the same recurrence
+ * as kda_prefill.  g never goes through memory; z costs 2 bytes per channel
+ * in bf16 where g costs 4.
+ *
+ *   z           device, in_dtype, [T_tot, H, d_k]: the decay logits; must not
+ *               alias `out`.
+ *   a_log       device fp32 [H]: the per-head log-scales A_h.
+ *   beta_logit  device fp32 [T_tot, H].
+ *
+ * Every other argument, and every other error, is as in kda_prefill;
+ * KDA_ERR_INVALID_ARGUMENT if there are tokens and z or a_log is NULL.
+ */
+kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k, const void *v,
+                             const void *z, const float *a_log, const float *beta_logit,
+                             const float *init_state, const int32_t *cu_seqlens, void *out,
+                             float *final_state, kda_stream_t stream);
+
+/*
  * kda_decode -- one single-token update of N independent fixed-size states.
  *
  * For each sequence n and head h: M = Diag(exp g) S, u = beta (v - M^T k),

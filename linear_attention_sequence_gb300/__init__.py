@@ -8,6 +8,7 @@ method and has no fallback: if the library is missing, every call raises.
 
     kda_prefill(q, k, v, g, beta, ...)  chunk-parallel prefill, packed batch
     kda_prefill_checkpointed(...)       the same, plus state checkpoints every `interval` tokens
+    kda_prefill_gated(q, k, v, z, a_log, beta_logit, ...)   the same, from gate logits
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -17,7 +18,7 @@ import os
 
 import torch
 
-__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -67,6 +68,9 @@ def lib():
         L.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp,
                                                fp, fp, ctypes.c_int64, ctypes.c_int64, vp]
         L.kda_prefill_checkpointed.restype = ctypes.c_int
+        L.kda_prefill_gated.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, fp, fp, fp, vp, vp, fp,
+                                        vp]
+        L.kda_prefill_gated.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -129,7 +133,7 @@ def _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs, out, final
                   out_dtype, variant, return_final_state):
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _require(t, n, ndim=3)
-    _require(g, "g", torch.float32, 3)
+    _require(g, "g", torch.float32, 3)   # None: the gated call, which has no g
     _require(beta, "beta", torch.float32, 2)
     _require(init_state, "init_state", torch.float32, 4)
     _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
@@ -137,7 +141,8 @@ def _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs, out, final
         raise ValueError("q, k, v must share one dtype, fp32 or bf16")
     T, H, dk = q.shape
     dv = v.shape[2]
-    if k.shape != q.shape or g.shape != q.shape or v.shape[:2] != (T, H) or beta.shape != (T, H):
+    if (k.shape != q.shape or (g is not None and g.shape != q.shape) or v.shape[:2] != (T, H)
+            or beta.shape != (T, H)):
         raise ValueError("inconsistent q/k/v/g/beta shapes")
     if cu_seqlens is not None:
         N = cu_seqlens.shape[0] - 1
@@ -186,6 +191,30 @@ def kda_prefill_checkpointed(q, k, v, g, beta, init_state=None, cu_seqlens=None,
                                         int(interval), int(checkpoints.shape[0]), _stream(stream))
     _check(st, "kda_prefill_checkpointed")
     return out, final_state, checkpoints
+
+
+def kda_prefill_gated(q, k, v, z, a_log, beta_logit, init_state=None, cu_seqlens=None, *,
+                      num_seqs=None, out=None, final_state=None, out_dtype=None,
+                      variant=PREFILL_DEFAULT, return_final_state=True, stream=None):
+    """Prefill with the gate prologue fused in (C entry point
+    ``kda_prefill_gated``): g = -5 Sigmoid(e^{a_log[h]} z) and beta =
+    Sigmoid(beta_logit) are formed inside the kernel.  z has the dtype and
+    shape of k; a_log fp32 [H]; beta_logit fp32 [T, H].  Returns
+    ``(out, final_state)``."""
+    if z.dtype != k.dtype or z.shape != k.shape:
+        raise ValueError("z must have the dtype and shape of k")
+    _require(z, "z", k.dtype, 3)
+    _require(a_log, "a_log", torch.float32, 1)
+    if a_log.shape[0] != q.shape[1]:
+        raise ValueError("a_log must hold one value per head")
+    dims, out, final_state = _prefill_args(q, k, v, None, beta_logit, init_state, cu_seqlens,
+                                           num_seqs, out, final_state, out_dtype, variant,
+                                           return_final_state)
+    st = lib().kda_prefill_gated(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(z),
+                                 _ptr(a_log), _ptr(beta_logit), _ptr(init_state),
+                                 _ptr(cu_seqlens), _ptr(out), _ptr(final_state), _stream(stream))
+    _check(st, "kda_prefill_gated")
+    return out, final_state
 
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,

@@ -82,11 +82,15 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
                           const float *g, const float *beta, const float *init_state,
                           const int32_t *cu_seqlens, void *out, float *final_state,
                           float *ckpt, int64_t ckpt_interval, int64_t ckpt_capacity,
-                          kda_stream_t stream, const char *where) {
+                          const void *z, const float *a_log, kda_stream_t stream,
+                          const char *where) {
     kda::Problem P;
     kda_status st = check_dims(dims, P);
     if (st != KDA_OK) return st;
-    if (P.T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    // with the gate prologue, z (decay logits) takes the place of g
+    const void *g_in = a_log ? z : (const void *)g;
+    if (P.T > 0 && (!q || !k || !v || !g_in || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.T > 0 && a_log && (z == (const void *)out)) return KDA_ERR_INVALID_ARGUMENT;
     if (!cu_seqlens) {
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
         P.seq_len = P.N ? P.T / P.N : 0;
@@ -98,10 +102,12 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
         const size_t bytes = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
         if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;
     }
+    P.z = a_log ? z : nullptr;
+    P.a_log = a_log;
     P.ckpt = ckpt_capacity > 0 ? ckpt : nullptr;
     P.ckpt_interval = ckpt_interval;
     P.ckpt_capacity = ckpt_capacity;
-    const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, g);
+    const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
@@ -121,7 +127,7 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                        const int32_t *cu_seqlens, void *out, float *final_state,
                        kda_stream_t stream) {
     return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
-                          nullptr, 0, 0, stream, "kda_prefill");
+                          nullptr, 0, 0, nullptr, nullptr, stream, "kda_prefill");
 }
 
 kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const void *k,
@@ -133,7 +139,21 @@ kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const v
     if (capacity > 0 && (!checkpoints || ((uintptr_t)checkpoints & 3u)))
         return KDA_ERR_INVALID_ARGUMENT;
     return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
-                          checkpoints, interval, capacity, stream, "kda_prefill_checkpointed");
+                          checkpoints, interval, capacity, nullptr, nullptr, stream,
+                          "kda_prefill_checkpointed");
+}
+
+kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k, const void *v,
+                             const void *z, const float *a_log, const float *beta_logit,
+                             const float *init_state, const int32_t *cu_seqlens, void *out,
+                             float *final_state, kda_stream_t stream) {
+    if (!dims) return KDA_ERR_INVALID_ARGUMENT;
+    if (dims->total_tokens > 0 && (!z || !a_log)) return KDA_ERR_INVALID_ARGUMENT;
+    // with no tokens nothing is read: the call only copies the initial states
+    const bool any = dims->total_tokens > 0;
+    return prefill_common(dims, q, k, v, nullptr, beta_logit, init_state, cu_seqlens, out,
+                          final_state, nullptr, 0, 0, any ? z : nullptr, any ? a_log : nullptr,
+                          stream, "kda_prefill_gated");
 }
 
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,

@@ -37,11 +37,23 @@ struct Problem {
     int32_t N, T, H, dk, dv;
     int32_t in_dtype, out_dtype, variant;
     int64_t seq_len;  // used when cu_seqlens == NULL
+    // gate prologue (kda_prefill_gated): with a_log != nullptr the kernels
+    // read the decay logits z (in_dtype) instead of g, and beta logits
+    const void *z = nullptr;
+    const float *a_log = nullptr;
     // state checkpoints (kda_prefill_checkpointed); ckpt == nullptr: none
     float *ckpt = nullptr;
     int64_t ckpt_interval = 0;  // tokens between checkpoints, a multiple of the chunk length
     int64_t ckpt_capacity = 0;  // rows of [capacity, H, d_k, d_v] that may be written
 };
+
+// Gate prologue ("Understanding Kimi K3's Attention", log-decay bound and
+// symbol table): g = g_min Sigmoid(e^{A_h} z) per key channel, beta =
+// Sigmoid(logit).  `scale` is e^{A_h}.  The fast reciprocal of +inf is +0, so
+// a very negative argument (e^{-x} = inf) gives exactly 0, the limit.
+constexpr float kGMin = -5.f;
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+__device__ __forceinline__ float gate_g(float z, float scale) { return kGMin * sigmoid_f(scale * z); }
 
 // Row of the first checkpoint of sequence n: the checkpoints of the earlier
 // sequences come first, floor(length / interval) of them each.

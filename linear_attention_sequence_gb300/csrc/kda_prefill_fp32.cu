@@ -58,7 +58,8 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                         const int32_t *__restrict__ cu, OUT_T *__restrict__ out,
                         float *__restrict__ final_state, int H, int DV, int64_t total,
                         int64_t seq_len, float *__restrict__ ckpt, int64_t ckpt_every,
-                        int64_t ckpt_cap) {
+                        int64_t ckpt_cap, const IN_T *__restrict__ z,
+                        const float *__restrict__ a_log) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<DK, C> &sm = *reinterpret_cast<Smem<DK, C> *>(smem_raw);
 
@@ -76,6 +77,8 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     }
 
     const int64_t rowK = (int64_t)H * DK, rowV = (int64_t)H * DV;
+    // gate prologue: z (decay logits) and beta logits instead of g and beta
+    const float gscale = z ? __expf(a_log[h]) : 0.f;
     // state checkpoints: after every ckpt_every chunks that end inside the sequence
     const int64_t ck_row0 = ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0;
     int64_t chunk = 0;
@@ -88,7 +91,7 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             float gv = 0.f, kv = 0.f, qv = 0.f;
             if (r < L) {
                 const int64_t off = (t0 + r) * rowK + (int64_t)h * DK + c;
-                gv = g[off];
+                gv = z ? kda::gate_g(kda::ld_elem(z + off), gscale) : g[off];
                 kv = kda::ld_elem(k + off);
                 qv = kda::ld_elem(q + off);
             }
@@ -100,7 +103,10 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             const int r = idx / BV, j = idx % BV;
             sm.U[r][j] = r < L ? kda::ld_elem(v + (t0 + r) * rowV + (int64_t)h * DV + j0 + j) : 0.f;
         }
-        if (t < C) sm.beta[t] = t < L ? beta[(t0 + t) * H + h] : 0.f;
+        if (t < C) {
+            const float bt = t < L ? beta[(t0 + t) * H + h] : 0.f;
+            sm.beta[t] = t < L ? (z ? kda::sigmoid_f(bt) : bt) : 0.f;
+        }
         __syncthreads();
 
         // ---- Gamma: running sum of g over the chunk, per key channel ----
@@ -236,7 +242,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     kern<<<grid, kThreads, smem, stream>>>((const IN_T *)q, (const IN_T *)k, (const IN_T *)v, g,
                                            beta, init_state, cu, (OUT_T *)out, final_state, P.H,
                                            P.dv, (int64_t)P.T, P.seq_len, P.ckpt,
-                                           P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity);
+                                           P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity,
+                                           P.a_log ? (const IN_T *)P.z : nullptr, P.a_log);
     return cudaGetLastError();
 }
 

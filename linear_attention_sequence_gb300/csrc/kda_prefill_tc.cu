@@ -73,7 +73,7 @@ constexpr uint32_t kPollLimit = 1u << 23;  // about half a second of polling per
 // Named barriers.  A phase of an mbarrier is awaited by one thread, and a named
 // barrier releases the threads that depend on it: hundreds of threads polling
 // mbarriers slow every other mbarrier and tensor-core operation of the SM.
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_E1 = 3, BAR_WG1 = 4;
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_E1 = 3, BAR_WG1 = 4, BAR_A1 = 5;
 constexpr int kGramIssuer = 96;   // warp 3: idle after the element-wise pass
 constexpr int kTmaIssuer = 224;   // warp 7: issues the first two stage loads
 constexpr int kBetaRing = 4;      // beta of chunk n sits in slot n % 4 (the prep runs <= 2 chunks ahead)
@@ -89,6 +89,7 @@ constexpr uint32_t TM_GA = 384;  // 128: Gram A operand, lanes 0-31 k~, 32-63 q~
 constexpr uint32_t kTileBf16 = C * D * 2;
 constexpr uint32_t kTileF32 = C * D * 4;
 constexpr uint32_t kStageBytes = 3 * kTileBf16 + kTileF32;
+constexpr uint32_t kStageBytesGated = 4 * kTileBf16;   // z (bf16 decay logits) in place of g
 
 // Input tiles arrive by TMA with the 128-byte swizzle: a bf16 tile is two
 // 4 KB halves (32 rows x 64 elements), an fp32 tile four 4 KB quarters (32
@@ -163,16 +164,19 @@ __device__ __forceinline__ float ld_bf16(const unsigned char *tile, int r, int c
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off_bf16(r, c)));
 }
 
+// With the gate prologue, `mg` maps the bf16 decay logits z (two segments per
+// head, like q) and the box lands in the first half of the g tile.
 __device__ __forceinline__ void issue_stage_loads(Stage &st, uint64_t *bar, const CUtensorMap *mq,
                                                   const CUtensorMap *mk, const CUtensorMap *mv,
-                                                  const CUtensorMap *mg, int h, int64_t t0) {
+                                                  const CUtensorMap *mg, int h, int64_t t0,
+                                                  bool gated) {
     // one box per tensor: {128-byte segment, C tokens, the head's segments}
-    mbar_arrive_expect_tx(bar, kStageBytes);
+    mbar_arrive_expect_tx(bar, gated ? kStageBytesGated : kStageBytes);
     const int y = (int)t0;
     tma_load_3d(st.q, mq, bar, 0, y, 2 * h);
     tma_load_3d(st.k, mk, bar, 0, y, 2 * h);
     tma_load_3d(st.v, mv, bar, 0, y, 2 * h);
-    tma_load_3d(st.g, mg, bar, 0, y, 4 * h);
+    tma_load_3d(st.g, mg, bar, 0, y, (gated ? 2 : 4) * h);
 }
 
 // Bounded wait for a phase.  The first poll is inline; the polling loop (and
@@ -199,10 +203,12 @@ __device__ __forceinline__ bool aborted(TcSmem &sm) {
 // Preparation warps (0-7): the decay prefix and decay-weighted operands of
 // chunk n and its Gram MMA, done while the chain warps run chunk n-1.
 // ---------------------------------------------------------------------------
+template <bool GATED>
 __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mg,
                                           const float *__restrict__ beta, int H, int h, int64_t a,
-                                          int64_t b, int nchunks, uint32_t tb) {
+                                          int64_t b, int nchunks, uint32_t tb, float gscale) {
+    constexpr bool gated = GATED;
     const int P = threadIdx.x;  // 0..255
     const int warp = P >> 5, lane = P & 31, qd = warp & 3, wg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
@@ -218,7 +224,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
     }
     if (P == kTmaIssuer)
         for (int s = 0; s < 2 && s < nchunks; ++s) {
-            issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C);
+            issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C, gated);
             sm.tma_issued[s] = 1;
         }
     __syncwarp();
@@ -242,6 +248,10 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         if (beta_thread) {
             cp_async_wait_all();   // beta of chunk n has landed
             const int r = P - 128;
+            if (gated && r < L) {   // beta = Sigmoid(logit) inside the sequence; zeros stay zeros
+                float *bn = &sm.betaS[n % kBetaRing][r];
+                *bn = kda::sigmoid_f(*bn);
+            }
             const int64_t tn = t0 + C + r;
             float *dst = &sm.betaS[(n + 1) % kBetaRing][r];
             if (n + 1 < nchunks && tn < b) cp_async4(dst, beta + tn * H + h);
@@ -255,8 +265,18 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             const int c = P;
             float *g = reinterpret_cast<float *>(in.g);
             float gv[C];
+            if (gated) {
+                // g = g_min Sigmoid(e^{A_h} z) from the bf16 logits; every z is read
+                // before Gamma (fp32) overwrites the tile they sit in
 #pragma unroll
-            for (int r = 0; r < C; ++r) gv[r] = g[off_f32(r, c) >> 2];
+                for (int r = 0; r < C; ++r) gv[r] = ld_bf16(in.g, r, c);
+                named_sync(BAR_A1, D);
+#pragma unroll
+                for (int r = 0; r < C; ++r) gv[r] = kda::gate_g(gv[r], gscale);
+            } else {
+#pragma unroll
+                for (int r = 0; r < C; ++r) gv[r] = g[off_f32(r, c) >> 2];
+            }
             float run = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
@@ -420,7 +440,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                                            OUT_T *__restrict__ out, int H, int h,
                                            int64_t a, int64_t b, int nchunks, uint32_t tb,
                                            float *__restrict__ ckpt, int64_t ckpt_every,
-                                           int64_t ckpt_cap, int64_t ck_row0) {
+                                           int64_t ckpt_cap, int64_t ck_row0, bool gated) {
     const int j = threadIdx.x - kPrep;   // 0..127
     const int warp = threadIdx.x >> 5, cw = j >> 5, lane = j & 31;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -513,7 +533,8 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                 mma_commit(&sm.bar_x);
                 if (wait_phase(sm, &sm.bar_x, x_par, 16u) && n + 2 < nchunks) {
                     // the stage is free again: refill it with chunk n+2
-                    issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C);
+                    issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C,
+                                      gated);
                     sm.tma_issued[st] += 1;
                 }
             }
@@ -607,7 +628,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
     }
 }
 
-template <typename OUT_T>
+template <typename OUT_T, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -616,7 +637,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const float *__restrict__ init_state, const int32_t *__restrict__ cu,
                       OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
                       int64_t total, int64_t seq_len, float *__restrict__ ckpt,
-                      int64_t ckpt_every, int64_t ckpt_cap) {
+                      int64_t ckpt_every, int64_t ckpt_cap, const float *__restrict__ a_log) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Round up to 1024 bytes by pointer arithmetic on the shared array itself
     // (an integer round trip would lose the shared address space and turn
@@ -679,11 +700,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
 
     if (!chain)
-        prep_loop(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb);
+        prep_loop<GATED>(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb,
+                         GATED ? __expf(a_log[h]) : 0.f);
     else
         chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, out, H, h, a, b, nchunks, tb, ckpt,
                           ckpt_every, ckpt_cap,
-                          ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0);
+                          ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0,
+                          GATED);
 
     tc_fence_before();
     __syncthreads();
@@ -752,9 +775,10 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
-        !make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H))
+        !(P.a_log ? make_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
+                  : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
         return cudaErrorInvalidValue;
-    auto kern = kda_prefill_tc_kernel<OUT_T>;
+    auto kern = P.a_log ? kda_prefill_tc_kernel<OUT_T, true> : kda_prefill_tc_kernel<OUT_T, false>;
     const size_t smem = sizeof(TcSmem) + 1024;
     static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -762,7 +786,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     const unsigned blocks = (unsigned)((int64_t)P.N * P.H);
     kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, beta, init_state, cu, (OUT_T *)out,
                                              final_state, P.H, (int64_t)P.T, P.seq_len, P.ckpt,
-                                             P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity);
+                                             P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity,
+                                             P.a_log);
     return cudaGetLastError();
 }
 

@@ -129,3 +129,20 @@ def random_inputs(T, H, d, dtype=torch.float32, mu=2.0, seed=0, device="cpu",
         init = torch.randn((num_seqs, H, d, d), generator=gen, device=device,
                            dtype=torch.float32) * init_std
     return dict(q=q, k=k, v=v, g=g, beta=beta, init_state=init)
+
+
+# Gate logits for the fused gate prologue (kda_prefill_gated).  Recipe:
+# z ~ N(-3.6, 1) per (token, head, channel), rounded once to `dtype`; A_h ~
+# 0.1 N(0, 1) per head; beta logits ~ N(0, 1) per (token, head).  With
+# g = -5 Sigmoid(e^{A_h} z) this gives a mean retention e^g of about 0.87,
+# close to the 0.88 of the g recipe above.  Draw order: z, A, beta logits.
+GATE_Z_MEAN = -3.6
+
+
+def gate_logits(T, H, d, dtype=torch.float32, seed=0, device="cpu"):
+    gen = _gen(seed, device)
+    z = (torch.randn((T, H, d), generator=gen, device=device, dtype=torch.float32)
+         + GATE_Z_MEAN).to(dtype)
+    a_log = 0.1 * torch.randn((H,), generator=gen, device=device, dtype=torch.float32)
+    beta_logit = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32)
+    return dict(z=z, a_log=a_log, beta_logit=beta_logit)

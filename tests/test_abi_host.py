@@ -144,6 +144,30 @@ def test_prefill_checkpointed_empty_batch_is_ok(L):
                         v=None, g=None, beta=None, out=None) == OK
 
 
+def prefill_gated(L, dims, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, z=ctypes.c_void_p(0x60000), a=ctypes.c_void_p(0x70000),
+                bl=FAKE, init=None, cu=None, out=ctypes.c_void_p(0x20000), fin=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_prefill_gated(d, args["q"], args["k"], args["v"], args["z"], args["a"],
+                               args["bl"], args["init"], args["cu"], args["out"], args["fin"],
+                               None)
+
+
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(), {"z": None}), (D(), {"a": None}),
+    (D(), {"bl": None}), (D(), {"q": None}), (D(), {"z": ctypes.c_void_p(0x20000)}),
+    (D(num_seqs=3, total_tokens=16), {}),
+])
+def test_prefill_gated_rejects(L, dims, over):
+    assert prefill_gated(L, dims, **over) == INVALID
+
+
+def test_prefill_gated_empty_batch_is_ok(L):
+    assert prefill_gated(L, D(num_seqs=0, total_tokens=0), q=None, k=None, v=None, z=None,
+                         a=None, bl=None, out=None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

@@ -121,3 +121,23 @@ def test_prefill_8k_checkpoints_match_prefix_runs():
         n = 1024 * j
         _, fin_p = kda.kda_prefill(*(inp[x][:n].contiguous() for x in ("q", "k", "v", "g", "beta")))
         assert torch.equal(ck[j - 1], fin_p[0]), f"checkpoint {j}"
+
+
+def test_gated_prefill_8k_sampled_heads():
+    """The 8K layer through the fused gate prologue (bf16 decay logits):
+    three heads against the oracle fed with the oracle's gate."""
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, "cuda")
+    gl = synth.gate_logits(w.total_tokens, w.heads, w.d, dtype=w.dtype, seed=81, device="cuda")
+    out, fin = kda.kda_prefill_gated(inp["q"], inp["k"], inp["v"], gl["z"], gl["a_log"],
+                                     gl["beta_logit"], cu_seqlens=inp["cu_seqlens"],
+                                     out_dtype=torch.float32)
+    heads = [0, 47, 95]
+    g, beta = oracle.gate(host64(gl["z"][:, heads]), host64(gl["a_log"][heads]),
+                          host64(gl["beta_logit"][:, heads]))
+    o_ref, s_ref = oracle.prefill(host64(inp["q"][:, heads]), host64(inp["k"][:, heads]),
+                                  host64(inp["v"][:, heads]), g, beta)
+    eo = rel_err(host64(out[:, heads]), o_ref)
+    es = rel_err(host64(fin[:, heads]), s_ref)
+    print(f"gated prefill_8k (3 heads): err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]

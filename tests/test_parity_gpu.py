@@ -298,3 +298,53 @@ def test_checkpoints_equal_prefix_final_states(variant, interval):
                 assert rel_err(host64(ck[row]), s_ref[0]) <= TOL[dtype]
             row += 1
     assert row == ck.shape[0]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_gated_prefill_matches_oracle(variant, d, dtype):
+    """kda_prefill_gated on a ragged packed batch (empty, short, multi-chunk
+    sequences) against the oracle fed with the oracle's own gate prologue."""
+    if not supported(variant, d, dtype):
+        pytest.skip("variant does not take this shape/dtype")
+    H = 2
+    lens = [1, 31, 32, 0, 65, 100]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=61, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    gl = synth.gate_logits(T, H, d, dtype=dtype, seed=62, device=DEV)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    try:
+        out, fin = kda.kda_prefill_gated(inp["q"], inp["k"], inp["v"], gl["z"], gl["a_log"],
+                                         gl["beta_logit"], init_state=inp["init_state"],
+                                         cu_seqlens=cu, out_dtype=torch.float32, variant=variant)
+    except kda.KdaError as e:
+        if e.status == 2:
+            pytest.skip("variant does not take this shape/dtype (KDA_ERR_UNSUPPORTED)")
+        raise
+    g, beta = oracle.gate(host64(gl["z"]), host64(gl["a_log"]), host64(gl["beta_logit"]))
+    o_ref, s_ref = oracle.prefill(host64(inp["q"]), host64(inp["k"]), host64(inp["v"]), g, beta,
+                                  init_state=host64(inp["init_state"]),
+                                  cu_seqlens=cu.cpu().numpy())
+    check(out, fin, o_ref, s_ref, dtype)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gated_prefill_equals_prefill_of_gate(variant):
+    """The fused prologue computes what kda_prefill computes from the same g
+    and beta formed outside (oracle gate, rounded to fp32), up to rounding."""
+    T, H, d = 150, 2, 128
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=71, device=DEV)
+    gl = synth.gate_logits(T, H, d, dtype=dtype, seed=72, device=DEV)
+    out, fin = kda.kda_prefill_gated(inp["q"], inp["k"], inp["v"], gl["z"], gl["a_log"],
+                                     gl["beta_logit"], out_dtype=torch.float32, variant=variant)
+    g, beta = oracle.gate(host64(gl["z"]), host64(gl["a_log"]), host64(gl["beta_logit"]))
+    g32 = torch.tensor(g, dtype=torch.float32, device=DEV)
+    b32 = torch.tensor(beta, dtype=torch.float32, device=DEV)
+    out0, fin0 = kda.kda_prefill(inp["q"], inp["k"], inp["v"], g32, b32,
+                                 out_dtype=torch.float32, variant=variant)
+    tol = TOL[dtype]
+    assert rel_err(host64(out), host64(out0)) <= tol
+    assert rel_err(host64(fin), host64(fin0)) <= tol
