@@ -55,7 +55,10 @@ typedef enum {
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
 /* Prefill kernel selection.  KDA_PREFILL_DEFAULT picks the tensor-core
- * kernel where it supports the shape and dtype, else the fp32 CUDA-core one. */
+ * kernel where it supports the call, else the fp32 CUDA-core one.  The
+ * tensor-core kernel takes d_k = d_v = 128, bf16 q/k/v, and q, k, v, g (or z)
+ * and out 16-byte aligned; KDA_PREFILL_TC on any other call returns
+ * KDA_ERR_UNSUPPORTED. */
 typedef enum {
     KDA_PREFILL_DEFAULT = 0,
     KDA_PREFILL_FP32 = 1,  /* CUDA-core fp32 chunked kernel (any supported shape) */

@@ -107,7 +107,7 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     P.ckpt = ckpt_capacity > 0 ? ckpt : nullptr;
     P.ckpt_interval = ckpt_interval;
     P.ckpt_capacity = ckpt_capacity;
-    const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in);
+    const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in, out);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;

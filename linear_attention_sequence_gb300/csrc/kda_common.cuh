@@ -76,7 +76,7 @@ cudaError_t kda_launch_decode(const kda::Problem &P, const void *q, const void *
                               const float *g, const float *beta, float *state, void *out,
                               cudaStream_t stream);
 bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
-                              const float *g);
+                              const float *g, const void *out);
 cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const void *k,
                                   const void *v, const float *g, const float *beta,
                                   const float *init_state, const int32_t *cu, void *out,

@@ -19,13 +19,17 @@
 // readout GEMM straight from TMEM and accumulates its own update in place.
 //
 // Warp specialisation.  Warps 0-7 prepare chunk n: decay prefix,
-// decay-weighted operands, the Gram MMA.  Warps 8-11 run the rest of a chunk:
-// extraction of the intra-chunk matrices from the Gram, the triangular solve,
-// U' = T diag(beta) V and the readout MMA X = S^T [gamma Q; gamma K]^T, the U
-// MMA that subtracts (gamma K S) T diag(beta) with the X accumulator itself as
-// A operand, the state decay, and one MMA group for the intra-chunk readout
-// and the state carry together, then the output store.  The two groups hand
-// buffers to each other through mbarriers; every wait is bounded.  The thread
+// decay-weighted operands, the Gram MMA.  Warps 8-11 run the rest of a chunk.
+// Warps 10 and 11 issue the readout MMA X = S^T [gamma Q; gamma K]^T as soon as
+// the chunk's operand is in place (it needs no solve) and then decay their half
+// of the state; meanwhile warps 8 and 9 extract the intra-chunk matrices from
+// the Gram and solve the triangular system.  Then, on all four: U' = T diag(beta)
+// V and the U MMA that subtracts (gamma K S) T diag(beta) with the X accumulator
+// itself as A operand (one accumulator, one issuing thread), the rest of the
+// state decay, one MMA group for the intra-chunk readout and the state carry
+// together, and the output store (a TMA store of a staged tile for a full
+// chunk).  The two groups hand buffers to each other through mbarriers; every
+// wait is bounded.  The thread
 // that issues a tcgen05.mma or a TMA load is held for roughly the time the
 // unit needs to accept it, so each issue is given to a warp that has nothing
 // else to do at that point.  A tcgen05.mma costs a roughly fixed time per
@@ -73,8 +77,8 @@ constexpr uint32_t kPollLimit = 1u << 23;  // about half a second of polling per
 // Named barriers.  A phase of an mbarrier is awaited by one thread, and a named
 // barrier releases the threads that depend on it: hundreds of threads polling
 // mbarriers slow every other mbarrier and tensor-core operation of the SM.
-constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_E1 = 3, BAR_WG1 = 4, BAR_A1 = 5;
-constexpr int kGramIssuer = 96;   // warp 3: idle after the element-wise pass
+constexpr uint32_t BAR_PREP = 1, BAR_CHAIN = 2, BAR_E1 = 3, BAR_A1 = 5, BAR_XG = 6;
+constexpr int kGramIssuer = 96;   // warp 3: issues the Gram MMA once its operands are in place
 constexpr int kTmaIssuer = 224;   // warp 7: issues the first two stage loads
 constexpr int kBetaRing = 4;      // beta of chunk n sits in slot n % 4 (the prep runs <= 2 chunks ahead)
 
@@ -82,7 +86,8 @@ constexpr int kBetaRing = 4;      // beta of chunk n sits in slot n % 4 (the pre
 constexpr uint32_t TM_S = 0;     // 128: S^T (lanes = value index, columns = key channel)
 constexpr uint32_t TM_X = 128;   // 64: [(gamma Q S)^T, then O^T | (gamma K S)^T]
 constexpr uint32_t TM_U = 192;   // 2 x 32: U'^T, then U^T, per chunk parity
-constexpr uint32_t TM_BV = 256;  // 32: V^T, A operand of the U' MMA
+constexpr uint32_t TM_BV = 256;  // 32: V^T of even chunks, A operand of the U' MMA
+constexpr uint32_t TM_BV1 = 352; // 32: V^T of odd chunks
 constexpr uint32_t TM_G = 288;   // 2 x 32: Gram, per chunk parity
 constexpr uint32_t TM_GA = 384;  // 128: Gram A operand, lanes 0-31 k~, 32-63 q~
 
@@ -117,16 +122,18 @@ static_assert(4 * 64 * 32 * 4 <= sizeof(Stage), "readout operand fits in a stage
 
 struct alignas(1024) TcSmem {
     Stage in[2];                // TMA destinations, double-buffered
+    unsigned char ostage[2][kTileF32];   // output rows of a full chunk, stored by TMA (SW128)
     float gramA[4 * 64 * 32];   // staging of the Gram A operand [k~ ; q~] (tf32), copied to TMEM
     float gramB[4 * 32 * 32];   // Gram B operand k e^{Gamma_15 - Gamma}
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
     float tmat[2][32 * 32];     // T diag(beta): B operand of the U' MMA and, negated, of the U MMA
     float akkT[32][32];         // solve scratch: (beta-scaled strict lower Akk)^T
+    float tsc[3][16][20];       // solve scratch: T11 by rows, T22^T, A21 T11 (rows padded)
     float betaS[kBetaRing][C];
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
-    uint64_t bar_tma[2], bar_gram[2], bar_bxfull[2], bar_up[2], bar_akempty[2];
-    uint64_t bar_x, bar_u, bar_s, bar_fin[2];
+    uint64_t bar_tma[2], bar_gram[2], bar_bxfull[2], bar_gops[2], bar_akempty[2];
+    uint64_t bar_x, bar_u, bar_s, bar_fin[3];
     uint32_t tma_issued[2];     // stage loads issued / awaited (for the drain after a stop)
     uint32_t tma_awaited[2];
     uint32_t tmem_base;
@@ -212,7 +219,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
     const int P = threadIdx.x;  // 0..255
     const int warp = P >> 5, lane = P & 31, qd = warp & 3, wg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, up_par[2] = {0, 0}, gram_par[2] = {0, 0};
+    uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, gram_par[2] = {0, 0};
     const bool beta_thread = P >= 128 && P < 128 + C;
 
     // beta of chunk 0 (asynchronous 4-byte copies; rows past the end are 0)
@@ -372,26 +379,39 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
             tmem_wait_st();
             tc_fence_before();
         } else if (wg == 1) {
-            // V^T (thread = value index); the U' MMA of chunk n-1 must be done with it
-            if (n >= 1) {
-                if (P == 128) wait_phase(sm, &sm.bar_up[st ^ 1], up_par[st ^ 1], 8u);
-                up_par[st ^ 1] ^= 1u;
-                named_sync(BAR_WG1, 128);
-                tc_fence_after();
-            }
+            // V^T (thread = value index) into the buffer of this parity; the U' MMA
+            // of chunk n-2 that read it is complete (akempty of chunk n-2, awaited above)
+            tc_fence_after();
             const int j = P - 128;
+            const uint32_t tbv = st ? TM_BV1 : TM_BV;
             float v0[16], v1[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 v0[r] = r < L ? ld_bf16(in.v, r, j) : 0.f;
                 v1[r] = 16 + r < L ? ld_bf16(in.v, 16 + r, j) : 0.f;
             }
-            tmem_st16(tb + lane_off + TM_BV, v0);
-            tmem_st16(tb + lane_off + TM_BV + 16, v1);
+            tmem_st16(tb + lane_off + tbv, v0);
+            tmem_st16(tb + lane_off + tbv + 16, v1);
             tmem_wait_st();
             tc_fence_before();
         }
         named_sync(BAR_PREP, kPrep);   // the inputs of chunk n are consumed
+        // Beta and the Gram operands of chunk n are in place: the chain may start
+        // its extraction once the Gram MMA, issued here, completes.  The issue
+        // holds warp 3 for about a microsecond; its share of the stores below
+        // waits meanwhile, and the readout MMA that needs them has slack.
+        if (P == 0) mbar_arrive(&sm.bar_gops[st]);
+        if (P == kGramIssuer) {
+            tc_fence_after();
+            const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+                mma_tf32_ts(tb + TM_G + 32 * st, tb + TM_GA + kk * 8,
+                            dB + (uint64_t)(((kk >> 2) * (32 * 128) + (kk & 3) * 32) >> 4),
+                            idesc_tf32(128, 32), kk > 0);
+            mma_commit(&sm.bar_gram[st]);
+        }
+        __syncwarp();
 
         // ---- readout operand [gamma q ; gamma k] into the chunk's own stage ----
         {
@@ -404,23 +424,10 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 st_op4(blk, 32 + r, k4, gk[it][0], gk[it][1], gk[it][2], gk[it][3]);
             }
         }
-        // End of chunk n.  After the barrier thread 0 hands the chunk to the
-        // chain, and the warp that issues the Gram MMA (the issue holds it for
-        // about a microsecond) does so without holding anyone up.
+        // End of chunk n: after the barrier thread 0 hands the chunk to the chain.
         fence_proxy_async_smem();
         named_sync(BAR_PREP, kPrep);
         if (P == 0) mbar_arrive(&sm.bar_bxfull[st]);   // chunk n is ready for the chain
-        if (P == kGramIssuer) {
-            tc_fence_after();
-            const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-                mma_tf32_ts(tb + TM_G + 32 * st, tb + TM_GA + kk * 8,
-                            dB + (uint64_t)(((kk >> 2) * (32 * 128) + (kk & 3) * 32) >> 4),
-                            idesc_tf32(128, 32), kk > 0);
-            mma_commit(&sm.bar_gram[st]);
-        }
-        __syncwarp();
         // (a stop is agreed on by the vote at the top of the next chunk)
     }
     if (beta_thread) cp_async_wait_all();
@@ -430,6 +437,36 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
     }
 }
 
+// Element (r, c) of an output tile in the TMA box layout (SW128 segments of 128 bytes).
+template <typename OUT_T>
+__device__ __forceinline__ void st_stage(unsigned char *tile, int r, int c, float x) {
+    if constexpr (sizeof(OUT_T) == 2)
+        *reinterpret_cast<__nv_bfloat16 *>(tile + off_bf16(r, c)) = __float2bfloat16_rn(x);
+    else
+        *reinterpret_cast<float *>(tile + off_f32(r, c)) = x;
+}
+
+// S^T <- S^T Diag(e^{Gamma_last}) on the 32 lanes of the calling warp (`tl` =
+// TMEM base + the warp's lane offset).
+__device__ __forceinline__ void scale_state(TcSmem &sm, uint32_t tl, int st) {
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float s0[16], s1[16];
+        tmem_ld16x2(tl + TM_S + c0, tl + TM_S + c0 + 16, s0, s1);
+        const float4 *gc = reinterpret_cast<const float4 *>(&sm.gamC[st][c0]);
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 a4 = gc[i4], b4 = gc[4 + i4];
+            s0[4 * i4] *= a4.x; s0[4 * i4 + 1] *= a4.y; s0[4 * i4 + 2] *= a4.z; s0[4 * i4 + 3] *= a4.w;
+            s1[4 * i4] *= b4.x; s1[4 * i4 + 1] *= b4.y; s1[4 * i4 + 2] *= b4.z; s1[4 * i4 + 3] *= b4.w;
+        }
+        tmem_st16(tl + TM_S + c0, s0);
+        tmem_st16(tl + TM_S + c0 + 16, s1);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+}
+
 // ---------------------------------------------------------------------------
 // Chain warps (8-11): everything of chunk n from its Gram on.  Thread j owns
 // TMEM lane j = value index j; warps 8 and 9 read the Gram rows (lanes 0-63).
@@ -437,15 +474,15 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
 template <typename OUT_T>
 __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                            const CUtensorMap *mv, const CUtensorMap *mg,
-                                           OUT_T *__restrict__ out, int H, int h,
+                                           const CUtensorMap *mo, OUT_T *__restrict__ out, int H, int h,
                                            int64_t a, int64_t b, int nchunks, uint32_t tb,
                                            float *__restrict__ ckpt, int64_t ckpt_every,
                                            int64_t ckpt_cap, int64_t ck_row0, bool gated) {
     const int j = threadIdx.x - kPrep;   // 0..127
     const int warp = threadIdx.x >> 5, cw = j >> 5, lane = j & 31;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const bool issuer = j == 0;
-    uint32_t bxf_par[2] = {0, 0}, gram_par[2] = {0, 0}, x_par = 0, u_par = 0, s_par = 0;
+    const bool issuer = j == 0, xissuer = j == 96, ostorer = j == 32;
+    uint32_t bxf_par[2] = {0, 0}, gops_par[2] = {0, 0}, gram_par[2] = {0, 0}, x_par = 0, u_par = 0, s_par = 0;
 
     for (int n = 0; n < nchunks; ++n) {
         const int st = n & 1;
@@ -454,16 +491,41 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
         const uint32_t tu = TM_U + 32 * st;
         const float *betaN = sm.betaS[n % kBetaRing];
 
-        // Chunk n handed over by the preparation warps (its beta, gamma_last,
-        // readout operand, Kbar^T and V^T are in place; the Gram MMA is issued).
-        // The issuer waits; the barriers below release the other threads.
-        if (issuer) wait_phase(sm, &sm.bar_bxfull[st], bxf_par[st], 64u);
-        bxf_par[st] ^= 1u;
-
-        // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram (warps 8, 9) ----
-        if (cw < 2) {
-            if (issuer) wait_phase(sm, &sm.bar_gram[st], gram_par[st], 2u);
-            gram_par[st] ^= 1u;
+        // Two hand-overs from the preparation warps: the Gram of chunk n (with its
+        // beta) for the extraction and solve, and the whole chunk (gamma_last,
+        // readout operand, Kbar^T, V^T) for the readout MMA and what follows.
+        if (cw >= 2) {
+            // ---- a5: X^T = S^T [gamma Q ; gamma K]^T (warps 10, 11).  It needs only
+            // the state and the readout operand, so it runs while warps 8, 9
+            // extract and solve; then S^T <- S^T Diag(e^{Gamma_last}) on lanes 64-127. ----
+            if (xissuer) {
+                if (wait_phase(sm, &sm.bar_bxfull[st], bxf_par[st], 64u)) {
+                    tc_fence_after();
+                    const uint64_t dX = sdesc_sw128(smem_u32(&sm.in[st]));   // the chunk's stage
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
+                                    dX + (uint64_t)(((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4),
+                                    idesc_tf32(128, 64), kk > 0);
+                    mma_commit(&sm.bar_x);
+                    if (wait_phase(sm, &sm.bar_x, x_par, 16u) && n + 2 < nchunks) {
+                        // the stage is free again: refill it with chunk n+2
+                        issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C,
+                                          gated);
+                        sm.tma_issued[st] += 1;
+                    }
+                }
+            }
+            __syncwarp();
+            named_sync(BAR_XG, 64);
+            tc_fence_after();
+            scale_state(sm, tb + lane_off, st);
+        } else {
+            // ---- a4: Akk (strict, beta rows) and Aqk (inclusive) from the Gram (warps 8, 9) ----
+            if (issuer) {
+                wait_phase(sm, &sm.bar_gops[st], gops_par[st], 64u);
+                wait_phase(sm, &sm.bar_gram[st], gram_par[st], 2u);
+            }
             named_sync(BAR_E1, 64);
             tc_fence_after();
             float d0[16], d1[16];
@@ -477,18 +539,20 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                 for (int m = 0; m < 32; ++m)
                     sm.akkT[m][r] = m < r ? br * (m < 16 ? d0[m] : d1[m - 16]) : 0.f;
                 __syncwarp();
-                // T = (I + Akk)^{-1}: lane j computes column j by forward
-                // substitution, one row of Akk^T (a broadcast) per step
-                const int jc = lane;
-                float x[32];
+                // T = (I + Akk)^{-1} by 16 x 16 blocks.  The diagonal blocks
+                // T11 = (I + A11)^{-1} (lanes 0-15) and T22 = (I + A22)^{-1} (lanes 16-31)
+                // by forward substitution, one column per lane; then
+                // T21 = -T22 (A21 T11), each lane 8 rows of one column.
+                const int hb = lane >> 4, jj = lane & 15, b0 = 16 * hb;
+                float x[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = i == jc ? 1.f : 0.f;
+                for (int i = 0; i < 16; ++i) x[i] = i == jj ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 31; ++m) {
+                for (int m = 0; m < 15; ++m) {
                     const float xm = x[m];
-                    const float4 *row = reinterpret_cast<const float4 *>(sm.akkT[m]);
+                    const float4 *row = reinterpret_cast<const float4 *>(&sm.akkT[b0 + m][b0]);
 #pragma unroll
-                    for (int q4 = (m + 1) >> 2; q4 < 8; ++q4) {
+                    for (int q4 = (m + 1) >> 2; q4 < 4; ++q4) {
                         const float4 a4 = row[q4];
                         const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
@@ -496,10 +560,51 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                             if (4 * q4 + e > m) x[4 * q4 + e] -= av[e] * xm;
                     }
                 }
-                // T diag(beta) as a tf32 operand: row i, column jc
-                const float bj = betaN[jc];
+                // T11 by rows (tsc[0][k][j] = T11[k][j]), T22 by columns (tsc[1][j][i] = T22[i][j])
+                if (hb == 0) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) st_op(sm.tmat[st], i, jc, x[i] * bj);
+                    for (int k = 0; k < 16; ++k) sm.tsc[0][k][jj] = x[k];
+                } else {
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; ++i4)
+                        *reinterpret_cast<float4 *>(&sm.tsc[1][jj][4 * i4]) =
+                            make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
+                }
+                __syncwarp();
+                // M = A21 T11, rows 8 hb .. 8 hb + 7 of column jj (A21[i][k] = akkT[k][16 + i])
+                float mm[8];
+#pragma unroll
+                for (int r8 = 0; r8 < 8; ++r8) mm[r8] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float t = sm.tsc[0][k][jj];
+                    const float4 a0 = *reinterpret_cast<const float4 *>(&sm.akkT[k][16 + 8 * hb]);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(&sm.akkT[k][20 + 8 * hb]);
+                    mm[0] += a0.x * t; mm[1] += a0.y * t; mm[2] += a0.z * t; mm[3] += a0.w * t;
+                    mm[4] += a1.x * t; mm[5] += a1.y * t; mm[6] += a1.z * t; mm[7] += a1.w * t;
+                }
+#pragma unroll
+                for (int r8 = 0; r8 < 8; ++r8) sm.tsc[2][8 * hb + r8][jj] = mm[r8];
+                __syncwarp();
+                // T21 = -T22 M, the same rows and column
+                float t21[8];
+#pragma unroll
+                for (int r8 = 0; r8 < 8; ++r8) t21[r8] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float mk = sm.tsc[2][k][jj];
+                    const float4 c0 = *reinterpret_cast<const float4 *>(&sm.tsc[1][k][8 * hb]);
+                    const float4 c1 = *reinterpret_cast<const float4 *>(&sm.tsc[1][k][8 * hb + 4]);
+                    t21[0] -= c0.x * mk; t21[1] -= c0.y * mk; t21[2] -= c0.z * mk; t21[3] -= c0.w * mk;
+                    t21[4] -= c1.x * mk; t21[5] -= c1.y * mk; t21[6] -= c1.z * mk; t21[7] -= c1.w * mk;
+                }
+                // T diag(beta) as a tf32 operand (row i, column c): the diagonal block of
+                // this half, then 8 rows of T21.  The block T12 = 0 is written once at the start.
+                const float bd = betaN[b0 + jj], bl = betaN[jj];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) st_op(sm.tmat[st], b0 + i, b0 + jj, x[i] * bd);
+#pragma unroll
+                for (int r8 = 0; r8 < 8; ++r8) st_op(sm.tmat[st], 16 + 8 * hb + r8, jj, t21[r8] * bl);
                 fence_proxy_async_smem();
             } else {
                 float av[32];
@@ -511,43 +616,23 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                 fence_proxy_async_smem();
             }
         }
-        if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
-
-        // ---- U'^T = V^T (T diag(beta))^T into TMEM U[st], then
-        // a5: X^T = S^T [gamma Q ; gamma K]^T, the state in TMEM as A operand ----
-        if (issuer) {
-            if (!aborted(sm)) {
-                tc_fence_after();
-                const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32_ts(tb + tu, tb + TM_BV + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
-                                idesc_tf32(128, 32), kk > 0);
-                mma_commit(&sm.bar_up[st]);   // V^T may be overwritten once this completes
-#pragma unroll
-                const uint64_t dX = sdesc_sw128(smem_u32(&sm.in[st]));   // the chunk's stage
-                for (int kk = 0; kk < 16; ++kk)
-                    mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
-                                dX + (uint64_t)(((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4),
-                                idesc_tf32(128, 64), kk > 0);
-                mma_commit(&sm.bar_x);
-                if (wait_phase(sm, &sm.bar_x, x_par, 16u) && n + 2 < nchunks) {
-                    // the stage is free again: refill it with chunk n+2
-                    issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C,
-                                      gated);
-                    sm.tma_issued[st] += 1;
-                }
-            }
-        }
-        __syncwarp();
+        bxf_par[st] ^= 1u;
+        gops_par[st] ^= 1u;
+        gram_par[st] ^= 1u;
         x_par ^= 1u;
         if (named_sync_or(BAR_CHAIN, kChain, aborted(sm))) break;
-        tc_fence_after();
 
-        // ---- a4 (state side): U^T = U'^T - (gamma K S)^T (T diag(beta))^T, accumulated
-        // onto U' (same accumulator and issuing thread, so it follows the U' MMA) ----
+        // ---- a4 (state side): U'^T = V^T (T diag(beta))^T into TMEM U[st], then
+        // U^T = U'^T - (gamma K S)^T (T diag(beta))^T accumulated onto it (same
+        // accumulator and issuing thread, so the second group follows the first) ----
         if (issuer) {
+            tc_fence_after();
             const uint64_t dT = sdesc_sw128(smem_u32(sm.tmat[st]));
+            const uint32_t tbv = st ? TM_BV1 : TM_BV;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_tf32_ts(tb + tu, tb + tbv + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
+                            idesc_tf32(128, 32), kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_tf32_ts(tb + tu, tb + TM_X + 32 + kk * 8, dT + (uint64_t)((kk * 32) >> 4),
@@ -555,23 +640,12 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             mma_commit(&sm.bar_u);
         }
         __syncwarp();
-        // S^T <- S^T Diag(e^{Gamma_last}), overlapping the U MMA
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float s0[16], s1[16];
-            tmem_ld16x2(tb + lane_off + TM_S + c0, tb + lane_off + TM_S + c0 + 16, s0, s1);
-            const float4 *gc = reinterpret_cast<const float4 *>(&sm.gamC[st][c0]);
-#pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-                const float4 a4 = gc[i4], b4 = gc[4 + i4];
-                s0[4 * i4] *= a4.x; s0[4 * i4 + 1] *= a4.y; s0[4 * i4 + 2] *= a4.z; s0[4 * i4 + 3] *= a4.w;
-                s1[4 * i4] *= b4.x; s1[4 * i4 + 1] *= b4.y; s1[4 * i4 + 2] *= b4.z; s1[4 * i4 + 3] *= b4.w;
-            }
-            tmem_st16(tb + lane_off + TM_S + c0, s0);
-            tmem_st16(tb + lane_off + TM_S + c0 + 16, s1);
+        // S^T <- S^T Diag(e^{Gamma_last}) on lanes 0-63, overlapping the U MMAs
+        // (the readout MMA that read S is complete: warps 10, 11 awaited it)
+        if (cw < 2) {
+            tc_fence_after();
+            scale_state(sm, tb + lane_off, st);
         }
-        tmem_wait_st();
-        tc_fence_before();
         if (issuer) wait_phase(sm, &sm.bar_u, u_par, 16u);
         u_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
@@ -588,23 +662,45 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             mma_commit(&sm.bar_akempty[st]);
             wait_phase(sm, &sm.bar_s, s_par, 16u);
         }
+        // the output staging buffer of this parity was last stored for chunk n-2
+        if (ostorer) bulk_wait_group_read<1>();
         __syncwarp();
         s_par ^= 1u;
         named_sync(BAR_CHAIN, kChain);
         tc_fence_after();
 
-        // ---- a7: output rows ----
+        // ---- a7: output rows (read from TMEM by every thread before the next
+        // chunk's readout MMA overwrites them) ----
         float o0[16], o1[16];
         tmem_ld16x2(tb + lane_off + TM_X, tb + lane_off + TM_X + 16, o0, o1);
         tc_fence_before();
-        OUT_T *dst = out + (t0 * H + h) * (int64_t)D + j;
-        const int64_t row = (int64_t)H * D;
+        if (L == C) {
+            // a full chunk: rows into the staging tile, one TMA store
+            unsigned char *stg = sm.ostage[st];
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (r < L) kda::st_elem(dst + r * row, o0[r]);
+            for (int r = 0; r < 16; ++r) {
+                st_stage<OUT_T>(stg, r, j, o0[r]);
+                st_stage<OUT_T>(stg, 16 + r, j, o1[r]);
+            }
+            fence_proxy_async_smem();
+        }
+        named_sync(BAR_CHAIN, kChain);
+        if (L == C) {
+            if (ostorer) {
+                tma_store_3d(mo, sm.ostage[st], 0, (int)t0, (int)(sizeof(OUT_T) * D / 128) * h);
+                bulk_commit_group();
+            }
+        } else {
+            // the last chunk of a sequence: the rows past its end belong to the next one
+            OUT_T *dst = out + (t0 * H + h) * (int64_t)D + j;
+            const int64_t row = (int64_t)H * D;
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
+            for (int r = 0; r < 16; ++r)
+                if (r < L) kda::st_elem(dst + r * row, o0[r]);
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (16 + r < L) kda::st_elem(dst + (16 + r) * row, o1[r]);
+        }
 
         // ---- state checkpoint after every ckpt_every chunks that end inside the
         // sequence: S (after this chunk's carry) from TMEM, thread j writes column j ----
@@ -622,9 +718,11 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             }
         }
     }
-    if (issuer) {   // every MMA issued here has completed
-        mma_commit(&sm.bar_fin[1]);
-        mbar_wait_bounded(&sm.bar_fin[1], 0, kPollLimit);
+    if (ostorer) bulk_wait_group_all();   // every output store has been performed
+    if (issuer || xissuer) {   // every MMA issued here has completed
+        uint64_t *fin = &sm.bar_fin[issuer ? 1 : 2];
+        mma_commit(fin);
+        mbar_wait_bounded(fin, 0, kPollLimit);
     }
 }
 
@@ -633,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_g, const float *__restrict__ beta,
+                      const __grid_constant__ CUtensorMap tm_g,
+                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ beta,
                       const float *__restrict__ init_state, const int32_t *__restrict__ cu,
                       OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
                       int64_t total, int64_t seq_len, float *__restrict__ ckpt,
@@ -654,11 +753,12 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.bar_tma[s], 1);
             mbar_init(&sm.bar_akempty[s], 1);
-            mbar_init(&sm.bar_up[s], 1);
+            mbar_init(&sm.bar_gops[s], 1);
             mbar_init(&sm.bar_gram[s], 1);
             mbar_init(&sm.bar_bxfull[s], 1);
             mbar_init(&sm.bar_fin[s], 1);
         }
+        mbar_init(&sm.bar_fin[2], 1);
         mbar_init(&sm.bar_x, 1);
         mbar_init(&sm.bar_u, 1);
         mbar_init(&sm.bar_s, 1);
@@ -670,6 +770,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_o);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -694,6 +795,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_st16(tb + lane_off + TM_S + c0, v);
         }
         tmem_wait_st();
+        // the block T12 of T diag(beta) (rows 0-15, columns 16-31) is zero for every chunk
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = j + 128 * q;
+            st_op(sm.tmat[e >> 8], (e >> 4) & 15, 16 + (e & 15), 0.f);
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -703,7 +811,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         prep_loop<GATED>(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb,
                          GATED ? __expf(a_log[h]) : 0.f);
     else
-        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, out, H, h, a, b, nchunks, tb, ckpt,
+        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, &tm_o, out, H, h, a, b, nchunks, tb, ckpt,
                           ckpt_every, ckpt_cap,
                           ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0,
                           GATED);
@@ -771,12 +879,14 @@ template <typename OUT_T>
 cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const void *v,
                    const float *g, const float *beta, const float *init_state, const int32_t *cu,
                    void *out, float *final_state, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv, mg;
+    CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !(P.a_log ? make_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
-                  : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
+                  : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)) ||
+        !(sizeof(OUT_T) == 2 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
+                             : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
         return cudaErrorInvalidValue;
     auto kern = P.a_log ? kda_prefill_tc_kernel<OUT_T, true> : kda_prefill_tc_kernel<OUT_T, false>;
     const size_t smem = sizeof(TcSmem) + 1024;
@@ -784,7 +894,7 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((int64_t)P.N * P.H);
-    kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, beta, init_state, cu, (OUT_T *)out,
+    kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, mo, beta, init_state, cu, (OUT_T *)out,
                                              final_state, P.H, (int64_t)P.T, P.seq_len, P.ckpt,
                                              P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity,
                                              P.a_log);
@@ -794,10 +904,11 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
 }  // namespace
 
 bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
-                              const float *g) {
+                              const float *g, const void *out) {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
     return P.dk == 128 && P.dv == 128 && P.in_dtype == KDA_DTYPE_BF16 && P.T > 0 &&
-           P.T <= 0x7fffffff - C && al16(q) && al16(k) && al16(v) && al16(g) && encode_fn() != nullptr;
+           P.T <= 0x7fffffff - C && al16(q) && al16(k) && al16(v) && al16(g) && al16(out) &&
+           encode_fn() != nullptr;
 }
 
 cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const void *k,
