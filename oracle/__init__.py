@@ -56,6 +56,7 @@ class Oracle:
         lib.kda_oracle_decode.restype = ctypes.c_int
         lib.kda_oracle_num_cpus.restype = ctypes.c_int
         lib.kda_oracle_gate.argtypes = [i32, i32, i32, dp, dp, dp, dp, dp]
+        lib.kda_oracle_output_gate.argtypes = [i32, i32, i32, dp, dp, dp, ctypes.c_double, dp]
         lib.kda_oracle_gate.restype = ctypes.c_int
         self.lib = lib
 
@@ -102,6 +103,20 @@ class Oracle:
         beta = np.empty_like(bl)
         self.lib.kda_oracle_gate(T, H, dk, _ptr(z), _ptr(a_log), _ptr(bl), _ptr(g), _ptr(beta))
         return g, beta
+
+    def output_gate(self, o, gate_logit, norm_weight=None, eps: float = 1e-6):
+        """y = Sigmoid(gate_logit) * RMSNorm(o) * norm_weight over the last axis
+        (d_v) of o, gate_logit [T, H, d_v] (fp64); norm_weight [d_v] or None
+        (C function ``kda_oracle_output_gate``)."""
+        o, gl, w = _f64(o), _f64(gate_logit), _f64(norm_weight)
+        T, H, dv = o.shape
+        assert gl.shape == o.shape and (w is None or w.shape == (dv,))
+        y = np.empty_like(o)
+        rc = self.lib.kda_oracle_output_gate(T, H, dv, _ptr(o), _ptr(gl), _ptr(w), float(eps),
+                                             _ptr(y))
+        if rc != 0:
+            raise ValueError("kda_oracle_output_gate rejected its arguments (eps must be > 0)")
+        return y
 
     def decode(self, q, k, v, g, beta, state, num_threads: int = 0, inplace: bool = False):
         """One decode step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
@@ -156,6 +171,10 @@ def prefill(*args, **kwargs):
 
 def gate(*args, **kwargs):
     return _load().gate(*args, **kwargs)
+
+
+def output_gate(*args, **kwargs):
+    return _load().output_gate(*args, **kwargs)
 
 
 def decode(*args, **kwargs):

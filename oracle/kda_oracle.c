@@ -212,6 +212,37 @@ int kda_oracle_gate(int32_t total_tokens, int32_t num_heads, int32_t d_k, const 
     return 0;
 }
 
+/* Output gate ("Inside Kimi K3", section "Sequence mixing: fixed-state KDA
+ * alongside global MLA": the layer output is W_o [Sigmoid(W_g x_t) .
+ * RMSNorm(o~_t)], with o~_t = S_t^T q_t the ungated readout).  The pages do not
+ * spell RMSNorm out; it is read here as the root-mean-square normalisation of
+ * one head's d_v channels, with an optional per-channel weight and eps inside
+ * the square root:
+ *
+ *   ms      = (1 / d_v) sum_j o~[t,h,j]^2
+ *   y[t,h,j] = Sigmoid(gate[t,h,j]) * o~[t,h,j] / sqrt(ms + eps) * w[j]
+ *
+ * w = 1 when norm_weight is NULL.  eps must be positive (a zero row then gives
+ * zeros).  Returns -1 on a bad argument, else 0. */
+int kda_oracle_output_gate(int32_t total_tokens, int32_t num_heads, int32_t d_v,
+                           const double *o, const double *gate_logit,
+                           const double *norm_weight, double eps, double *y) {
+    if (total_tokens < 0 || num_heads < 1 || d_v < 1 || !(eps > 0.0) || !o || !gate_logit || !y)
+        return -1;
+    for (int64_t t = 0; t < total_tokens; ++t)
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const int64_t row = (t * num_heads + h) * (int64_t)d_v;
+            double ss = 0.0;
+            for (int32_t j = 0; j < d_v; ++j) ss += o[row + j] * o[row + j];
+            const double rinv = 1.0 / sqrt(ss / d_v + eps);
+            for (int32_t j = 0; j < d_v; ++j) {
+                const double w = norm_weight ? norm_weight[j] : 1.0;
+                y[row + j] = sigmoid(gate_logit[row + j]) * o[row + j] * rinv * w;
+            }
+        }
+    return 0;
+}
+
 int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                       const double *q, const double *k, const double *v,
                       const double *g, const double *beta, double *state_inout,

@@ -39,6 +39,14 @@ int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t 
 int kda_oracle_gate(int32_t total_tokens, int32_t num_heads, int32_t d_k, const double *z,
                     const double *a_log, const double *beta_logit, double *g, double *beta);
 
+/* Output gate: y[t,h,j] = Sigmoid(gate_logit[t,h,j]) * o[t,h,j] /
+ * sqrt(mean_j o[t,h,:]^2 + eps) * norm_weight[j] (norm_weight NULL => 1),
+ * over [total_tokens, num_heads, d_v] arrays.  eps > 0.  Returns -1 on a bad
+ * argument, else 0. */
+int kda_oracle_output_gate(int32_t total_tokens, int32_t num_heads, int32_t d_v,
+                           const double *o, const double *gate_logit,
+                           const double *norm_weight, double eps, double *y);
+
 #ifdef __cplusplus
 }
 #endif

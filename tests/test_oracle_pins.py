@@ -221,9 +221,40 @@ def pin_gate_closed_forms(orc):
     assert np.all((gp > -5.0) & (gp < 0.0))
 
 
+def pin_output_gate_closed_forms(orc):
+    """Output gate, y = Sigmoid(gate) . RMSNorm(o~) with RMSNorm over one
+    head's d_v channels ("Inside Kimi K3", section "Sequence mixing"):
+    - a constant row c (any sign) normalises to sign(c); a zero logit halves it;
+    - a logit of ln 3 gives Sigmoid = 3/4, and the weight scales channel j;
+    - with eps = 3 c^2 a constant row c gives c / sqrt(4 c^2) = sign(c) / 2;
+    - each (token, head) row, whatever its scale, leaves with mean square 1
+      under an open gate (rows are normalised one head at a time);
+    - a zero row stays zero."""
+    T, H, dv = 2, 3, 8
+    o = np.empty((T, H, dv))
+    o[:, 0, :] = 3.0
+    o[:, 1, :] = -2.0
+    o[:, 2, :] = 0.0
+    y = orc.output_gate(o, np.zeros_like(o), eps=1e-30)
+    assert np.allclose(y[:, 0], 0.5, rtol=0, atol=1e-15)
+    assert np.allclose(y[:, 1], -0.5, rtol=0, atol=1e-15)
+    assert np.all(y[:, 2] == 0.0)
+    w = np.arange(1.0, dv + 1.0)
+    y = orc.output_gate(np.ones((T, H, dv)), np.full((T, H, dv), np.log(3.0)), norm_weight=w,
+                        eps=1e-30)
+    assert np.allclose(y, 0.75 * w, rtol=1e-15, atol=0)
+    y = orc.output_gate(o[:, :2], np.zeros((T, 2, dv)), eps=3.0 * 4.0)   # c = -2: eps = 3 c^2
+    assert np.allclose(y[:, 1], -0.25, rtol=0, atol=1e-15)
+    rng = np.random.default_rng(11)
+    o = rng.standard_normal((4, 3, 16)) * np.array([1e-3, 1.0, 1e3])[None, :, None]
+    y = orc.output_gate(o, np.full(o.shape, 40.0), eps=1e-30)
+    assert np.allclose((y ** 2).mean(axis=-1), 1.0, rtol=1e-12, atol=0)
+    assert np.all(np.sign(y) == np.sign(o))
+
+
 PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
         pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound,
-        pin_gate_closed_forms]
+        pin_gate_closed_forms, pin_output_gate_closed_forms]
 
 
 def _run_pin(pin, orc, golden):
@@ -336,6 +367,16 @@ MUTANTS = {
                   "g[i] = KDA_ORACLE_G_MIN * sigmoid(-scale * z[i]);"),
     "gate_beta_raw": ("beta[t * num_heads + h] = sigmoid(beta_logit[t * num_heads + h]);",
                       "beta[t * num_heads + h] = beta_logit[t * num_heads + h];"),
+    "ogate_sum_not_mean": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
+                           "const double rinv = 1.0 / sqrt(ss + eps);"),
+    "ogate_eps_outside_root": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
+                               "const double rinv = 1.0 / (sqrt(ss / d_v) + eps);"),
+    "ogate_gate_sign": ("y[row + j] = sigmoid(gate_logit[row + j]) * o[row + j] * rinv * w;",
+                        "y[row + j] = sigmoid(-gate_logit[row + j]) * o[row + j] * rinv * w;"),
+    "ogate_weight_dropped": ("const double w = norm_weight ? norm_weight[j] : 1.0;",
+                             "const double w = 1.0;"),
+    "ogate_norm_over_heads": ("            double ss = 0.0;\n            for (int32_t j = 0; j < d_v; ++j) ss += o[row + j] * o[row + j];",
+                              "            double ss = 0.0;\n            for (int32_t j = 0; j < d_v; ++j) ss += o[t * num_heads * (int64_t)d_v + j] * o[t * num_heads * (int64_t)d_v + j];"),
 }
 
 
