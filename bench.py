@@ -38,6 +38,8 @@ UNIT = "tokens/s"
 PREFILL_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 96 * 128 * 4 + 96 * 4  # 147840
 # the gated call reads bf16 decay logits z instead of fp32 g, and beta logits
 GATED_BYTES_PER_TOKEN = 5 * 96 * 128 * 2 + 96 * 4  # 123264
+# the output-gated call also reads the bf16 gate logits [T, H, d_v]
+OGATED_BYTES_PER_TOKEN = 147840 + 96 * 128 * 2  # 172416
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -360,6 +362,27 @@ def run_gpu(args):
                           "algorithmic_bytes_per_launch": GATED_BYTES_PER_TOKEN * T}}
     del gl
 
+    # ---------------- the same layer with the output gate fused into the store ----------------
+    og = synth.output_gate_inputs(T, w.heads, w.d, dtype=w.dtype, seed=83, device=dev)
+
+    def ogated_step():
+        kda.kda_prefill_output_gated(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     og["gate"], og["norm_weight"], 1e-6,
+                                     cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
+                                     stream=stream)
+
+    ms_og, _, _ = time_steps(ogated_step, ck_steps, max(args.warmup, 3), world, stream)
+    og_ach = OGATED_BYTES_PER_TOKEN * T / (ms_og * 1e-3) / 1e9
+    output_gated = {
+        "value": T * world / (ms_og * 1e-3), "unit": UNIT, "ms_per_step": ms_og, "steps": ck_steps,
+        "config": {"workload": "prefill_8k inputs with output-gate logits: bf16 ~ N(0, 1), "
+                               "norm weight ~ U(0.5, 1.5), eps 1e-6; bf16 out (fused epilogue)"},
+        "roofline": {"bound": "hbm", "achieved": og_ach, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": og_ach / hbm_gbs, "peak_source": peak_src,
+                     "kernel": "kda_prefill_tc_kernel",
+                     "algorithmic_bytes_per_launch": OGATED_BYTES_PER_TOKEN * T}}
+    del og
+
     # ---------------- e2e through the public API, host buffers ----------------
     host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
     dbuf = {x: torch.empty_like(inp[x]) for x in host}
@@ -433,7 +456,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-            "checkpointed": checkpointed, "gated": gated,
+            "checkpointed": checkpointed, "gated": gated, "output_gated": output_gated,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

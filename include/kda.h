@@ -174,6 +174,40 @@ kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k,
                              float *final_state, kda_stream_t stream);
 
 /*
+ * kda_prefill_output_gated -- kda_prefill followed by the layer's output gate,
+ * fused into the store of the output where the kernel allows:
+ *
+ *   y[t,h,j] = Sigmoid(gate_logit[t,h,j]) * o~[t,h,j] / sqrt(ms + eps) * w[j],
+ *   ms = (1/d_v) sum_j o~[t,h,j]^2
+ *
+ * with o~ the ungated readout that kda_prefill would write.  The pages give
+ * the layer output as W_o [Sigmoid(W_g x_t) . RMSNorm(o~_t)] ("Inside Kimi
+ * K3", section "Sequence mixing: fixed-state KDA alongside global MLA"); this
+ * call forms the bracket.  The pages do not define the norm further; here it
+ * is the root-mean-square over one head's d_v channels with eps inside the
+ * root and an optional per-channel weight.  The projections W_g, W_o stay
+ * with the caller.
+ *
+ *   gate_logit  device, in_dtype, [T_tot, H, d_v]: W_g x_t per head; must not
+ *               alias `out`.
+ *   norm_weight device fp32 [d_v], 4-byte aligned, or NULL (weight 1).
+ *   eps         finite, > 0.
+ *
+ * The tensor-core kernel applies the gate before its store when out is bf16
+ * and gate_logit is 16-byte aligned; otherwise the prefill writes o~ and a
+ * second kernel gates `out` in place (with a bf16 `out`, o~ is then rounded
+ * to bf16 once before the norm).  Every other argument, and every other
+ * error, is as in kda_prefill; KDA_ERR_INVALID_ARGUMENT if there are tokens
+ * and gate_logit is NULL or equals out, or eps is not a positive finite
+ * number, or norm_weight is misaligned.
+ */
+kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const void *gate_logit, const float *norm_weight, float eps,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, kda_stream_t stream);
+
+/*
  * kda_decode -- one single-token update of N independent fixed-size states.
  *
  * For each sequence n and head h: M = Diag(exp g) S, u = beta (v - M^T k),

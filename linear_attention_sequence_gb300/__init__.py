@@ -9,6 +9,7 @@ method and has no fallback: if the library is missing, every call raises.
     kda_prefill(q, k, v, g, beta, ...)  chunk-parallel prefill, packed batch
     kda_prefill_checkpointed(...)       the same, plus state checkpoints every `interval` tokens
     kda_prefill_gated(q, k, v, z, a_log, beta_logit, ...)   the same, from gate logits
+    kda_prefill_output_gated(q, k, v, g, beta, gate_logit, ...)   the same, then the output gate
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -18,7 +19,8 @@ import os
 
 import torch
 
-__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
+           "kda_prefill_output_gated", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -71,6 +73,9 @@ def lib():
         L.kda_prefill_gated.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, fp, fp, fp, vp, vp, fp,
                                         vp]
         L.kda_prefill_gated.restype = ctypes.c_int
+        L.kda_prefill_output_gated.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, vp, fp,
+                                               ctypes.c_float, fp, vp, vp, fp, vp]
+        L.kda_prefill_output_gated.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -214,6 +219,32 @@ def kda_prefill_gated(q, k, v, z, a_log, beta_logit, init_state=None, cu_seqlens
                                  _ptr(a_log), _ptr(beta_logit), _ptr(init_state),
                                  _ptr(cu_seqlens), _ptr(out), _ptr(final_state), _stream(stream))
     _check(st, "kda_prefill_gated")
+    return out, final_state
+
+
+def kda_prefill_output_gated(q, k, v, g, beta, gate_logit, norm_weight=None, eps=1e-6,
+                             init_state=None, cu_seqlens=None, *, num_seqs=None, out=None,
+                             final_state=None, out_dtype=None, variant=PREFILL_DEFAULT,
+                             return_final_state=True, stream=None):
+    """Prefill followed by the output gate (C entry point
+    ``kda_prefill_output_gated``): out = Sigmoid(gate_logit) * o~ /
+    sqrt(mean over d_v of o~^2 + eps) * norm_weight, per token and head.
+    gate_logit has the dtype and shape of v; norm_weight fp32 [d_v] or None.
+    Returns ``(out, final_state)``."""
+    if gate_logit.dtype != v.dtype or gate_logit.shape != v.shape:
+        raise ValueError("gate_logit must have the dtype and shape of v")
+    _require(gate_logit, "gate_logit", v.dtype, 3)
+    _require(norm_weight, "norm_weight", torch.float32, 1)
+    if norm_weight is not None and norm_weight.shape[0] != v.shape[2]:
+        raise ValueError("norm_weight must hold one value per value channel")
+    dims, out, final_state = _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs,
+                                           out, final_state, out_dtype, variant,
+                                           return_final_state)
+    st = lib().kda_prefill_output_gated(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(gate_logit), _ptr(norm_weight),
+                                        ctypes.c_float(eps), _ptr(init_state), _ptr(cu_seqlens),
+                                        _ptr(out), _ptr(final_state), _stream(stream))
+    _check(st, "kda_prefill_output_gated")
     return out, final_state
 
 

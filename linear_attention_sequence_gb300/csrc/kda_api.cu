@@ -1,6 +1,7 @@
 // kda_api.cu -- the C ABI front end: argument validation, kernel selection,
 // launch and error mapping.  Declarations and semantics: include/kda.h.
 
+#include <math.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -78,12 +79,23 @@ kda_status kda_get_last_device_error(kda_stream_t stream) {
 
 namespace {
 
+// The optional parts of a prefill call (all off by default).
+struct Extras {
+    float *ckpt = nullptr;            // state checkpoints
+    int64_t ckpt_interval = 0, ckpt_capacity = 0;
+    const void *z = nullptr;          // gate prologue: decay logits instead of g
+    const float *a_log = nullptr;
+    const void *ogate = nullptr;      // output gate
+    const float *onorm_w = nullptr;
+    float oeps = 0.f;
+};
+
 kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, const void *v,
                           const float *g, const float *beta, const float *init_state,
                           const int32_t *cu_seqlens, void *out, float *final_state,
-                          float *ckpt, int64_t ckpt_interval, int64_t ckpt_capacity,
-                          const void *z, const float *a_log, kda_stream_t stream,
-                          const char *where) {
+                          const Extras &x, kda_stream_t stream, const char *where) {
+    const void *z = x.z;
+    const float *a_log = x.a_log;
     kda::Problem P;
     kda_status st = check_dims(dims, P);
     if (st != KDA_OK) return st;
@@ -104,18 +116,28 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     }
     P.z = a_log ? z : nullptr;
     P.a_log = a_log;
-    P.ckpt = ckpt_capacity > 0 ? ckpt : nullptr;
-    P.ckpt_interval = ckpt_interval;
-    P.ckpt_capacity = ckpt_capacity;
+    P.ckpt = x.ckpt_capacity > 0 ? x.ckpt : nullptr;
+    P.ckpt_interval = x.ckpt_interval;
+    P.ckpt_capacity = x.ckpt_capacity;
+    if (P.T > 0 && x.ogate) {
+        P.ogate = x.ogate;
+        P.onorm_w = x.onorm_w;
+        P.oeps = x.oeps;
+    }
     const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in, out);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
+    // the tensor-core kernel gates its bf16 output before the store (the gate
+    // tile arrives by TMA); every other case gates `out` in place afterwards
+    P.ogate_fused = P.ogate && use_tc && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
+                    aligned16(P.ogate);
     cudaError_t e = use_tc ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                    out, final_state, s)
                            : kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                      out, final_state, s);
+    if (e == cudaSuccess && P.ogate && !P.ogate_fused) e = kda_launch_output_gate(P, out, s);
     if (e != cudaSuccess) return cuda_fail(e, where);
     return KDA_OK;
 }
@@ -127,7 +149,7 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                        const int32_t *cu_seqlens, void *out, float *final_state,
                        kda_stream_t stream) {
     return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
-                          nullptr, 0, 0, nullptr, nullptr, stream, "kda_prefill");
+                          Extras(), stream, "kda_prefill");
 }
 
 kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const void *k,
@@ -138,9 +160,12 @@ kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const v
     if (interval <= 0 || interval % KDA_CHUNK != 0 || capacity < 0) return KDA_ERR_INVALID_ARGUMENT;
     if (capacity > 0 && (!checkpoints || ((uintptr_t)checkpoints & 3u)))
         return KDA_ERR_INVALID_ARGUMENT;
-    return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
-                          checkpoints, interval, capacity, nullptr, nullptr, stream,
-                          "kda_prefill_checkpointed");
+    Extras x;
+    x.ckpt = checkpoints;
+    x.ckpt_interval = interval;
+    x.ckpt_capacity = capacity;
+    return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, x,
+                          stream, "kda_prefill_checkpointed");
 }
 
 kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k, const void *v,
@@ -151,9 +176,31 @@ kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k,
     if (dims->total_tokens > 0 && (!z || !a_log)) return KDA_ERR_INVALID_ARGUMENT;
     // with no tokens nothing is read: the call only copies the initial states
     const bool any = dims->total_tokens > 0;
+    Extras x;
+    x.z = any ? z : nullptr;
+    x.a_log = any ? a_log : nullptr;
     return prefill_common(dims, q, k, v, nullptr, beta_logit, init_state, cu_seqlens, out,
-                          final_state, nullptr, 0, 0, any ? z : nullptr, any ? a_log : nullptr,
-                          stream, "kda_prefill_gated");
+                          final_state, x, stream, "kda_prefill_gated");
+}
+
+kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const void *gate_logit, const float *norm_weight, float eps,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, kda_stream_t stream) {
+    if (!dims) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARGUMENT;
+    if (norm_weight && ((uintptr_t)norm_weight & 3u)) return KDA_ERR_INVALID_ARGUMENT;
+    if (dims->total_tokens > 0 && (!gate_logit || gate_logit == (const void *)out))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (gate_logit && ((uintptr_t)gate_logit & (dims->in_dtype == KDA_DTYPE_BF16 ? 1u : 3u)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    Extras x;
+    x.ogate = gate_logit;
+    x.onorm_w = norm_weight;
+    x.oeps = eps;
+    return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, x,
+                          stream, "kda_prefill_output_gated");
 }
 
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,

@@ -45,6 +45,11 @@ struct Problem {
     float *ckpt = nullptr;
     int64_t ckpt_interval = 0;  // tokens between checkpoints, a multiple of the chunk length
     int64_t ckpt_capacity = 0;  // rows of [capacity, H, d_k, d_v] that may be written
+    // output gate (kda_prefill_output_gated): y = Sigmoid(gate) RMSNorm(o~) w
+    const void *ogate = nullptr;     // gate logits, in_dtype [T, H, d_v]; nullptr: none
+    const float *onorm_w = nullptr;  // [d_v] or nullptr (weight 1)
+    float oeps = 0.f;
+    bool ogate_fused = false;        // applied by the tensor-core kernel before its store
 };
 
 // Gate prologue ("Understanding Kimi K3's Attention", log-decay bound and
@@ -81,6 +86,7 @@ cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const vo
                                   const void *v, const float *g, const float *beta,
                                   const float *init_state, const int32_t *cu, void *out,
                                   float *final_state, cudaStream_t stream);
+cudaError_t kda_launch_output_gate(const kda::Problem &P, void *out, cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
 cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,

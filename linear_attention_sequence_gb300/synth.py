@@ -146,3 +146,14 @@ def gate_logits(T, H, d, dtype=torch.float32, seed=0, device="cpu"):
     a_log = 0.1 * torch.randn((H,), generator=gen, device=device, dtype=torch.float32)
     beta_logit = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32)
     return dict(z=z, a_log=a_log, beta_logit=beta_logit)
+
+
+
+def output_gate_inputs(T, H, dv, dtype=torch.float32, seed=0, device="cpu"):
+    """Inputs of the output gate: gate logits W_g x_t ~ N(0, 1) per (token, head,
+    value channel), in the activation dtype, and a per-channel norm weight
+    ~ U(0.5, 1.5) (fp32)."""
+    gen = _gen(seed, device)
+    gate = torch.randn((T, H, dv), generator=gen, device=device, dtype=torch.float32).to(dtype)
+    w = 0.5 + torch.rand((dv,), generator=gen, device=device, dtype=torch.float32)
+    return dict(gate=gate, norm_weight=w)

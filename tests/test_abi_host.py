@@ -168,6 +168,34 @@ def test_prefill_gated_empty_batch_is_ok(L):
                          a=None, bl=None, out=None) == OK
 
 
+def prefill_ogated(L, dims, eps=1e-6, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, gl=ctypes.c_void_p(0x60000), w=None,
+                init=None, cu=None, out=ctypes.c_void_p(0x20000), fin=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_prefill_output_gated(d, args["q"], args["k"], args["v"], args["g"], args["beta"],
+                                      args["gl"], args["w"], ctypes.c_float(eps), args["init"],
+                                      args["cu"], args["out"], args["fin"], None)
+
+
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(), {"gl": None}), (D(), {"q": None}),
+    (D(), {"g": None}), (D(), {"gl": ctypes.c_void_p(0x20000)}),     # gate aliases out
+    (D(), {"gl": ctypes.c_void_p(0x60001)}),                         # misaligned bf16 gate
+    (D(in_dtype=0), {"gl": ctypes.c_void_p(0x60002)}),               # misaligned fp32 gate
+    (D(), {"w": ctypes.c_void_p(0x80002)}),                          # misaligned weight
+    (D(), {"eps": 0.0}), (D(), {"eps": -1e-6}), (D(), {"eps": float("nan")}),
+    (D(), {"eps": float("inf")}), (D(num_seqs=3, total_tokens=16), {}),
+])
+def test_prefill_output_gated_rejects(L, dims, over):
+    assert prefill_ogated(L, dims, **over) == INVALID
+
+
+def test_prefill_output_gated_empty_batch_is_ok(L):
+    assert prefill_ogated(L, D(num_seqs=0, total_tokens=0), q=None, k=None, v=None, g=None,
+                          beta=None, gl=None, out=None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

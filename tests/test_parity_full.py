@@ -141,3 +141,27 @@ def test_gated_prefill_8k_sampled_heads():
     es = rel_err(host64(fin[:, heads]), s_ref)
     print(f"gated prefill_8k (3 heads): err_o {eo:.3e} err_S {es:.3e}")
     assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
+
+
+def test_output_gated_8k_sampled_heads():
+    """The 8K layer with the output gate fused into the store (bf16 out, the
+    launch the benchmark times): three heads against the oracle's prefill
+    followed by the oracle's output gate."""
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, "cuda")
+    og = synth.output_gate_inputs(w.total_tokens, w.heads, w.d, dtype=w.dtype, seed=83,
+                                  device="cuda")
+    eps = 1e-6
+    out, fin = kda.kda_prefill_output_gated(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                            og["gate"], og["norm_weight"], eps,
+                                            cu_seqlens=inp["cu_seqlens"])
+    assert out.dtype == torch.bfloat16
+    heads = [0, 47, 95]
+    o_ref, s_ref = oracle.prefill(*(host64(inp[x][:, heads]) for x in ("q", "k", "v", "g", "beta")))
+    y_ref = oracle.output_gate(o_ref, host64(og["gate"][:, heads]), host64(og["norm_weight"]), eps)
+    eo = rel_err(host64(out[:, heads]), y_ref)
+    es = rel_err(host64(fin[:, heads]), s_ref)
+    bound = TOL[torch.bfloat16] + 2.0 ** -8 * np.abs(y_ref).max() / np.sqrt(np.mean(y_ref ** 2))
+    print(f"output-gated prefill_8k (3 heads, bf16 out): err_y {eo:.3e} (bound {bound:.3e}) "
+          f"err_S {es:.3e}")
+    assert eo <= bound and es <= TOL[torch.bfloat16]

@@ -348,3 +348,101 @@ def test_gated_prefill_equals_prefill_of_gate(variant):
     tol = TOL[dtype]
     assert rel_err(host64(out), host64(out0)) <= tol
     assert rel_err(host64(fin), host64(fin0)) <= tol
+
+
+# ---------------------------------------------------------------------------
+# output gate: y = Sigmoid(gate) RMSNorm(o~) w
+# ---------------------------------------------------------------------------
+
+OG_EPS = 1e-6
+
+
+def run_output_gated(inp, og, variant, out_dtype, cu=None, weight=True):
+    try:
+        return kda.kda_prefill_output_gated(
+            inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], og["gate"],
+            og["norm_weight"] if weight else None, OG_EPS, init_state=inp.get("init_state"),
+            cu_seqlens=cu, out_dtype=out_dtype, variant=variant)
+    except kda.KdaError as e:
+        if e.status == 2:
+            pytest.skip("variant does not take this shape/dtype (KDA_ERR_UNSUPPORTED)")
+        raise
+
+
+def check_bf16_out(out, y_ref, dtype):
+    """A bf16 output: the fp32 bound plus half a bf16 ulp of the largest value."""
+    ref = np.asarray(y_ref)
+    bound = TOL[dtype] + 2.0 ** -8 * np.max(np.abs(ref)) / np.sqrt(np.mean(ref ** 2))
+    e = rel_err(host64(out), ref)
+    assert e <= bound, f"bf16 output error {e:.3e} > {bound:.3e}"
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_output_gated_matches_oracle(variant, d, dtype, out_dtype):
+    """kda_prefill_output_gated on a ragged packed batch against the oracle's
+    prefill followed by the oracle's output gate.  A bf16 output on the
+    tensor-core path takes the fused epilogue; the other cases gate in place."""
+    if not supported(variant, d, dtype):
+        pytest.skip("variant does not take this shape/dtype")
+    H = 2
+    lens = [1, 31, 32, 0, 65, 100]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=81, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    og = synth.output_gate_inputs(T, H, d, dtype=dtype, seed=82, device=DEV)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    out, fin = run_output_gated(inp, og, variant, out_dtype, cu=cu)
+    o_ref, s_ref = run_oracle(inp, cu=cu)
+    y_ref = oracle.output_gate(o_ref, host64(og["gate"]), host64(og["norm_weight"]), OG_EPS)
+    es = rel_err(host64(fin), s_ref)
+    assert es <= TOL[dtype], f"final-state error {es:.3e}"
+    if out_dtype == torch.float32:
+        eo = rel_err(host64(out), y_ref)
+        assert eo <= TOL[dtype], f"gated output error {eo:.3e} > {TOL[dtype]}"
+    else:
+        check_bf16_out(out, y_ref, dtype)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_output_gate_of_the_kernels_own_readout(variant, out_dtype):
+    """The epilogue alone: the gated output equals the gate applied in fp64 to
+    the ungated fp32 readout the same kernel writes (kda_prefill), to fp32
+    rounding (fp32 out).  A bf16 out is one bf16 rounding away on the fused
+    tensor-core path, and at most two on the in-place path (o~ itself goes
+    through bf16 there).  Full chunks and a ragged tail; no weight, then a
+    weight."""
+    T, H, d = 150, 3, 128
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=91, device=DEV)
+    og = synth.output_gate_inputs(T, H, d, dtype=dtype, seed=92, device=DEV)
+    o32, _ = kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                             out_dtype=torch.float32, variant=variant)
+    o = host64(o32)
+    gate = host64(og["gate"])
+    for weight in (False, True):
+        w = host64(og["norm_weight"]) if weight else np.ones(d)
+        rinv = 1.0 / np.sqrt((o ** 2).mean(axis=-1, keepdims=True) + OG_EPS)
+        y = o * rinv * w / (1.0 + np.exp(-gate))
+        out, _ = run_output_gated(inp, og, variant, out_dtype, weight=weight)
+        if out_dtype == torch.float32:
+            assert np.allclose(host64(out), y, rtol=2e-6, atol=1e-6 * np.abs(y).max())
+        else:
+            fused = dtype == torch.bfloat16   # this shape on bf16 inputs runs the tensor-core kernel
+            rel = 2.0 ** -8 if fused else 2.0 ** -7
+            assert np.all(np.abs(host64(out) - y) <= rel * np.abs(y) + 1e-6 * np.abs(y).max())
+
+
+def test_output_gate_zero_rows_stay_zero():
+    """Zero values give a zero readout, and the gated output of a zero row is
+    zero (eps > 0), on the fused and the in-place paths."""
+    T, H, d = 64, 2, 128
+    inp = synth.random_inputs(T, H, d, dtype=torch.bfloat16, seed=93, device=DEV)
+    inp["v"].zero_()
+    og = synth.output_gate_inputs(T, H, d, dtype=torch.bfloat16, seed=94, device=DEV)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        out, _ = run_output_gated(inp, og, kda.PREFILL_DEFAULT, out_dtype)
+        assert torch.count_nonzero(out).item() == 0
