@@ -52,6 +52,8 @@ class Oracle:
         lib.kda_oracle_prefill.argtypes = [i32, i32, i32, i32, i32, dp, dp, dp, dp, dp,
                                            dp, ip, dp, dp, i32]
         lib.kda_oracle_prefill.restype = ctypes.c_int
+        lib.kda_oracle_prefill_scalar_decay.argtypes = lib.kda_oracle_prefill.argtypes
+        lib.kda_oracle_prefill_scalar_decay.restype = ctypes.c_int
         lib.kda_oracle_decode.argtypes = [i32, i32, i32, i32, dp, dp, dp, dp, dp, dp, dp, i32]
         lib.kda_oracle_decode.restype = ctypes.c_int
         lib.kda_oracle_num_cpus.restype = ctypes.c_int
@@ -90,6 +92,26 @@ class Oracle:
         if rc != 0:
             raise ValueError("kda_oracle_prefill rejected its arguments (shapes, "
                              "cu_seqlens, or gates outside g in [-5,0], beta in [0,1])")
+        return out, fin
+
+    def prefill_scalar_decay(self, q, k, v, g_head, beta, init_state=None, cu_seqlens=None,
+                             num_seqs=None, num_threads: int = 0):
+        """Gated DeltaNet: one log-decay per (token, head), g_head [T, H], or
+        None for the delta rule (alpha = 1).  Other arguments and the result as
+        :meth:`prefill` (C function ``kda_oracle_prefill_scalar_decay``)."""
+        q, k, v, gh, beta, init = (_f64(x) for x in (q, k, v, g_head, beta, init_state))
+        T, H, dk = q.shape
+        dv = v.shape[2]
+        assert gh is None or gh.shape == (T, H)
+        cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = (cu.shape[0] - 1) if cu is not None else (1 if num_seqs is None else int(num_seqs))
+        out = np.zeros((T, H, dv), np.float64)
+        fin = np.zeros((N, H, dk, dv), np.float64)
+        rc = self.lib.kda_oracle_prefill_scalar_decay(
+            N, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(gh), _ptr(beta), _ptr(init),
+            _ptr(cu, ctypes.c_int32), _ptr(out), _ptr(fin), int(num_threads))
+        if rc != 0:
+            raise ValueError("kda_oracle_prefill_scalar_decay rejected its arguments")
         return out, fin
 
     def gate(self, z, a_log, beta_logit):
@@ -167,6 +189,10 @@ def _ptr(a, ctype=ctypes.c_double):
 def prefill(*args, **kwargs):
     """Module-level form of :meth:`Oracle.prefill` on the default build."""
     return _load().prefill(*args, **kwargs)
+
+
+def prefill_scalar_decay(*args, **kwargs):
+    return _load().prefill_scalar_decay(*args, **kwargs)
 
 
 def gate(*args, **kwargs):

@@ -190,6 +190,32 @@ int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads
     return rc;
 }
 
+/* Gated DeltaNet and the delta rule ("Kimi K3.1 and the Road From Softmax
+ * Attention to Kimi Delta Attention", sections "3. The delta rule" and "4.
+ * Gating"): S_t = (I - beta_t k_t k_t^T) alpha_t S_{t-1} + beta_t k_t v_t^T
+ * with one decay alpha_t = exp(g_head[t,h]) per head and step; with g_head
+ * NULL, alpha_t = 1, the delta rule.  A scalar decay scales every key channel
+ * alike, so this is the channel-wise recurrence above with g[t,h,c] =
+ * g_head[t,h] for every channel c. */
+int kda_oracle_prefill_scalar_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    int32_t d_k, int32_t d_v, const double *q, const double *k,
+                                    const double *v, const double *g_head, const double *beta,
+                                    const double *init_state, const int32_t *cu_seqlens,
+                                    double *out, double *final_state, int32_t num_threads) {
+    if (total_tokens < 0 || num_heads <= 0 || d_k <= 0) return -1;
+    const int64_t n = (int64_t)total_tokens * num_heads * d_k;
+    double *g = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    if (!g) return -1;
+    for (int64_t t = 0; t < total_tokens; ++t)
+        for (int32_t h = 0; h < num_heads; ++h)
+            for (int32_t c = 0; c < d_k; ++c)
+                g[(t * num_heads + h) * (int64_t)d_k + c] = g_head ? g_head[t * num_heads + h] : 0.0;
+    const int rc = kda_oracle_prefill(num_seqs, total_tokens, num_heads, d_k, d_v, q, k, v, g, beta,
+                                      init_state, cu_seqlens, out, final_state, num_threads);
+    free(g);
+    return rc;
+}
+
 /* Gate prologue.  "Understanding Kimi K3's Attention": the log-decay bound
  * equation g_t = g_min Sigmoid(e^{A_h} z_t) (per key channel; A_h the
  * per-head log-scale of the symbol table, z_t the decay logit), and the

@@ -27,6 +27,15 @@ int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads
                        const double *init_state, const int32_t *cu_seqlens,
                        double *out, double *final_state, int32_t num_threads);
 
+/* Gated DeltaNet (one decay per head and step: alpha_t = exp(g_head[t,h]),
+ * g_head [total_tokens, num_heads]) and, with g_head NULL, the delta rule
+ * (alpha_t = 1).  Other arguments as kda_oracle_prefill. */
+int kda_oracle_prefill_scalar_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    int32_t d_k, int32_t d_v, const double *q, const double *k,
+                                    const double *v, const double *g_head, const double *beta,
+                                    const double *init_state, const int32_t *cu_seqlens,
+                                    double *out, double *final_state, int32_t num_threads);
+
 /* One decode step: one token per sequence, state updated in place. */
 int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                       const double *q, const double *k, const double *v,

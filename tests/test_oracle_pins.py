@@ -252,15 +252,61 @@ def pin_output_gate_closed_forms(orc):
     assert np.all(np.sign(y) == np.sign(o))
 
 
+def pin_scalar_decay_closed_forms(orc, gold):
+    """Gated DeltaNet and the delta rule ("Kimi K3.1 and the Road ...",
+    sections "3. The delta rule" and "4. Gating"):
+    - without a decay (g_head None) the toy memory experiment gives the
+      page's delta-rule errors 0.00 (rewritten key) and 0.36 (key 5);
+    - beta = 0 writes nothing: S_t = exp(sum of g_head up to t) S_0, one
+      factor per head (heads decay at different rates);
+    - brute-force unrolled products with the scalar transition
+      alpha_s (I - beta_s k_s k_s^T)."""
+    d, n = int(gold["d"]), int(gold["pairs"])
+    rng = np.random.default_rng(int(gold["seed"]))
+    keys = np.stack([_unit(rng.standard_normal(d)) for _ in range(n)])
+    vals = np.stack([rng.standard_normal(d) for _ in range(n)])
+    new0 = rng.standard_normal(d)
+    ks = np.concatenate([keys, keys[:1]])
+    vs = np.concatenate([vals, new0[None]])
+    _, fin = orc.prefill_scalar_decay(ks[:, None], ks[:, None], vs[:, None], None,
+                                      np.ones((ks.shape[0], 1)))
+    S = fin[0, 0]
+    rel = lambda key, target: np.linalg.norm(S.T @ key - target) / np.linalg.norm(target)
+    assert round(rel(keys[0], new0), 2) == gold["delta_rule_key0"]
+    assert round(rel(keys[5], vals[5]), 2) == gold["delta_rule_key5"]
+
+    T, H, dk, dv = 9, 2, 4, 6
+    q, k, v, _, beta = _rand_case(RNG, T, H, dk, dv)
+    gh = -RNG.uniform(0.0, 1.0, (T, H)) * np.array([0.2, 2.0])
+    S0 = RNG.standard_normal((1, H, dk, dv))
+    out, fin = orc.prefill_scalar_decay(q, k, v, gh, np.zeros((T, H)), init_state=S0)
+    for h in range(H):
+        for t in range(T):
+            St = np.exp(gh[:t + 1, h].sum()) * S0[0, h]
+            assert np.allclose(out[t, h], St.T @ q[t, h], atol=1e-13, rtol=1e-13)
+        assert np.allclose(fin[0, h], np.exp(gh[:, h].sum()) * S0[0, h], atol=1e-13, rtol=1e-13)
+
+    for (T, dk, dv) in [(5, 3, 4), (8, 4, 2)]:
+        q, k, v, _, beta = _rand_case(RNG, T, H, dk, dv, unit_keys=False)
+        gh = -RNG.uniform(0.0, 1.5, (T, H))
+        S0 = RNG.standard_normal((1, H, dk, dv))
+        out, fin = orc.prefill_scalar_decay(q, k, v, gh, beta, init_state=S0)
+        for h in range(H):
+            g_full = np.repeat(gh[:, h:h + 1], dk, axis=1)
+            o_ref, S_ref = _brute(q[:, h], k[:, h], v[:, h], g_full, beta[:, h], S0[0, h])
+            assert np.max(np.abs(out[:, h] - o_ref)) < 1e-12
+            assert np.max(np.abs(fin[0, h] - S_ref)) < 1e-12
+
+
 PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
         pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound,
-        pin_gate_closed_forms, pin_output_gate_closed_forms]
+        pin_gate_closed_forms, pin_output_gate_closed_forms, pin_scalar_decay_closed_forms]
 
 
 def _run_pin(pin, orc, golden):
     if pin is pin_worked_example:
         pin(orc, golden("worked_delta_example.txt"))
-    elif pin is pin_toy_memory:
+    elif pin is pin_toy_memory or pin is pin_scalar_decay_closed_forms:
         pin(orc, golden("toy_delta_memory.txt"))
     else:
         pin(orc)
@@ -367,6 +413,9 @@ MUTANTS = {
                   "g[i] = KDA_ORACLE_G_MIN * sigmoid(-scale * z[i]);"),
     "gate_beta_raw": ("beta[t * num_heads + h] = sigmoid(beta_logit[t * num_heads + h]);",
                       "beta[t * num_heads + h] = beta_logit[t * num_heads + h];"),
+    "scalar_decay_ignored": ("g_head ? g_head[t * num_heads + h] : 0.0;", "0.0;"),
+    "scalar_decay_one_head": ("g_head ? g_head[t * num_heads + h] : 0.0;",
+                              "g_head ? g_head[t * num_heads] : 0.0;"),
     "ogate_sum_not_mean": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
                            "const double rinv = 1.0 / sqrt(ss + eps);"),
     "ogate_eps_outside_root": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
