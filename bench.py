@@ -40,6 +40,8 @@ PREFILL_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 96 * 128 * 4 + 96 * 4  # 147840
 GATED_BYTES_PER_TOKEN = 5 * 96 * 128 * 2 + 96 * 4  # 123264
 # the output-gated call also reads the bf16 gate logits [T, H, d_v]
 OGATED_BYTES_PER_TOKEN = 147840 + 96 * 128 * 2  # 172416
+# the scalar-decay call (Gated DeltaNet) reads one fp32 log-decay per (token, head) instead of g
+SDECAY_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 2 * 96 * 4  # 99072
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -383,6 +385,26 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": OGATED_BYTES_PER_TOKEN * T}}
     del og
 
+    # ---------------- Gated DeltaNet: one decay per head and step ----------------
+    gh = synth.scalar_decay(T, w.heads, seed=85, device=dev)
+
+    def sdecay_step():
+        kda.kda_prefill_scalar_decay(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+                                     cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
+                                     stream=stream)
+
+    ms_sd, _, _ = time_steps(sdecay_step, ck_steps, max(args.warmup, 3), world, stream)
+    sd_ach = SDECAY_BYTES_PER_TOKEN * T / (ms_sd * 1e-3) / 1e9
+    scalar_decay = {
+        "value": T * world / (ms_sd * 1e-3), "unit": UNIT, "ms_per_step": ms_sd, "steps": ck_steps,
+        "config": {"workload": "prefill_8k inputs, one log-decay per (token, head): "
+                               "max(-5, log Sigmoid(x)), x ~ N(2, 1)"},
+        "roofline": {"bound": "hbm", "achieved": sd_ach, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": sd_ach / hbm_gbs, "peak_source": peak_src,
+                     "kernel": "kda_prefill_tc_kernel",
+                     "algorithmic_bytes_per_launch": SDECAY_BYTES_PER_TOKEN * T}}
+    del gh
+
     # ---------------- e2e through the public API, host buffers ----------------
     host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
     dbuf = {x: torch.empty_like(inp[x]) for x in host}
@@ -457,6 +479,7 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
             "checkpointed": checkpointed, "gated": gated, "output_gated": output_gated,
+            "scalar_decay": scalar_decay,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -208,6 +208,32 @@ kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const v
                                     void *out, float *final_state, kda_stream_t stream);
 
 /*
+ * kda_prefill_scalar_decay -- the same chunked prefill for the two special
+ * cases of the recurrence the pages build KDA from ("Kimi K3.1 and the Road
+ * From Softmax Attention to Kimi Delta Attention", sections "3. The delta
+ * rule" and "4. Gating"):
+ *
+ *   Gated DeltaNet: S_t = (I - beta_t k_t k_t^T) alpha_t S_{t-1} + beta_t k_t v_t^T
+ *                   with one decay alpha_t = exp(g_head[t,h]) per head and step;
+ *   delta rule:     g_head == NULL, alpha_t = 1.
+ *
+ * A scalar decay is the channel-wise decay with one value repeated over the
+ * key channels, so the result equals kda_prefill with g[t,h,c] = g_head[t,h]
+ * (the kernels form the same running sums from it, and the same output).
+ * The per-channel decay tensor is not read: 4 bytes per (token, head)
+ * replace 4 d_k.
+ *
+ *   g_head  device fp32 [T_tot, H], 4-byte aligned, values in [-5, 0]; or
+ *           NULL (no decay).
+ *
+ * Every other argument, and every other error, is as in kda_prefill.
+ */
+kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g_head, const float *beta,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, kda_stream_t stream);
+
+/*
  * kda_decode -- one single-token update of N independent fixed-size states.
  *
  * For each sequence n and head h: M = Diag(exp g) S, u = beta (v - M^T k),

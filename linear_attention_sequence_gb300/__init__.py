@@ -10,6 +10,7 @@ method and has no fallback: if the library is missing, every call raises.
     kda_prefill_checkpointed(...)       the same, plus state checkpoints every `interval` tokens
     kda_prefill_gated(q, k, v, z, a_log, beta_logit, ...)   the same, from gate logits
     kda_prefill_output_gated(q, k, v, g, beta, gate_logit, ...)   the same, then the output gate
+    kda_prefill_scalar_decay(q, k, v, g_head, beta, ...)   Gated DeltaNet / the delta rule
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ import os
 import torch
 
 __all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
-           "kda_prefill_output_gated", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+           "kda_prefill_output_gated", "kda_prefill_scalar_decay", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -76,6 +77,9 @@ def lib():
         L.kda_prefill_output_gated.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, vp, fp,
                                                ctypes.c_float, fp, vp, vp, fp, vp]
         L.kda_prefill_output_gated.restype = ctypes.c_int
+        L.kda_prefill_scalar_decay.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp,
+                                               fp, vp]
+        L.kda_prefill_scalar_decay.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -245,6 +249,26 @@ def kda_prefill_output_gated(q, k, v, g, beta, gate_logit, norm_weight=None, eps
                                         ctypes.c_float(eps), _ptr(init_state), _ptr(cu_seqlens),
                                         _ptr(out), _ptr(final_state), _stream(stream))
     _check(st, "kda_prefill_output_gated")
+    return out, final_state
+
+
+def kda_prefill_scalar_decay(q, k, v, g_head, beta, init_state=None, cu_seqlens=None, *,
+                             num_seqs=None, out=None, final_state=None, out_dtype=None,
+                             variant=PREFILL_DEFAULT, return_final_state=True, stream=None):
+    """Gated DeltaNet prefill, one log-decay per (token, head): g_head fp32
+    [T, H]; or the delta rule with g_head None (C entry point
+    ``kda_prefill_scalar_decay``).  Returns ``(out, final_state)``."""
+    _require(g_head, "g_head", torch.float32, 2)
+    if g_head is not None and g_head.shape != q.shape[:2]:
+        raise ValueError("g_head must be [T, H]")
+    dims, out, final_state = _prefill_args(q, k, v, None, beta, init_state, cu_seqlens, num_seqs,
+                                           out, final_state, out_dtype, variant,
+                                           return_final_state)
+    st = lib().kda_prefill_scalar_decay(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v),
+                                        _ptr(g_head), _ptr(beta), _ptr(init_state),
+                                        _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                        _stream(stream))
+    _check(st, "kda_prefill_scalar_decay")
     return out, final_state
 
 

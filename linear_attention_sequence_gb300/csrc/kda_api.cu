@@ -88,6 +88,8 @@ struct Extras {
     const void *ogate = nullptr;      // output gate
     const float *onorm_w = nullptr;
     float oeps = 0.f;
+    bool scalar_decay = false;        // one log-decay per (token, head) instead of g
+    const float *g_head = nullptr;    // (nullptr: no decay, the delta rule)
 };
 
 kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, const void *v,
@@ -99,9 +101,11 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     kda::Problem P;
     kda_status st = check_dims(dims, P);
     if (st != KDA_OK) return st;
-    // with the gate prologue, z (decay logits) takes the place of g
+    // with the gate prologue, z (decay logits) takes the place of g; with a
+    // scalar decay there is no per-channel decay tensor at all
     const void *g_in = a_log ? z : (const void *)g;
-    if (P.T > 0 && (!q || !k || !v || !g_in || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.T > 0 && (!q || !k || !v || (!g_in && !x.scalar_decay) || !beta || !out))
+        return KDA_ERR_INVALID_ARGUMENT;
     if (P.T > 0 && a_log && (z == (const void *)out)) return KDA_ERR_INVALID_ARGUMENT;
     if (!cu_seqlens) {
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
@@ -116,6 +120,8 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     }
     P.z = a_log ? z : nullptr;
     P.a_log = a_log;
+    P.scalar_decay = x.scalar_decay;
+    P.g_head = x.scalar_decay ? x.g_head : nullptr;
     P.ckpt = x.ckpt_capacity > 0 ? x.ckpt : nullptr;
     P.ckpt_interval = x.ckpt_interval;
     P.ckpt_capacity = x.ckpt_capacity;
@@ -201,6 +207,18 @@ kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const v
     x.oeps = eps;
     return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, x,
                           stream, "kda_prefill_output_gated");
+}
+
+kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const void *k,
+                                    const void *v, const float *g_head, const float *beta,
+                                    const float *init_state, const int32_t *cu_seqlens,
+                                    void *out, float *final_state, kda_stream_t stream) {
+    if (g_head && ((uintptr_t)g_head & 3u)) return KDA_ERR_INVALID_ARGUMENT;
+    Extras x;
+    x.scalar_decay = true;
+    x.g_head = g_head;
+    return prefill_common(dims, q, k, v, nullptr, beta, init_state, cu_seqlens, out, final_state,
+                          x, stream, "kda_prefill_scalar_decay");
 }
 
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,

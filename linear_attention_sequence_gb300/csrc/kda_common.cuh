@@ -50,6 +50,10 @@ struct Problem {
     const float *onorm_w = nullptr;  // [d_v] or nullptr (weight 1)
     float oeps = 0.f;
     bool ogate_fused = false;        // applied by the tensor-core kernel before its store
+    // scalar decay (kda_prefill_scalar_decay): one log-decay per (token, head)
+    // replaces g; g_head == nullptr means no decay (the delta rule)
+    bool scalar_decay = false;
+    const float *g_head = nullptr;   // fp32 [T, H]
 };
 
 // Gate prologue ("Understanding Kimi K3's Attention", log-decay bound and

@@ -59,7 +59,8 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                         float *__restrict__ final_state, int H, int DV, int64_t total,
                         int64_t seq_len, float *__restrict__ ckpt, int64_t ckpt_every,
                         int64_t ckpt_cap, const IN_T *__restrict__ z,
-                        const float *__restrict__ a_log) {
+                        const float *__restrict__ a_log, int sdecay,
+                        const float *__restrict__ g_head) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<DK, C> &sm = *reinterpret_cast<Smem<DK, C> *>(smem_raw);
 
@@ -91,7 +92,10 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             float gv = 0.f, kv = 0.f, qv = 0.f;
             if (r < L) {
                 const int64_t off = (t0 + r) * rowK + (int64_t)h * DK + c;
-                gv = z ? kda::gate_g(kda::ld_elem(z + off), gscale) : g[off];
+                // the decay: from its logits, one per (token, head), or per channel
+                gv = z        ? kda::gate_g(kda::ld_elem(z + off), gscale)
+                     : sdecay ? (g_head ? g_head[(t0 + r) * H + h] : 0.f)
+                              : g[off];
                 kv = kda::ld_elem(k + off);
                 qv = kda::ld_elem(q + off);
             }
@@ -243,7 +247,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
                                            beta, init_state, cu, (OUT_T *)out, final_state, P.H,
                                            P.dv, (int64_t)P.T, P.seq_len, P.ckpt,
                                            P.ckpt ? P.ckpt_interval / C : 1, P.ckpt_capacity,
-                                           P.a_log ? (const IN_T *)P.z : nullptr, P.a_log);
+                                           P.a_log ? (const IN_T *)P.z : nullptr, P.a_log,
+                                           P.scalar_decay ? 1 : 0, P.g_head);
     return cudaGetLastError();
 }
 

@@ -133,6 +133,7 @@ struct alignas(1024) TcSmem {
     float tsc[3][16][20];       // solve scratch: T11 by rows, T22^T, A21 T11 (rows padded)
     float ored[4][32];          // output gate: per-warp partial sums of o~^2 by row
     float betaS[kBetaRing][C];
+    float ghS[kBetaRing][C];    // one log-decay per token (scalar-decay variants), like beta
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
     uint64_t bar_tma[2], bar_gram[2], bar_bxfull[2], bar_gops[2], bar_akempty[2];
@@ -174,19 +175,24 @@ __device__ __forceinline__ float ld_bf16(const unsigned char *tile, int r, int c
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off_bf16(r, c)));
 }
 
-// With the gate prologue, `mg` maps the bf16 decay logits z (two segments per
-// head, like q) and the box lands in the first half of the g tile.
+// How the decay arrives: 0 = the fp32 log-decay g by TMA; 1 = the bf16 decay
+// logits z by TMA (gate prologue; `mg` maps z, two segments per head like q,
+// and the box lands in the first half of the g tile); 2 = one log-decay per
+// (token, head), fetched with beta (no tile).
+constexpr int kDecayTile = 0, kDecayLogits = 1, kDecayScalar = 2;
 __device__ __forceinline__ void issue_stage_loads(Stage &st, uint64_t *bar, const CUtensorMap *mq,
                                                   const CUtensorMap *mk, const CUtensorMap *mv,
                                                   const CUtensorMap *mg, int h, int64_t t0,
-                                                  bool gated) {
+                                                  int gmode) {
     // one box per tensor: {128-byte segment, C tokens, the head's segments}
-    mbar_arrive_expect_tx(bar, gated ? kStageBytesGated : kStageBytes);
+    mbar_arrive_expect_tx(bar, gmode == kDecayScalar   ? 3 * kTileBf16
+                               : gmode == kDecayLogits ? kStageBytesGated
+                                                       : kStageBytes);
     const int y = (int)t0;
     tma_load_3d(st.q, mq, bar, 0, y, 2 * h);
     tma_load_3d(st.k, mk, bar, 0, y, 2 * h);
     tma_load_3d(st.v, mv, bar, 0, y, 2 * h);
-    tma_load_3d(st.g, mg, bar, 0, y, (gated ? 2 : 4) * h);
+    if (gmode != kDecayScalar) tma_load_3d(st.g, mg, bar, 0, y, (gmode == kDecayLogits ? 2 : 4) * h);
 }
 
 // Bounded wait for a phase.  The first poll is inline; the polling loop (and
@@ -213,28 +219,36 @@ __device__ __forceinline__ bool aborted(TcSmem &sm) {
 // Preparation warps (0-7): the decay prefix and decay-weighted operands of
 // chunk n and its Gram MMA, done while the chain warps run chunk n-1.
 // ---------------------------------------------------------------------------
-template <bool GATED>
+template <bool GATED, bool SDECAY>
 __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                           const CUtensorMap *mv, const CUtensorMap *mg,
-                                          const float *__restrict__ beta, int H, int h, int64_t a,
+                                          const float *__restrict__ beta,
+                                          const float *__restrict__ g_head, int H, int h, int64_t a,
                                           int64_t b, int nchunks, uint32_t tb, float gscale) {
     constexpr bool gated = GATED;
+    constexpr int gmode = GATED ? kDecayLogits : SDECAY ? kDecayScalar : kDecayTile;
     const int P = threadIdx.x;  // 0..255
     const int warp = P >> 5, lane = P & 31, qd = warp & 3, wg = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     uint32_t tma_par[2] = {0, 0}, ake_par[2] = {0, 0}, gram_par[2] = {0, 0};
     const bool beta_thread = P >= 128 && P < 128 + C;
 
-    // beta of chunk 0 (asynchronous 4-byte copies; rows past the end are 0)
+    // beta of chunk 0 (asynchronous 4-byte copies; rows past the end are 0), and
+    // with a scalar decay the log-decay of each token (0 without one: the delta rule)
     if (beta_thread) {
         const int r = P - 128;
-        if (nchunks > 0 && a + r < b) cp_async4(&sm.betaS[0][r], beta + (a + r) * H + h);
+        const bool in_seq = nchunks > 0 && a + r < b;
+        if (in_seq) cp_async4(&sm.betaS[0][r], beta + (a + r) * H + h);
         else sm.betaS[0][r] = 0.f;
+        if (SDECAY) {
+            if (in_seq && g_head) cp_async4(&sm.ghS[0][r], g_head + (a + r) * H + h);
+            else sm.ghS[0][r] = 0.f;
+        }
         cp_async_commit();
     }
     if (P == kTmaIssuer)
         for (int s = 0; s < 2 && s < nchunks; ++s) {
-            issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C, gated);
+            issue_stage_loads(sm.in[s], &sm.bar_tma[s], mq, mk, mv, mg, h, a + (int64_t)s * C, gmode);
             sm.tma_issued[s] = 1;
         }
     __syncwarp();
@@ -263,9 +277,15 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 *bn = kda::sigmoid_f(*bn);
             }
             const int64_t tn = t0 + C + r;
+            const bool in_seq = n + 1 < nchunks && tn < b;
             float *dst = &sm.betaS[(n + 1) % kBetaRing][r];
-            if (n + 1 < nchunks && tn < b) cp_async4(dst, beta + tn * H + h);
+            if (in_seq) cp_async4(dst, beta + tn * H + h);
             else *dst = 0.f;
+            if (SDECAY) {
+                float *gdst = &sm.ghS[(n + 1) % kBetaRing][r];
+                if (in_seq && g_head) cp_async4(gdst, g_head + tn * H + h);
+                else *gdst = 0.f;
+            }
             cp_async_commit();
         }
         if (named_sync_or(BAR_PREP, kPrep, aborted(sm))) break;
@@ -283,6 +303,11 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
                 named_sync(BAR_A1, D);
 #pragma unroll
                 for (int r = 0; r < C; ++r) gv[r] = kda::gate_g(gv[r], gscale);
+            } else if (SDECAY) {
+                // one log-decay per token, the same for every key channel
+                const float *gh = sm.ghS[n % kBetaRing];
+#pragma unroll
+                for (int r = 0; r < C; ++r) gv[r] = gh[r];
             } else {
 #pragma unroll
                 for (int r = 0; r < C; ++r) gv[r] = g[off_f32(r, c) >> 2];
@@ -481,7 +506,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                                            OUT_T *__restrict__ out, int H, int h,
                                            int64_t a, int64_t b, int nchunks, uint32_t tb,
                                            float *__restrict__ ckpt, int64_t ckpt_every,
-                                           int64_t ckpt_cap, int64_t ck_row0, bool gated, float wj,
+                                           int64_t ckpt_cap, int64_t ck_row0, int gmode, float wj,
                                            float oeps) {
     static_assert(!OGATE || sizeof(OUT_T) == 2, "the fused output gate stages a bf16 output");
     const int j = threadIdx.x - kPrep;   // 0..127
@@ -525,7 +550,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                     if (wait_phase(sm, &sm.bar_x, x_par, 16u) && n + 2 < nchunks) {
                         // the stage is free again: refill it with chunk n+2
                         issue_stage_loads(sm.in[st], &sm.bar_tma[st], mq, mk, mv, mg, h, t0 + 2 * C,
-                                          gated);
+                                          gmode);
                         sm.tma_issued[st] += 1;
                     }
                 }
@@ -780,7 +805,7 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
     }
 }
 
-template <typename OUT_T, bool GATED, bool OGATE>
+template <typename OUT_T, bool GATED, bool OGATE, bool SDECAY>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -792,7 +817,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
                       int64_t total, int64_t seq_len, float *__restrict__ ckpt,
                       int64_t ckpt_every, int64_t ckpt_cap, const float *__restrict__ a_log,
-                      const float *__restrict__ onorm_w, float oeps) {
+                      const float *__restrict__ onorm_w, float oeps,
+                      const float *__restrict__ g_head) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Round up to 1024 bytes by pointer arithmetic on the shared array itself
     // (an integer round trip would lose the shared address space and turn
@@ -867,13 +893,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
 
     if (!chain)
-        prep_loop<GATED>(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, H, h, a, b, nchunks, tb,
-                         GATED ? __expf(a_log[h]) : 0.f);
+        prep_loop<GATED, SDECAY>(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, g_head, H, h, a, b, nchunks,
+                                 tb, GATED ? __expf(a_log[h]) : 0.f);
     else
         chain_loop<OUT_T, OGATE>(sm, &tm_q, &tm_k, &tm_v, &tm_g, &tm_o, &tm_og, out, H, h, a, b,
                                  nchunks, tb, ckpt, ckpt_every, ckpt_cap,
                                  ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0,
-                                 GATED, OGATE && onorm_w ? onorm_w[t - kPrep] : 1.f, oeps);
+                                 GATED ? kDecayLogits : SDECAY ? kDecayScalar : kDecayTile,
+                                 OGATE && onorm_w ? onorm_w[t - kPrep] : 1.f, oeps);
 
     tc_fence_before();
     __syncthreads();
@@ -942,20 +969,23 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
-        !(P.a_log ? make_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
-                  : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)) ||
+        !(P.a_log          ? make_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
+          : P.scalar_decay ? make_map(&mg, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)   // unused
+                           : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)) ||
         !(sizeof(OUT_T) == 2 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
                              : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
         return cudaErrorInvalidValue;
     mog = mq;   // not read unless the output gate is fused
-    auto kern = P.a_log ? kda_prefill_tc_kernel<OUT_T, true, false>
-                        : kda_prefill_tc_kernel<OUT_T, false, false>;
+    auto kern = P.a_log          ? kda_prefill_tc_kernel<OUT_T, true, false, false>
+                : P.scalar_decay ? kda_prefill_tc_kernel<OUT_T, false, false, true>
+                                 : kda_prefill_tc_kernel<OUT_T, false, false, false>;
     if constexpr (sizeof(OUT_T) == 2) {
         // the output gate, fused for a bf16 output (with plain g and beta)
         if (P.ogate_fused) {
-            if (P.a_log || !make_map(&mog, P.ogate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H))
+            if (P.a_log || P.scalar_decay ||
+                !make_map(&mog, P.ogate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H))
                 return cudaErrorInvalidValue;
-            kern = kda_prefill_tc_kernel<OUT_T, false, true>;
+            kern = kda_prefill_tc_kernel<OUT_T, false, true, false>;
         }
     }
     const size_t smem = sizeof(TcSmem) + 1024;
@@ -966,7 +996,8 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
     kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, mo, mog, beta, init_state, cu,
                                              (OUT_T *)out, final_state, P.H, (int64_t)P.T,
                                              P.seq_len, P.ckpt, P.ckpt ? P.ckpt_interval / C : 1,
-                                             P.ckpt_capacity, P.a_log, P.onorm_w, P.oeps);
+                                             P.ckpt_capacity, P.a_log, P.onorm_w, P.oeps,
+                                             P.g_head);
     return cudaGetLastError();
 }
 
@@ -976,7 +1007,7 @@ bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *
                               const float *g, const void *out) {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
     return P.dk == 128 && P.dv == 128 && P.in_dtype == KDA_DTYPE_BF16 && P.T > 0 &&
-           P.T <= 0x7fffffff - C && al16(q) && al16(k) && al16(v) && al16(g) && al16(out) &&
+           P.T <= 0x7fffffff - C && al16(q) && al16(k) && al16(v) && (P.scalar_decay || al16(g)) && al16(out) &&
            encode_fn() != nullptr;
 }
 

@@ -157,3 +157,12 @@ def output_gate_inputs(T, H, dv, dtype=torch.float32, seed=0, device="cpu"):
     gate = torch.randn((T, H, dv), generator=gen, device=device, dtype=torch.float32).to(dtype)
     w = 0.5 + torch.rand((dv,), generator=gen, device=device, dtype=torch.float32)
     return dict(gate=gate, norm_weight=w)
+
+
+def scalar_decay(T, H, mu=2.0, seed=0, device="cpu"):
+    """One log-decay per (token, head) for the scalar-decay variant (Gated
+    DeltaNet): g = max(-5, log Sigmoid(x)), x ~ N(mu, 1), the per-channel
+    recipe drawn once per head instead of once per channel (fp32 [T, H])."""
+    gen = _gen(seed, device)
+    x = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32) + mu
+    return torch.clamp(torch.nn.functional.logsigmoid(x), min=-5.0)

@@ -196,6 +196,30 @@ def test_prefill_output_gated_empty_batch_is_ok(L):
                           beta=None, gl=None, out=None) == OK
 
 
+def prefill_sdecay(L, dims, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, gh=ctypes.c_void_p(0x60000), beta=FAKE, init=None,
+                cu=None, out=ctypes.c_void_p(0x20000), fin=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_prefill_scalar_decay(d, args["q"], args["k"], args["v"], args["gh"],
+                                      args["beta"], args["init"], args["cu"], args["out"],
+                                      args["fin"], None)
+
+
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(), {"q": None}), (D(), {"beta": None}),
+    (D(), {"out": None}), (D(), {"gh": ctypes.c_void_p(0x60002)}),   # misaligned decay
+    (D(num_seqs=3, total_tokens=16), {}), (D(), {"out": FAKE}),
+])
+def test_prefill_scalar_decay_rejects(L, dims, over):
+    assert prefill_sdecay(L, dims, **over) == INVALID
+
+
+def test_prefill_scalar_decay_empty_batch_is_ok(L):
+    assert prefill_sdecay(L, D(num_seqs=0, total_tokens=0), q=None, k=None, v=None, gh=None,
+                          beta=None, out=None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

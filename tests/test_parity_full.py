@@ -165,3 +165,21 @@ def test_output_gated_8k_sampled_heads():
     print(f"output-gated prefill_8k (3 heads, bf16 out): err_y {eo:.3e} (bound {bound:.3e}) "
           f"err_S {es:.3e}")
     assert eo <= bound and es <= TOL[torch.bfloat16]
+
+
+def test_scalar_decay_8k_sampled_heads():
+    """The 8K layer as Gated DeltaNet (one decay per head and step), in the
+    launch the benchmark times: three heads against the oracle."""
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, "cuda")
+    gh = synth.scalar_decay(w.total_tokens, w.heads, seed=85, device="cuda")
+    out, fin = kda.kda_prefill_scalar_decay(inp["q"], inp["k"], inp["v"], gh, inp["beta"],
+                                            cu_seqlens=inp["cu_seqlens"], out_dtype=torch.float32)
+    heads = [0, 47, 95]
+    o_ref, s_ref = oracle.prefill_scalar_decay(
+        *(host64(inp[x][:, heads]) for x in ("q", "k", "v")), host64(gh[:, heads]),
+        host64(inp["beta"][:, heads]))
+    eo = rel_err(host64(out[:, heads]), o_ref)
+    es = rel_err(host64(fin[:, heads]), s_ref)
+    print(f"scalar-decay prefill_8k (3 heads): err_o {eo:.3e} err_S {es:.3e}")
+    assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]

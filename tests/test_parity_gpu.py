@@ -446,3 +446,61 @@ def test_output_gate_zero_rows_stay_zero():
     for out_dtype in (torch.float32, torch.bfloat16):
         out, _ = run_output_gated(inp, og, kda.PREFILL_DEFAULT, out_dtype)
         assert torch.count_nonzero(out).item() == 0
+
+
+# ---------------------------------------------------------------------------
+# scalar decay: Gated DeltaNet (one decay per head and step) and the delta rule
+# ---------------------------------------------------------------------------
+
+def run_scalar_decay(inp, g_head, variant, out_dtype=torch.float32, cu=None):
+    try:
+        return kda.kda_prefill_scalar_decay(inp["q"], inp["k"], inp["v"], g_head, inp["beta"],
+                                            init_state=inp.get("init_state"), cu_seqlens=cu,
+                                            out_dtype=out_dtype, variant=variant)
+    except kda.KdaError as e:
+        if e.status == 2:
+            pytest.skip("variant does not take this shape/dtype (KDA_ERR_UNSUPPORTED)")
+        raise
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("decay", ["gated_deltanet", "delta_rule"])
+def test_scalar_decay_matches_oracle(variant, d, dtype, decay):
+    """kda_prefill_scalar_decay on a ragged packed batch against the oracle's
+    scalar-decay recurrence (one decay per head and step, or none)."""
+    if not supported(variant, d, dtype):
+        pytest.skip("variant does not take this shape/dtype")
+    H = 2
+    lens = [1, 31, 32, 0, 65, 100]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=101, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    gh = synth.scalar_decay(T, H, seed=102, device=DEV) if decay == "gated_deltanet" else None
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    out, fin = run_scalar_decay(inp, gh, variant, cu=cu)
+    o_ref, s_ref = oracle.prefill_scalar_decay(host64(inp["q"]), host64(inp["k"]),
+                                               host64(inp["v"]), host64(gh), host64(inp["beta"]),
+                                               init_state=host64(inp["init_state"]),
+                                               cu_seqlens=cu.cpu().numpy())
+    check(out, fin, o_ref, s_ref, dtype)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_scalar_decay_equals_prefill_of_broadcast_decay(variant):
+    """A scalar decay is the channel-wise decay with one value per head: the
+    variant returns exactly (bit for bit) what kda_prefill returns for g
+    repeated over the key channels, and the delta rule what it returns for
+    g = 0.  Full chunks and a ragged tail, nonzero initial state."""
+    T, H, d = 150, 3, 128
+    dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=103, device=DEV, init_std=0.05)
+    gh = synth.scalar_decay(T, H, seed=104, device=DEV)
+    for g_head, g_full in ((gh, gh[:, :, None].expand(T, H, d).contiguous()),
+                           (None, torch.zeros((T, H, d), dtype=torch.float32, device=DEV))):
+        out, fin = run_scalar_decay(inp, g_head, variant)
+        out0, fin0 = kda.kda_prefill(inp["q"], inp["k"], inp["v"], g_full, inp["beta"],
+                                     init_state=inp["init_state"], out_dtype=torch.float32,
+                                     variant=variant)
+        assert torch.equal(out, out0) and torch.equal(fin, fin0)
