@@ -54,6 +54,9 @@ class Oracle:
         lib.kda_oracle_prefill.restype = ctypes.c_int
         lib.kda_oracle_prefill_scalar_decay.argtypes = lib.kda_oracle_prefill.argtypes
         lib.kda_oracle_prefill_scalar_decay.restype = ctypes.c_int
+        lib.kda_oracle_backward.argtypes = [i32, i32, i32, i32, i32] + [dp] * 6 + [
+            ctypes.POINTER(ctypes.c_int32)] + [dp] * 8 + [i32]
+        lib.kda_oracle_backward.restype = ctypes.c_int
         lib.kda_oracle_decode.argtypes = [i32, i32, i32, i32, dp, dp, dp, dp, dp, dp, dp, i32]
         lib.kda_oracle_decode.restype = ctypes.c_int
         lib.kda_oracle_num_cpus.restype = ctypes.c_int
@@ -113,6 +116,30 @@ class Oracle:
         if rc != 0:
             raise ValueError("kda_oracle_prefill_scalar_decay rejected its arguments")
         return out, fin
+
+    def backward(self, q, k, v, g, beta, d_out, d_final_state=None, init_state=None,
+                 cu_seqlens=None, num_seqs=None, num_threads: int = 0):
+        """Gradients of (out, final_state) = prefill(...) for the upstream
+        gradients d_out [T, H, d_v] and d_final_state [N, H, d_k, d_v] (None:
+        zero), in fp64 (C function ``kda_oracle_backward``).  Returns a dict
+        with dq, dk, dv, dg, dbeta and d_init_state."""
+        q, k, v, g, beta, do, dfin, init = (_f64(x) for x in (q, k, v, g, beta, d_out,
+                                                              d_final_state, init_state))
+        T, H, dk = q.shape
+        dv = v.shape[2]
+        cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = (cu.shape[0] - 1) if cu is not None else (1 if num_seqs is None else int(num_seqs))
+        res = dict(dq=np.zeros((T, H, dk)), dk=np.zeros((T, H, dk)), dv=np.zeros((T, H, dv)),
+                   dg=np.zeros((T, H, dk)), dbeta=np.zeros((T, H)),
+                   d_init_state=np.zeros((N, H, dk, dv)))
+        rc = self.lib.kda_oracle_backward(
+            N, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init),
+            _ptr(cu, ctypes.c_int32), _ptr(do), _ptr(dfin), _ptr(res["dq"]), _ptr(res["dk"]),
+            _ptr(res["dv"]), _ptr(res["dg"]), _ptr(res["dbeta"]), _ptr(res["d_init_state"]),
+            int(num_threads))
+        if rc != 0:
+            raise ValueError("kda_oracle_backward rejected its arguments")
+        return res
 
     def gate(self, z, a_log, beta_logit):
         """g [T, H, d_k] and beta [T, H] (fp64) from the decay logits z
@@ -193,6 +220,10 @@ def prefill(*args, **kwargs):
 
 def prefill_scalar_decay(*args, **kwargs):
     return _load().prefill_scalar_decay(*args, **kwargs)
+
+
+def backward(*args, **kwargs):
+    return _load().backward(*args, **kwargs)
 
 
 def gate(*args, **kwargs):

@@ -190,6 +190,194 @@ int kda_oracle_prefill(int32_t num_seqs, int32_t total_tokens, int32_t num_heads
     return rc;
 }
 
+/* Gradients of the recurrence, reverse mode, token by token (the pages'
+ * training path compares the chunked computation's gradients with those of
+ * the simple recurrent version: "Hybrid Attention", section "But isn't a
+ * recurrent update sequential?").  For a loss L with dL/do_t = d_out[t] and
+ * dL/dS_T = d_final_state (NULL => 0), per (sequence, head), the forward
+ * states S_0..S_T are kept; then for t = T..1, with dS = dL/dS_t:
+ *
+ *   dS   += q_t do_t^T,  dq_t = S_t do_t                    (o_t = S_t^T q_t)
+ *   du    = dS^T k_t,    dk_t = dS u_t                      (S_t = M_t + k_t u_t^T)
+ *   dv_t  = beta_t du,   dbeta_t = du . (v_t - p_t),  dp = -beta_t du
+ *   dM    = dS + k_t dp^T,  dk_t += M_t dp                   (p_t = M_t^T k_t)
+ *   dg_t[i] = alpha_t[i] sum_j dM[i][j] S_{t-1}[i][j],  dS <- Diag(alpha_t) dM
+ *                                                            (M_t = Diag(alpha_t) S_{t-1})
+ *
+ * and dL/dS_0 is the dS left after t = 1. */
+typedef struct {
+    int64_t h_count, dk, dv;
+    const double *q, *k, *v, *g, *beta, *init_state, *d_out, *d_final;
+    const int32_t *cu;
+    double *dq, *dkk, *dvv, *dg, *dbeta, *d_init;
+    int64_t n_items, next;
+    pthread_mutex_t lock;
+} oracle_bwd_job;
+
+static int bwd_one(const oracle_bwd_job *J, int64_t n, int64_t h) {
+    const int64_t H = J->h_count, dk = J->dk, dv = J->dv, sz = dk * dv;
+    const int64_t a = J->cu[n], L = J->cu[n + 1] - J->cu[n];
+    double *st = (double *)malloc(sizeof(double) * (size_t)((L + 1) * sz));
+    double *dS = (double *)malloc(sizeof(double) * (size_t)sz);
+    double *dM = (double *)malloc(sizeof(double) * (size_t)sz);
+    double *w = (double *)malloc(sizeof(double) * (size_t)(dk + 4 * dv));
+    if (!st || !dS || !dM || !w) {
+        free(st); free(dS); free(dM); free(w);
+        return -1;
+    }
+    double *al = w, *pp = w + dk, *uu = pp + dv, *du = uu + dv, *dp = du + dv;
+    if (J->init_state) memcpy(st, J->init_state + (n * H + h) * sz, sizeof(double) * sz);
+    else memset(st, 0, sizeof(double) * sz);
+    /* forward, keeping every state */
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t ix = (a + t) * H + h;
+        const double *kt = J->k + ix * dk, *vt = J->v + ix * dv, *gt = J->g + ix * dk;
+        const double *S0 = st + t * sz;
+        double *S1 = st + (t + 1) * sz;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S1[i * dv + j] = exp(gt[i]) * S0[i * dv + j];
+        for (int64_t j = 0; j < dv; ++j) pp[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) pp[j] += S1[i * dv + j] * kt[i];
+        for (int64_t j = 0; j < dv; ++j) uu[j] = J->beta[ix] * (vt[j] - pp[j]);
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) S1[i * dv + j] += kt[i] * uu[j];
+    }
+    /* backward */
+    if (J->d_final) memcpy(dS, J->d_final + (n * H + h) * sz, sizeof(double) * sz);
+    else memset(dS, 0, sizeof(double) * sz);
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t ix = (a + t) * H + h;
+        const double *qt = J->q + ix * dk, *kt = J->k + ix * dk, *vt = J->v + ix * dv;
+        const double *gt = J->g + ix * dk, *dot = J->d_out + ix * dv;
+        const double bt = J->beta[ix];
+        const double *Sp = st + t * sz, *St = st + (t + 1) * sz;
+        double *dqt = J->dq + ix * dk, *dkt = J->dkk + ix * dk, *dgt = J->dg + ix * dk;
+        double *dvt = J->dvv + ix * dv;
+        for (int64_t i = 0; i < dk; ++i) al[i] = exp(gt[i]);
+        /* o_t = S_t^T q_t */
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                dS[i * dv + j] += qt[i] * dot[j];
+                acc += St[i * dv + j] * dot[j];
+            }
+            dqt[i] = acc;
+        }
+        /* recompute p_t and u_t from M_t = Diag(alpha) S_{t-1} */
+        for (int64_t j = 0; j < dv; ++j) pp[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j) pp[j] += al[i] * Sp[i * dv + j] * kt[i];
+        for (int64_t j = 0; j < dv; ++j) uu[j] = bt * (vt[j] - pp[j]);
+        /* S_t = M_t + k u^T */
+        for (int64_t j = 0; j < dv; ++j) du[j] = 0.0;
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                du[j] += dS[i * dv + j] * kt[i];
+                acc += dS[i * dv + j] * uu[j];
+            }
+            dkt[i] = acc;
+        }
+        /* u = beta (v - p) */
+        double db = 0.0;
+        for (int64_t j = 0; j < dv; ++j) {
+            dvt[j] = bt * du[j];
+            db += du[j] * (vt[j] - pp[j]);
+            dp[j] = -bt * du[j];
+        }
+        J->dbeta[ix] = db;
+        /* p = M^T k and M = Diag(alpha) S_{t-1} */
+        for (int64_t i = 0; i < dk; ++i) {
+            double acc = 0.0, ga = 0.0;
+            for (int64_t j = 0; j < dv; ++j) {
+                dM[i * dv + j] = dS[i * dv + j] + kt[i] * dp[j];
+                acc += al[i] * Sp[i * dv + j] * dp[j];
+                ga += dM[i * dv + j] * Sp[i * dv + j];
+            }
+            dkt[i] += acc;
+            dgt[i] = al[i] * ga;
+            for (int64_t j = 0; j < dv; ++j) dS[i * dv + j] = al[i] * dM[i * dv + j];
+        }
+    }
+    memcpy(J->d_init + (n * H + h) * sz, dS, sizeof(double) * sz);
+    free(st); free(dS); free(dM); free(w);
+    return 0;
+}
+
+static void *bwd_worker(void *arg) {
+    oracle_bwd_job *J = (oracle_bwd_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        const int64_t item = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (item >= J->n_items) break;
+        if (bwd_one(J, item / J->h_count, item % J->h_count) != 0) return (void *)1;
+    }
+    return NULL;
+}
+
+int kda_oracle_backward(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t d_k,
+                        int32_t d_v, const double *q, const double *k, const double *v,
+                        const double *g, const double *beta, const double *init_state,
+                        const int32_t *cu_seqlens, const double *d_out,
+                        const double *d_final_state, double *dq, double *dk, double *dv,
+                        double *dg, double *dbeta, double *d_init_state, int32_t num_threads) {
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || d_k <= 0 || d_v <= 0) return -1;
+    if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv ||
+                             !dg || !dbeta))
+        return -1;
+    if (num_seqs > 0 && !d_init_state) return -1;
+    int32_t *cu_local = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        if (num_seqs == 0 ? total_tokens != 0 : total_tokens % num_seqs != 0) return -1;
+        cu_local = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_seqs + 1));
+        if (!cu_local) return -1;
+        const int32_t len = num_seqs ? total_tokens / num_seqs : 0;
+        for (int32_t n = 0; n <= num_seqs; ++n) cu_local[n] = n * len;
+        cu = cu_local;
+    }
+    int rc = 0;
+    if (cu[0] != 0 || cu[num_seqs] != total_tokens) rc = -1;
+    for (int32_t n = 0; n < num_seqs && rc == 0; ++n)
+        if (cu[n + 1] < cu[n]) rc = -1;
+    for (int64_t i = 0; i < (int64_t)total_tokens * num_heads * d_k && rc == 0; ++i)
+        if (!(g[i] >= KDA_ORACLE_G_MIN && g[i] <= 0.0)) rc = -1;
+    for (int64_t i = 0; i < (int64_t)total_tokens * num_heads && rc == 0; ++i)
+        if (!(beta[i] >= 0.0 && beta[i] <= 1.0)) rc = -1;
+    if (rc != 0) {
+        free(cu_local);
+        return rc;
+    }
+    oracle_bwd_job J;
+    J.h_count = num_heads; J.dk = d_k; J.dv = d_v;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta; J.init_state = init_state;
+    J.d_out = d_out; J.d_final = d_final_state; J.cu = cu;
+    J.dq = dq; J.dkk = dk; J.dvv = dv; J.dg = dg; J.dbeta = dbeta; J.d_init = d_init_state;
+    J.n_items = (int64_t)num_seqs * num_heads;
+    J.next = 0;
+    pthread_mutex_init(&J.lock, NULL);
+    int nt = num_threads > 0 ? num_threads : kda_oracle_num_cpus();
+    if (nt > J.n_items) nt = (int)(J.n_items > 0 ? J.n_items : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    int started = 0;
+    if (th)
+        for (int i = 1; i < nt; ++i)
+            if (pthread_create(&th[i], NULL, bwd_worker, &J) == 0) ++started;
+            else break;
+    if (bwd_worker(&J) != NULL) rc = -1;
+    for (int i = 1; i <= started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret != NULL) rc = -1;
+    }
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    free(cu_local);
+    return rc;
+}
+
 /* Gated DeltaNet and the delta rule ("Kimi K3.1 and the Road From Softmax
  * Attention to Kimi Delta Attention", sections "3. The delta rule" and "4.
  * Gating"): S_t = (I - beta_t k_t k_t^T) alpha_t S_{t-1} + beta_t k_t v_t^T

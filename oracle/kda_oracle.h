@@ -36,6 +36,17 @@ int kda_oracle_prefill_scalar_decay(int32_t num_seqs, int32_t total_tokens, int3
                                     const double *init_state, const int32_t *cu_seqlens,
                                     double *out, double *final_state, int32_t num_threads);
 
+/* Gradients of kda_oracle_prefill's outputs and final states, reverse mode:
+ * given d_out [T, H, d_v] and d_final_state [N, H, d_k, d_v] (NULL => 0),
+ * writes dq, dk, dg [T, H, d_k], dv [T, H, d_v], dbeta [T, H] and
+ * d_init_state [N, H, d_k, d_v].  Other arguments as kda_oracle_prefill. */
+int kda_oracle_backward(int32_t num_seqs, int32_t total_tokens, int32_t num_heads, int32_t d_k,
+                        int32_t d_v, const double *q, const double *k, const double *v,
+                        const double *g, const double *beta, const double *init_state,
+                        const int32_t *cu_seqlens, const double *d_out,
+                        const double *d_final_state, double *dq, double *dk, double *dv,
+                        double *dg, double *dbeta, double *d_init_state, int32_t num_threads);
+
 /* One decode step: one token per sequence, state updated in place. */
 int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                       const double *q, const double *k, const double *v,

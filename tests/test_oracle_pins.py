@@ -298,9 +298,73 @@ def pin_scalar_decay_closed_forms(orc, gold):
             assert np.max(np.abs(fin[0, h] - S_ref)) < 1e-12
 
 
+def pin_backward_finite_differences(orc):
+    """Gradients of L = sum(d_out . o) + sum(d_final . S_T), reverse mode,
+    against central finite differences of the (pinned) forward for every
+    entry of q, k, v, g, beta and the initial states; a packed batch with an
+    empty sequence, keys not normalised, gates inside the domain."""
+    T, H, dk, dv = 6, 2, 3, 4
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((T, H, dk))
+    k = 0.6 * rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    g = -rng.uniform(0.2, 2.0, (T, H, dk))
+    beta = rng.uniform(0.2, 0.8, (T, H))
+    cu = np.array([0, 4, 4, 6], np.int32)
+    S0 = rng.standard_normal((3, H, dk, dv))
+    do = rng.standard_normal((T, H, dv))
+    dfin = rng.standard_normal((3, H, dk, dv))
+    args = dict(q=q, k=k, v=v, g=g, beta=beta, S0=S0)
+
+    def loss(a):
+        o, f = orc.prefill(a["q"], a["k"], a["v"], a["g"], a["beta"], init_state=a["S0"],
+                           cu_seqlens=cu, num_threads=1)
+        return float((o * do).sum() + (f * dfin).sum())
+
+    r = orc.backward(q, k, v, g, beta, do, dfin, init_state=S0, cu_seqlens=cu)
+    eps = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("S0", "d_init_state")):
+        fd = np.zeros_like(args[name])
+        for idx in np.ndindex(fd.shape):
+            a = dict(args)
+            x = args[name].copy(); x[idx] += eps; a[name] = x; lp = loss(a)
+            x = args[name].copy(); x[idx] -= eps; a[name] = x; lm = loss(a)
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert np.max(np.abs(r[key] - fd)) <= 1e-7 * max(1.0, np.max(np.abs(fd))), name
+
+
+def pin_backward_beta_zero_closed_form(orc):
+    """beta = 0 writes nothing: o_t = (Diag(e^{Gamma_t}) S_0)^T q_t and
+    S_T = Diag(e^{Gamma_T}) S_0, so dq_t = Diag(e^{Gamma_t}) S_0 do_t, dk = dv = 0,
+    dS_0 = sum_t Diag(e^{Gamma_t}) q_t do_t^T + Diag(e^{Gamma_T}) dS_T, and
+    dg_t[i] = sum over s >= t of e^{Gamma_s[i]} q_s[i] (S_0 do_s)[i] plus the
+    final-state term e^{Gamma_T[i]} (S_0 . dS_T summed over values)[i]."""
+    T, H, dk, dv = 7, 2, 4, 3
+    q, k, v, g, beta = _rand_case(RNG, T, H, dk, dv)
+    beta[:] = 0.0
+    S0 = RNG.standard_normal((1, H, dk, dv))
+    do = RNG.standard_normal((T, H, dv))
+    dfin = RNG.standard_normal((1, H, dk, dv))
+    r = orc.backward(q, k, v, g, beta, do, dfin, init_state=S0)
+    Gam = np.cumsum(g, axis=0)
+    for h in range(H):
+        E = np.exp(Gam[:, h])                            # [T, dk]
+        S0h, dfh = S0[0, h], dfin[0, h]
+        dq = E * (do[:, h] @ S0h.T)
+        assert np.allclose(r["dq"][:, h], dq, atol=1e-12, rtol=1e-12)
+        dS0 = (E * q[:, h]).T @ do[:, h] + E[-1][:, None] * dfh
+        assert np.allclose(r["d_init_state"][0, h], dS0, atol=1e-12, rtol=1e-12)
+        per_s = E * q[:, h] * (do[:, h] @ S0h.T)         # [T, dk]: term of o_s
+        dg = np.cumsum(per_s[::-1], axis=0)[::-1] + E[-1] * (S0h * dfh).sum(axis=1)
+        assert np.allclose(r["dg"][:, h], dg, atol=1e-12, rtol=1e-12)
+    assert np.all(r["dk"] == 0.0) and np.all(r["dv"] == 0.0)
+
+
 PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
         pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound,
-        pin_gate_closed_forms, pin_output_gate_closed_forms, pin_scalar_decay_closed_forms]
+        pin_gate_closed_forms, pin_output_gate_closed_forms, pin_scalar_decay_closed_forms,
+        pin_backward_finite_differences, pin_backward_beta_zero_closed_form]
 
 
 def _run_pin(pin, orc, golden):
@@ -416,6 +480,12 @@ MUTANTS = {
     "scalar_decay_ignored": ("g_head ? g_head[t * num_heads + h] : 0.0;", "0.0;"),
     "scalar_decay_one_head": ("g_head ? g_head[t * num_heads + h] : 0.0;",
                               "g_head ? g_head[t * num_heads] : 0.0;"),
+    "bwd_no_prediction_term": ("            dkt[i] += acc;", "            dkt[i] += 0.0 * acc;"),
+    "bwd_no_decay": ("for (int64_t j = 0; j < dv; ++j) dS[i * dv + j] = al[i] * dM[i * dv + j];",
+                     "for (int64_t j = 0; j < dv; ++j) dS[i * dv + j] = dM[i * dv + j];"),
+    "bwd_dbeta_sign": ("db += du[j] * (vt[j] - pp[j]);", "db += du[j] * (vt[j] + pp[j]);"),
+    "bwd_dg_no_alpha": ("dgt[i] = al[i] * ga;", "dgt[i] = ga;"),
+    "bwd_read_before_write": ("acc += St[i * dv + j] * dot[j];", "acc += Sp[i * dv + j] * dot[j];"),
     "ogate_sum_not_mean": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
                            "const double rinv = 1.0 / sqrt(ss + eps);"),
     "ogate_eps_outside_root": ("const double rinv = 1.0 / sqrt(ss / d_v + eps);",
