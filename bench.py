@@ -42,6 +42,18 @@ GATED_BYTES_PER_TOKEN = 5 * 96 * 128 * 2 + 96 * 4  # 123264
 OGATED_BYTES_PER_TOKEN = 147840 + 96 * 128 * 2  # 172416
 # the scalar-decay call (Gated DeltaNet) reads one fp32 log-decay per (token, head) instead of g
 SDECAY_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 2 * 96 * 4  # 99072
+# backward: algorithmic fp32 flops per (chunk, head) of the chunked backward (C = 32,
+# d = 128), counted as 2 per multiply-add over the products it forms:
+#   G, P (pairwise, C(C+1)/2 pairs x 2 d)      135,168 MACs
+#   Y = V - Kt S0, dU's Kb dS, dQt, dKt, dKb, the two products of dS0   7 C d^2
+#   P^T dO, T B, T^T dU, dP, dT (triangular, C^2 d / 2 each)            5/2 C^2 d
+#   dA = -T^T dT T^T (2 C^3 / 3), the pairwise gradient terms (3 C^2 d)
+BWD_C, BWD_D = 32, 128
+BWD_MACS_PER_CHUNK_HEAD = (BWD_C * (BWD_C + 1) // 2 * 2 * BWD_D + 7 * BWD_C * BWD_D * BWD_D
+                           + 5 * BWD_C * BWD_C * BWD_D // 2 + 2 * BWD_C ** 3 // 3
+                           + 3 * BWD_C * BWD_C * BWD_D)
+# fp32 CUDA-core peak of the part: 152 SMs x 128 fp32 lanes x 2 flops per FMA x SM clock
+FP32_LANES = 152 * 128
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -405,6 +417,35 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": SDECAY_BYTES_PER_TOKEN * T}}
     del gh
 
+    # ---------------- the backward pass (gradients of the same layer) ----------------
+    gen = torch.Generator(device=dev).manual_seed(87)
+    d_out = torch.randn((T, w.heads, w.d), generator=gen, device=dev).to(w.dtype)
+    _, _, cstates = kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"],
+                                                 inp["beta"], cu_seqlens=inp["cu_seqlens"],
+                                                 interval=kda.CHUNK, stream=stream)
+
+    def backward_step():
+        kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                         cu_seqlens=inp["cu_seqlens"], chunk_states=cstates, stream=stream)
+
+    bw_steps = 3
+    ms_bw, _, _ = time_steps(backward_step, bw_steps, 2, world, stream)
+    bw_flops = 2.0 * BWD_MACS_PER_CHUNK_HEAD * ((T + BWD_C - 1) // BWD_C) * w.heads
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    fp32_peak = FP32_LANES * 2 * sm_mhz * 1e6 / 1e12
+    bw_ach = bw_flops / (ms_bw * 1e-3) / 1e12
+    backward = {
+        "value": T * world / (ms_bw * 1e-3), "unit": UNIT, "ms_per_step": ms_bw,
+        "steps": bw_steps,
+        "config": {"workload": "prefill_8k inputs, upstream gradient of out ~ N(0, 1) (bf16), "
+                               "chunk states from kda_prefill_checkpointed (interval 32); "
+                               "fp32 gradients of q, k, v, g, beta"},
+        "roofline": {"bound": "alu", "achieved": bw_ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                     "frac": bw_ach / fp32_peak,
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x sampled SM clock",
+                     "kernel": "kda_backward_kernel", "algorithmic_flops_per_launch": bw_flops}}
+    del cstates, d_out
+
     # ---------------- e2e through the public API, host buffers ----------------
     host = {x: inp[x].cpu().pin_memory() for x in ("q", "k", "v", "g", "beta")}
     dbuf = {x: torch.empty_like(inp[x]) for x in host}
@@ -479,7 +520,7 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
             "checkpointed": checkpointed, "gated": gated, "output_gated": output_gated,
-            "scalar_decay": scalar_decay,
+            "scalar_decay": scalar_decay, "backward": backward,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

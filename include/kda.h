@@ -234,6 +234,41 @@ kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const v
                                     void *out, float *final_state, kda_stream_t stream);
 
 /*
+ * kda_backward -- gradients of kda_prefill.  Given the upstream gradients
+ * d_out = dL/d out and d_final_state = dL/d final_state (NULL => 0), writes
+ * dL/dq, dL/dk, dL/dv, dL/dg, dL/dbeta and dL/d init_state for the same packed
+ * batch.  The pages train the chunked computation and check its gradients
+ * against the recurrent version ("Hybrid Attention", section "But isn't a
+ * recurrent update sequential?"); this call computes them chunk by chunk,
+ * walking each sequence's chunks in reverse and carrying the adjoint of the
+ * state, from the forward's state at the start of every chunk.
+ *
+ *   chunk_states   device fp32 [chunk_capacity, H, d_k, d_v]: the checkpoints
+ *                  kda_prefill_checkpointed writes with interval = KDA_CHUNK
+ *                  for the same inputs (row layout as there).  It may be NULL
+ *                  only if T_tot <= KDA_CHUNK (then no sequence has a second
+ *                  chunk).  Rows at or past chunk_capacity are treated as zero
+ *                  states, never read.
+ *   d_out          device, in_dtype, [T_tot, H, d_v].
+ *   d_final_state  device fp32 [N, H, d_k, d_v] or NULL.
+ *   dq, dk, dv     device, out_dtype: [T_tot, H, d_k], [T_tot, H, d_k], [T_tot, H, d_v].
+ *   dg             device fp32 [T_tot, H, d_k];  dbeta  device fp32 [T_tot, H].
+ *   d_init_state   device fp32 [N, H, d_k, d_v] or NULL (not written).
+ *
+ * The gradients must not alias any input.  Arithmetic is fp32 on CUDA cores.
+ * Every other argument (q, k, v, g, beta, init_state, cu_seqlens, dims) and
+ * every other error is as in kda_prefill; KDA_ERR_INVALID_ARGUMENT also if
+ * chunk_capacity < 0, chunk_states is NULL or misaligned where it is needed,
+ * or a gradient pointer equals an input pointer.
+ */
+kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, const float *init_state,
+                        const int32_t *cu_seqlens, const float *chunk_states,
+                        int64_t chunk_capacity, const void *d_out, const float *d_final_state,
+                        void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                        float *d_init_state, kda_stream_t stream);
+
+/*
  * kda_decode -- one single-token update of N independent fixed-size states.
  *
  * For each sequence n and head h: M = Diag(exp g) S, u = beta (v - M^T k),

@@ -11,6 +11,7 @@ method and has no fallback: if the library is missing, every call raises.
     kda_prefill_gated(q, k, v, z, a_log, beta_logit, ...)   the same, from gate logits
     kda_prefill_output_gated(q, k, v, g, beta, gate_logit, ...)   the same, then the output gate
     kda_prefill_scalar_decay(q, k, v, g_head, beta, ...)   Gated DeltaNet / the delta rule
+    kda_backward(q, k, v, g, beta, d_out, ...)   gradients of kda_prefill
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -21,7 +22,7 @@ import os
 import torch
 
 __all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
-           "kda_prefill_output_gated", "kda_prefill_scalar_decay", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+           "kda_prefill_output_gated", "kda_prefill_scalar_decay", "kda_backward", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -80,6 +81,9 @@ def lib():
         L.kda_prefill_scalar_decay.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp,
                                                fp, vp]
         L.kda_prefill_scalar_decay.restype = ctypes.c_int
+        L.kda_backward.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, fp,
+                                   ctypes.c_int64, vp, fp, vp, vp, vp, fp, fp, fp, vp]
+        L.kda_backward.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -270,6 +274,54 @@ def kda_prefill_scalar_decay(q, k, v, g_head, beta, init_state=None, cu_seqlens=
                                         _stream(stream))
     _check(st, "kda_prefill_scalar_decay")
     return out, final_state
+
+
+def kda_backward(q, k, v, g, beta, d_out, d_final_state=None, init_state=None, cu_seqlens=None,
+                 *, chunk_states=None, num_seqs=None, grad_dtype=None, stream=None):
+    """Gradients of kda_prefill (C entry point ``kda_backward``) for the
+    upstream gradients d_out [T, H, d_v] (dtype of q) and d_final_state
+    [N, H, d_k, d_v] fp32 (None: zero).  ``chunk_states`` are the forward's
+    states at every chunk start, as kda_prefill_checkpointed writes them with
+    interval CHUNK; when None they are computed here by that call.  Returns a
+    dict with dq, dk, dv (``grad_dtype``, default the dtype of q), dg, dbeta
+    and d_init_state (fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_out, "d_out")):
+        _require(t, n, q.dtype, 3)
+    _require(g, "g", torch.float32, 3)
+    _require(beta, "beta", torch.float32, 2)
+    _require(init_state, "init_state", torch.float32, 4)
+    _require(d_final_state, "d_final_state", torch.float32, 4)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if q.dtype not in _DTYPES:
+        raise ValueError("q, k, v must be fp32 or bf16")
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if d_out.shape != v.shape:
+        raise ValueError("d_out must have the shape of v")
+    N = cu_seqlens.shape[0] - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    if chunk_states is None:
+        _, _, chunk_states = kda_prefill_checkpointed(q, k, v, g, beta, init_state, cu_seqlens,
+                                                      interval=CHUNK, num_seqs=N,
+                                                      return_final_state=False, stream=stream)
+    _require(chunk_states, "chunk_states", torch.float32, 4)
+    grad_dtype = grad_dtype or q.dtype
+    dev = q.device
+    res = dict(dq=torch.empty((T, H, dk), dtype=grad_dtype, device=dev),
+               dk=torch.empty((T, H, dk), dtype=grad_dtype, device=dev),
+               dv=torch.empty((T, H, dv), dtype=grad_dtype, device=dev),
+               dg=torch.empty((T, H, dk), dtype=torch.float32, device=dev),
+               dbeta=torch.empty((T, H), dtype=torch.float32, device=dev),
+               d_init_state=torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev))
+    dims = Dims(N, T, H, dk, dv, _DTYPES[q.dtype], _DTYPES[grad_dtype], 0)
+    cs = chunk_states if chunk_states.numel() else None
+    st = lib().kda_backward(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                            _ptr(init_state), _ptr(cu_seqlens), _ptr(cs),
+                            int(chunk_states.shape[0]) if cs is not None else 0, _ptr(d_out),
+                            _ptr(d_final_state), _ptr(res["dq"]), _ptr(res["dk"]),
+                            _ptr(res["dv"]), _ptr(res["dg"]), _ptr(res["dbeta"]),
+                            _ptr(res["d_init_state"]), _stream(stream))
+    _check(st, "kda_backward")
+    return res
 
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,

@@ -221,6 +221,39 @@ kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const v
                           x, stream, "kda_prefill_scalar_decay");
 }
 
+kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, const float *init_state,
+                        const int32_t *cu_seqlens, const float *chunk_states,
+                        int64_t chunk_capacity, const void *d_out, const float *d_final_state,
+                        void *dq, void *dk, void *dv, float *dg, float *dbeta,
+                        float *d_init_state, kda_stream_t stream) {
+    kda::Problem P;
+    kda_status st = check_dims(dims, P);
+    if (st != KDA_OK) return st;
+    if (chunk_capacity < 0 || (chunk_capacity > 0 && !chunk_states)) return KDA_ERR_INVALID_ARGUMENT;
+    if (chunk_states && ((uintptr_t)chunk_states & 3u)) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.T > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta))
+        return KDA_ERR_INVALID_ARGUMENT;
+    // a sequence longer than one chunk needs the forward's state at its chunk starts
+    if (P.T > KDA_CHUNK && !chunk_states) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens) {
+        if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
+        P.seq_len = P.N ? P.T / P.N : 0;
+    }
+    // the gradients must not overwrite what the kernel still reads
+    const void *ins[] = {q, k, v, g, beta, d_out, chunk_states, init_state, d_final_state};
+    const void *outs[] = {dq, dk, dv, dg, dbeta};
+    for (const void *o : outs)
+        for (const void *i : ins)
+            if (P.T > 0 && o && o == i) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.N == 0) return KDA_OK;
+    cudaError_t e = kda_launch_backward(P, q, k, v, g, beta, init_state, cu_seqlens, chunk_states,
+                                        chunk_capacity, d_out, d_final_state, dq, dk, dv, dg,
+                                        dbeta, d_init_state, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_backward");
+    return KDA_OK;
+}
+
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,
                       const float *g, const float *beta, float *state_inout, void *out,
                       kda_stream_t stream) {

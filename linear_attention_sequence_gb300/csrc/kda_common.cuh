@@ -91,6 +91,13 @@ cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const vo
                                   const float *init_state, const int32_t *cu, void *out,
                                   float *final_state, cudaStream_t stream);
 cudaError_t kda_launch_output_gate(const kda::Problem &P, void *out, cudaStream_t stream);
+cudaError_t kda_launch_backward(const kda::Problem &P, const void *q, const void *k,
+                                const void *v, const float *g, const float *beta,
+                                const float *init_state, const int32_t *cu,
+                                const float *chunk_states, int64_t chunk_capacity,
+                                const void *d_out, const float *d_final, void *dq, void *dk,
+                                void *dv, float *dg, float *dbeta, float *d_init,
+                                cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
 cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,

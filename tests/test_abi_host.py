@@ -220,6 +220,39 @@ def test_prefill_scalar_decay_empty_batch_is_ok(L):
                           beta=None, out=None) == OK
 
 
+def backward(L, dims, cap=4, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, init=None, cu=None,
+                cs=ctypes.c_void_p(0x90000), do=ctypes.c_void_p(0x98000), dfin=None,
+                dq=ctypes.c_void_p(0xa0000), dk=ctypes.c_void_p(0xa8000),
+                dv=ctypes.c_void_p(0xb0000), dg=ctypes.c_void_p(0xb8000),
+                db=ctypes.c_void_p(0xc0000), dinit=None)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_backward(d, args["q"], args["k"], args["v"], args["g"], args["beta"],
+                          args["init"], args["cu"], args["cs"], cap, args["do"], args["dfin"],
+                          args["dq"], args["dk"], args["dv"], args["dg"], args["db"],
+                          args["dinit"], None)
+
+
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(d_k=96, d_v=96), {}), (D(), {"q": None}),
+    (D(), {"do": None}), (D(), {"dg": None}), (D(), {"db": None}), (D(), {"dq": None}),
+    (D(), {"cap": -1}), (D(total_tokens=64), {"cs": None, "cap": 0}),   # needs chunk states
+    (D(), {"cs": ctypes.c_void_p(0x90002)}),                          # misaligned
+    (D(), {"dq": FAKE}), (D(), {"dk": ctypes.c_void_p(0x98000)}),     # gradient aliases an input
+    (D(num_seqs=3, total_tokens=16), {}),
+])
+def test_backward_rejects(L, dims, over):
+    want = UNSUPPORTED if dims is not None and dims.d_k == 96 else INVALID
+    assert backward(L, dims, **over) == want
+
+
+def test_backward_empty_batch_is_ok(L):
+    assert backward(L, D(num_seqs=0, total_tokens=0), cap=0, cs=None, q=None, k=None, v=None,
+                    g=None, beta=None, do=None, dq=None, dk=None, dv=None, dg=None,
+                    db=None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

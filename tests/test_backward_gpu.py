@@ -1,0 +1,107 @@
+"""GPU parity of kda_backward (the gradients of the chunked prefill) with the
+oracle's reverse mode through the token recurrence."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_sequence_gb300 as kda
+from linear_attention_sequence_gb300 import synth
+import oracle
+from kda_testutil import TOL, rel_err, host64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "d_init_state")
+
+
+def _upstream(T, H, N, d, dtype, seed):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    d_out = torch.randn((T, H, d), generator=gen, device=DEV).to(dtype)
+    d_fin = 0.5 * torch.randn((N, H, d, d), generator=gen, device=DEV)
+    return d_out, d_fin
+
+
+def _oracle_grads(inp, d_out, d_fin, cu, heads=None):
+    sel = (lambda x: x) if heads is None else (lambda x: x[:, heads])
+    return oracle.backward(*(host64(sel(inp[x])) for x in ("q", "k", "v", "g", "beta")),
+                           host64(sel(d_out)),
+                           None if d_fin is None else host64(d_fin if heads is None else d_fin[:, heads]),
+                           init_state=None if inp.get("init_state") is None else
+                           host64(inp["init_state"] if heads is None else inp["init_state"][:, heads]),
+                           cu_seqlens=None if cu is None else cu.cpu().numpy())
+
+
+def _check(res, ref, tol, heads=None):
+    errs = {}
+    for name in GRADS:
+        x = host64(res[name])
+        if heads is not None:
+            x = x[:, heads]
+        errs[name] = rel_err(x, ref[name])
+    bad = {k: v for k, v in errs.items() if v > tol}
+    assert not bad, f"gradient errors above {tol}: {bad} (all: {errs})"
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_backward_matches_oracle(d, dtype):
+    """A ragged packed batch (one token, chunk-1, chunk, chunk+1, empty, multi-
+    chunk) with initial states and final-state gradients; the chunk states come
+    from kda_prefill_checkpointed with interval CHUNK (tensor cores for bf16,
+    d = 128)."""
+    H = 2
+    lens = [1, 31, 32, 33, 0, 65, 100]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=111, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    d_out, d_fin = _upstream(T, H, len(lens), d, dtype, 112)
+    res = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                           init_state=inp["init_state"], cu_seqlens=cu, grad_dtype=torch.float32)
+    ref = _oracle_grads(inp, d_out, d_fin, cu)
+    errs = _check(res, ref, TOL[dtype])
+    print(f"backward d={d} {dtype}: " + " ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+
+
+def test_backward_bf16_grads_are_rne_of_fp32():
+    T, H, d = 100, 2, 128
+    inp = synth.random_inputs(T, H, d, dtype=torch.bfloat16, seed=113, device=DEV)
+    d_out, d_fin = _upstream(T, H, 1, d, torch.bfloat16, 114)
+    a = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                         grad_dtype=torch.float32)
+    b = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                         grad_dtype=torch.bfloat16)
+    for name in ("dq", "dk", "dv"):
+        assert torch.equal(b[name], a[name].to(torch.bfloat16)), name
+    for name in ("dg", "dbeta", "d_init_state"):
+        assert torch.equal(b[name], a[name]), name
+
+
+def test_backward_single_chunks_need_no_states():
+    """Sequences of at most one chunk: no chunk states, no d_final; the
+    gradients still match the oracle."""
+    H, d = 3, 64
+    lens = [5, 20, 7]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=torch.float32, seed=115, device=DEV)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    d_out, _ = _upstream(T, H, len(lens), d, torch.float32, 116)
+    res = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                           cu_seqlens=cu, chunk_states=torch.empty((0, H, d, d), device=DEV))
+    ref = _oracle_grads(inp, d_out, None, cu)
+    _check(res, ref, TOL[torch.float32])
+
+
+def test_backward_layer_1k_sampled_heads():
+    """The 96-head layer over 1024 tokens (bf16, tensor-core forward states),
+    in one launch; three heads against the oracle."""
+    T, H, d = 1024, 96, 128
+    inp = synth.random_inputs(T, H, d, dtype=torch.bfloat16, seed=117, device=DEV)
+    d_out, d_fin = _upstream(T, H, 1, d, torch.bfloat16, 118)
+    res = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                           grad_dtype=torch.float32)
+    heads = [0, 47, 95]
+    ref = _oracle_grads(inp, d_out, d_fin, None, heads=heads)
+    errs = _check(res, ref, TOL[torch.bfloat16], heads=heads)
+    print("backward 1k layer (3 heads): " + " ".join(f"{k} {v:.2e}" for k, v in errs.items()))
