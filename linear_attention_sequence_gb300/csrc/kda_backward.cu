@@ -45,7 +45,10 @@ struct BwdSmem {
     float Q[C][D], K[C][D];    // q, k of the chunk (rows past its end are 0)
     float Gam[C][D];           // Gamma
     float Qt[C][D], Kt[C][D], Kb[C][D];   // q.gamma, k.gamma, k.gamma_last/gamma
-    float V[C][BV + 1], dO[C][BV + 1], Y[C][BV + 1], U[C][BV + 1], dU[C][BV + 1];
+    // rows of 36 floats (16-byte aligned: read four columns at a time); Y keeps 33
+    // (read down its columns)
+    float V[C][BV + 4], dO[C][BV + 4], U[C][BV + 4], dU[C][BV + 4];
+    float Y[C][BV + 1];
     float G[C][C + 1], P[C][C + 1], T[C][C + 1], dP[C][C + 1], dT[C][C + 1];
     float beta[C], dbeta[C];
     float gC[D], gsum[D];      // gamma_last; sum_j dS . S0 by row (the gamma_last term)
@@ -134,29 +137,52 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             sm.Kt[r][c] = sm.K[r][c] * e;
             sm.Kb[r][c] = sm.K[r][c] * eb;
         }
-        // ---- G (strict) and P (inclusive): one warp per (r, i) pair ----
-        for (int p = warp; p < C * C; p += kWarps) {
-            const int r = p / C, i = p % C;
-            float gg = 0.f, pp = 0.f;
-            if (i <= r) {
-                for (int c = lane; c < D; c += 32) {
-                    const float e = __expf(sm.Gam[r][c] - sm.Gam[i][c]);
-                    const float ke = sm.K[i][c] * e;
-                    gg += sm.K[r][c] * ke;
-                    pp += sm.Q[r][c] * ke;
+        // ---- G (strict) and P (inclusive) over the lower triangle: each warp takes
+        // four (r, i) pairs at a time, lanes over channels, so that the four
+        // reductions overlap; the upper triangle is zero ----
+        for (int idx = t; idx < C * C; idx += kThreads) {
+            const int r = idx / C, i = idx % C;
+            if (i > r) sm.G[r][i] = sm.P[r][i] = sm.dP[r][i] = sm.dT[r][i] = 0.f;
+        }
+        constexpr int NPAIR = C * (C + 1) / 2;
+        for (int p0 = 4 * warp; p0 < NPAIR; p0 += 4 * kWarps) {
+            int rr[4], ii[4];
+            float gg[4], pp[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = p0 + u < NPAIR ? p0 + u : NPAIR - 1;
+                int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+                while (r * (r + 1) / 2 > p) --r;
+                while ((r + 1) * (r + 2) / 2 <= p) ++r;
+                rr[u] = r;
+                ii[u] = p - r * (r + 1) / 2;
+                gg[u] = pp[u] = 0.f;
+            }
+            for (int c = lane; c < D; c += 32) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float e = __expf(sm.Gam[rr[u]][c] - sm.Gam[ii[u]][c]);
+                    const float ke = sm.K[ii[u]][c] * e;
+                    gg[u] += sm.K[rr[u]][c] * ke;
+                    pp[u] += sm.Q[rr[u]][c] * ke;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    gg[u] += __shfl_xor_sync(0xffffffffu, gg[u], o);
+                    pp[u] += __shfl_xor_sync(0xffffffffu, pp[u], o);
                 }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    gg += __shfl_xor_sync(0xffffffffu, gg, o);
-                    pp += __shfl_xor_sync(0xffffffffu, pp, o);
+            for (int u = 0; u < 4; ++u)
+                if (lane == u && p0 + u < NPAIR) {
+                    const int r = rr[u], i = ii[u];
+                    sm.G[r][i] = i < r ? gg[u] : 0.f;
+                    sm.P[r][i] = pp[u];
+                    sm.dP[r][i] = 0.f;
+                    sm.dT[r][i] = 0.f;
                 }
-            }
-            if (lane == 0) {
-                sm.G[r][i] = i < r ? gg : 0.f;
-                sm.P[r][i] = pp;   // 0 above the diagonal
-                sm.dP[r][i] = 0.f;
-                sm.dT[r][i] = 0.f;
-            }
         }
         __syncthreads();
         // ---- T = (I + diag(beta) G)^{-1}: lane j solves column j (warp 0) ----
@@ -193,18 +219,47 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 sm.dO[r][j] = r < L ? kda::ld_elem(d_out + off) : 0.f;
             }
             __syncthreads();
-            // ---- Y = V - Kt S0 and dU = Kb dS + P^T dO (thread: column lane, rows warp, warp + 16) ----
+            // ---- Y = V - Kt S0 (threads 0-255) and dU = Kb dS + P^T dO (threads 256-511),
+            // each thread a tile of 2 rows x 2 columns ----
+            {
+                const bool du_half = t >= kThreads / 2;   // warp-uniform
+                const int th = t & (kThreads / 2 - 1);
+                const int jp = (th & 15) * 2, r2 = (th >> 4) * 2;
+                const float(*A)[D] = du_half ? sm.Kb : sm.Kt;
+                float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+                for (int c = 0; c < D; c += 4) {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(&A[r2][c]);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(&A[r2 + 1][c]);
+                    float b0[4], b1[4];
 #pragma unroll
-            for (int rr = 0; rr < C; rr += kWarps) {
-                const int r = rr + warp, j = lane;
-                float y = sm.V[r][j], du = 0.f;
-                for (int c = 0; c < D; ++c) {
-                    y -= sm.Kt[r][c] * sm.S0[c][j];
-                    du += sm.Kb[r][c] * sm.dS[c][j0 + j];
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        b0[q2] = du_half ? sm.dS[c + q2][j0 + jp] : sm.S0[c + q2][jp];
+                        b1[q2] = du_half ? sm.dS[c + q2][j0 + jp + 1] : sm.S0[c + q2][jp + 1];
+                    }
+                    a00 += x0.x * b0[0] + x0.y * b0[1] + x0.z * b0[2] + x0.w * b0[3];
+                    a01 += x0.x * b1[0] + x0.y * b1[1] + x0.z * b1[2] + x0.w * b1[3];
+                    a10 += x1.x * b0[0] + x1.y * b0[1] + x1.z * b0[2] + x1.w * b0[3];
+                    a11 += x1.x * b1[0] + x1.y * b1[1] + x1.z * b1[2] + x1.w * b1[3];
                 }
-                for (int r2 = r; r2 < C; ++r2) du += sm.P[r2][r] * sm.dO[r2][j];
-                sm.Y[r][j] = y;
-                sm.dU[r][j] = du;
+                if (!du_half) {
+                    sm.Y[r2][jp] = sm.V[r2][jp] - a00;
+                    sm.Y[r2][jp + 1] = sm.V[r2][jp + 1] - a01;
+                    sm.Y[r2 + 1][jp] = sm.V[r2 + 1][jp] - a10;
+                    sm.Y[r2 + 1][jp + 1] = sm.V[r2 + 1][jp + 1] - a11;
+                } else {
+                    for (int rp = r2; rp < C; ++rp) {   // P^T dO (P[rp][r] is 0 for rp < r)
+                        const float p0v = sm.P[rp][r2], p1v = sm.P[rp][r2 + 1];
+                        const float o0 = sm.dO[rp][jp], o1 = sm.dO[rp][jp + 1];
+                        a00 += p0v * o0;
+                        a01 += p0v * o1;
+                        a10 += p1v * o0;
+                        a11 += p1v * o1;
+                    }
+                    sm.dU[r2][jp] = a00;
+                    sm.dU[r2][jp + 1] = a01;
+                    sm.dU[r2 + 1][jp] = a10;
+                    sm.dU[r2 + 1][jp + 1] = a11;
+                }
             }
             __syncthreads();
             // ---- U = T diag(beta) Y; dB = T^T dU (in place of dU after the reads below) ----
@@ -224,9 +279,13 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             for (int x = 0; x < C / kWarps; ++x) {
                 const int r = x * kWarps + warp, i = lane;
                 float sp = 0.f, st = 0.f;
-                for (int j = 0; j < BV; ++j) {
-                    sp += sm.dO[r][j] * sm.U[i][j];
-                    st += sm.dU[r][j] * sm.Y[i][j];
+                for (int j = 0; j < BV; j += 4) {
+                    const float4 o4 = *reinterpret_cast<const float4 *>(&sm.dO[r][j]);
+                    const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[i][j]);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dU[r][j]);
+                    sp += o4.x * u4.x + o4.y * u4.y + o4.z * u4.z + o4.w * u4.w;
+                    st += d4.x * sm.Y[i][j] + d4.y * sm.Y[i][j + 1] + d4.z * sm.Y[i][j + 2] +
+                          d4.w * sm.Y[i][j + 3];
                 }
                 if (i <= r) sm.dP[r][i] += sp;
                 if (i < r) sm.dT[r][i] += st * sm.beta[i];
@@ -246,19 +305,23 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             }
             __syncthreads();
             // ---- dQt += dO S0^T, dKt -= dY S0^T, dKb += U dS^T (old dS), gamma_last term ----
+            for (int j = 0; j < BV; j += 4) {
+                float s0v[4], dsv[4];
 #pragma unroll
-            for (int m = 0; m < RPT; ++m) {
-                const int r = or0 + RSTEP * m, c = oc;
-                float sq = 0.f, sk = 0.f, sb = 0.f;
-                for (int j = 0; j < BV; ++j) {
-                    const float s0 = sm.S0[c][j];
-                    sq += sm.dO[r][j] * s0;
-                    sk += sm.dU[r][j] * s0;
-                    sb += sm.U[r][j] * sm.dS[c][j0 + j];
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    s0v[q2] = sm.S0[oc][j + q2];
+                    dsv[q2] = sm.dS[oc][j0 + j + q2];
                 }
-                aQt[m] += sq;
-                aKt[m] -= sk;
-                aKb[m] += sb;
+#pragma unroll
+                for (int m = 0; m < RPT; ++m) {
+                    const int r = or0 + RSTEP * m;
+                    const float4 o4 = *reinterpret_cast<const float4 *>(&sm.dO[r][j]);
+                    const float4 y4 = *reinterpret_cast<const float4 *>(&sm.dU[r][j]);
+                    const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[r][j]);
+                    aQt[m] += o4.x * s0v[0] + o4.y * s0v[1] + o4.z * s0v[2] + o4.w * s0v[3];
+                    aKt[m] -= y4.x * s0v[0] + y4.y * s0v[1] + y4.z * s0v[2] + y4.w * s0v[3];
+                    aKb[m] += u4.x * dsv[0] + u4.y * dsv[1] + u4.z * dsv[2] + u4.w * dsv[3];
+                }
             }
             if (t < D) {
                 float s = 0.f;
@@ -266,12 +329,34 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 sm.gsum[t] += s;
             }
             __syncthreads();
-            // ---- dS <- diag(gC) dS + Qt^T dO - Kt^T dY on this block's columns ----
-            for (int idx = t; idx < D * BV; idx += kThreads) {
-                const int c = idx / BV, j = idx % BV;
-                float s = sm.gC[c] * sm.dS[c][j0 + j];
-                for (int r = 0; r < C; ++r) s += sm.Qt[r][c] * sm.dO[r][j] - sm.Kt[r][c] * sm.dU[r][j];
-                sm.dS[c][j0 + j] = s;
+            // ---- dS <- diag(gC) dS + Qt^T dO - Kt^T dY on this block's columns,
+            // each thread a tile of 4 channels x 2 columns (D / 4 x 16 threads:
+            // all 512 for D = 128, warps 0-7 for D = 64) ----
+            if (t < (D / 4) * 16) {
+                const int jp = (t & 15) * 2, c4 = (t >> 4) * 4;
+                float acc[4][2];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    acc[m][0] = sm.gC[c4 + m] * sm.dS[c4 + m][j0 + jp];
+                    acc[m][1] = sm.gC[c4 + m] * sm.dS[c4 + m][j0 + jp + 1];
+                }
+                for (int r = 0; r < C; ++r) {
+                    const float4 qv = *reinterpret_cast<const float4 *>(&sm.Qt[r][c4]);
+                    const float4 kv = *reinterpret_cast<const float4 *>(&sm.Kt[r][c4]);
+                    const float o0 = sm.dO[r][jp], o1 = sm.dO[r][jp + 1];
+                    const float y0 = sm.dU[r][jp], y1 = sm.dU[r][jp + 1];
+                    const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        acc[m][0] += qa[m] * o0 - ka[m] * y0;
+                        acc[m][1] += qa[m] * o1 - ka[m] * y1;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    sm.dS[c4 + m][j0 + jp] = acc[m][0];
+                    sm.dS[c4 + m][j0 + jp + 1] = acc[m][1];
+                }
             }
         }
         __syncthreads();
