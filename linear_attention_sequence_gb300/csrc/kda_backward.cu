@@ -9,8 +9,7 @@
 // chunk).
 //
 // Per chunk (C = 32 tokens; Gamma the running sum of g inside the chunk,
-// gamma = e^Gamma, gC its last row; products taken pairwise as
-// e^{Gamma_r - Gamma_i} <= 1, so nothing overflows):
+// gamma = e^Gamma, gC its last row):
 //
 //   forward again:  G[r,i] = sum_c k_rc k_ic e^{Gamma_rc - Gamma_ic} (i < r),
 //                   P[r,i] = sum_c q_rc k_ic e^{...} (i <= r), T = (I + diag(beta) G)^{-1},
@@ -23,6 +22,15 @@
 //                   dS0 = diag(gC) dS + Qt^T dO - Kt^T dY   (the adjoint for the chunk before),
 //   then the pairwise terms of dG = diag(beta) dA and dP into dq, dk and dGamma, the
 //   element-wise terms of Qt, Kt, Kb, and dg = the reverse running sum of dGamma.
+//
+// Every decay factor is taken against the chunk midpoint Gamma_15 ("Understanding
+// Kimi K3's Attention", log-decay bound: |Gamma_r - Gamma_15| <= 16 x 5 = 80 inside a
+// 32-token chunk, so each factor stays in the fp32 range): with Q1 = q e^{Gamma -
+// Gamma_15}, A1 = k e^{Gamma - Gamma_15} and B1 = k e^{Gamma_15 - Gamma}, G = A1 B1^T and
+// P = Q1 B1^T are plain products, the pairwise gradient terms are R1 = dP B1,
+// R2 = dG B1, R3 = dG^T A1 + dP^T Q1, and Qt, Kt, Kb differ from Q1, A1, B1 by the
+// per-channel factors e^{Gamma_15} and e^{Gamma_C - Gamma_15}, folded into the operands
+// and results.
 //
 // One CTA of 512 threads per (sequence, head).  The adjoint dS (d x d) stays in
 // shared memory for the whole sequence; the value axis is processed in blocks of
@@ -40,18 +48,20 @@ constexpr int kWarps = kThreads / 32;
 
 template <int D>
 struct BwdSmem {
-    float dS[D][D + 1];        // adjoint of the state at the end of the current chunk
-    float S0[D][BV + 1];       // the chunk's start state, one column block
-    float Q[C][D], K[C][D];    // q, k of the chunk (rows past its end are 0)
-    float Gam[C][D];           // Gamma
-    float Qt[C][D], Kt[C][D], Kb[C][D];   // q.gamma, k.gamma, k.gamma_last/gamma
+    float dS[D][D + 4];        // adjoint of the state at the end of the current chunk
+    float S0[D][BV + 4];       // e^{Gamma_15} . S0 (the chunk's start state), one column block
+    float Gam[C][D + 4];       // Gamma
+    // decay factored around the chunk midpoint (|Gamma - Gamma_15| <= 80: no factor
+    // leaves the fp32 range): q e^{Gamma - Gamma_15}, k e^{Gamma - Gamma_15}, k e^{Gamma_15 - Gamma}
+    float Q1[C][D + 4], A1[C][D + 4], B1[C][D + 4];
     // rows of 36 floats (16-byte aligned: read four columns at a time); Y keeps 33
     // (read down its columns)
     float V[C][BV + 4], dO[C][BV + 4], U[C][BV + 4], dU[C][BV + 4];
     float Y[C][BV + 1];
-    float G[C][C + 1], P[C][C + 1], T[C][C + 1], dP[C][C + 1], dT[C][C + 1];
+    float G[C][C + 4], P[C][C + 4], dP[C][C + 4];   // G holds dG after the column blocks
+    float T[C][C + 1], dT[C][C + 1];
     float beta[C], dbeta[C];
-    float gC[D], gsum[D];      // gamma_last; sum_j dS . S0 by row (the gamma_last term)
+    float e15[D], fC[D], gC[D], gsum[D];   // e^{Gamma_15}, e^{Gamma_C - Gamma_15}, e^{Gamma_C}, sum dS . S0
 };
 
 template <typename IN_T, typename OUT_T, int D>
@@ -60,10 +70,11 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                     const IN_T *__restrict__ v, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *__restrict__ init_state,
                     const int32_t *__restrict__ cu, const float *__restrict__ chunk_states,
-                    int64_t chunk_capacity, const IN_T *__restrict__ d_out, const float *__restrict__ d_final,
-                    OUT_T *__restrict__ dq, OUT_T *__restrict__ dk, OUT_T *__restrict__ dv,
-                    float *__restrict__ dg, float *__restrict__ dbeta,
-                    float *__restrict__ d_init, int H, int64_t total, int64_t seq_len) {
+                    int64_t chunk_capacity, const IN_T *__restrict__ d_out,
+                    const float *__restrict__ d_final, OUT_T *__restrict__ dq,
+                    OUT_T *__restrict__ dk, OUT_T *__restrict__ dv, float *__restrict__ dg,
+                    float *__restrict__ dbeta, float *__restrict__ d_init, int H, int64_t total,
+                    int64_t seq_len) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdSmem<D> &sm = *reinterpret_cast<BwdSmem<D> *>(smem_raw);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -80,6 +91,10 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     constexpr int RSTEP = kThreads / D;        // 4 (D = 128) or 8 (D = 64)
     constexpr int RPT = C / RSTEP;             // rows per thread: 8 or 4
     const int oc = t % D, or0 = t / D;
+    // 2 x 2 tiles of a C x C or C x BV product, one half of the block per product
+    const bool hi_half = t >= kThreads / 2;    // warp-uniform
+    const int th = t & (kThreads / 2 - 1);
+    const int tcol = (th & 15) * 2, trow = (th >> 4) * 2;
 
     for (int idx = t; idx < D * D; idx += kThreads) {
         const int r = idx / D, c = idx % D;
@@ -98,7 +113,7 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                                : nullptr;
         __syncthreads();   // the previous chunk is done with every buffer
 
-        // ---- load q, k, g (rows past the end are 0) and beta ----
+        // ---- load q (into Q1), k (into A1), g (into Gam); rows past the end are 0 ----
         for (int idx = t; idx < C * D; idx += kThreads) {
             const int r = idx / D, c = idx % D;
             float qv = 0.f, kv = 0.f, gv = 0.f;
@@ -108,8 +123,8 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 kv = kda::ld_elem(k + off);
                 gv = g[off];
             }
-            sm.Q[r][c] = qv;
-            sm.K[r][c] = kv;
+            sm.Q1[r][c] = qv;
+            sm.A1[r][c] = kv;
             sm.Gam[r][c] = gv;
         }
         if (t < C) {
@@ -117,72 +132,58 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             sm.dbeta[t] = 0.f;
         }
         __syncthreads();
-        // ---- Gamma (running sum per channel), gamma_last ----
+        // ---- Gamma (running sum per channel) and the per-channel factors ----
         if (t < D) {
-            float run = 0.f;
+            float run = 0.f, g15 = 0.f;
             for (int r = 0; r < C; ++r) {
                 run += sm.Gam[r][t];
                 sm.Gam[r][t] = run;
+                if (r == 15) g15 = run;
             }
+            sm.e15[t] = __expf(g15);
+            sm.fC[t] = __expf(run - g15);
             sm.gC[t] = __expf(run);
             sm.gsum[t] = 0.f;
         }
         __syncthreads();
-        // ---- decay-weighted copies ----
+        // ---- decay-factored copies ----
         for (int idx = t; idx < C * D; idx += kThreads) {
             const int r = idx / D, c = idx % D;
-            const float gam = sm.Gam[r][c];
-            const float e = __expf(gam), eb = __expf(sm.Gam[C - 1][c] - gam);
-            sm.Qt[r][c] = sm.Q[r][c] * e;
-            sm.Kt[r][c] = sm.K[r][c] * e;
-            sm.Kb[r][c] = sm.K[r][c] * eb;
+            const float d1 = sm.Gam[r][c] - sm.Gam[15][c];
+            const float kv = sm.A1[r][c];
+            sm.Q1[r][c] *= __expf(d1);
+            sm.A1[r][c] = kv * __expf(d1);
+            sm.B1[r][c] = kv * __expf(-d1);
         }
-        // ---- G (strict) and P (inclusive) over the lower triangle: each warp takes
-        // four (r, i) pairs at a time, lanes over channels, so that the four
-        // reductions overlap; the upper triangle is zero ----
+        __syncthreads();
+        // ---- G = A1 B1^T (strict) on one half, P = Q1 B1^T (inclusive) on the other ----
+        {
+            const float(*Am)[D + 4] = hi_half ? sm.Q1 : sm.A1;
+            float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+            for (int c = 0; c < D; c += 4) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(&Am[trow][c]);
+                const float4 x1 = *reinterpret_cast<const float4 *>(&Am[trow + 1][c]);
+                const float4 y0 = *reinterpret_cast<const float4 *>(&sm.B1[tcol][c]);
+                const float4 y1 = *reinterpret_cast<const float4 *>(&sm.B1[tcol + 1][c]);
+                a00 += x0.x * y0.x + x0.y * y0.y + x0.z * y0.z + x0.w * y0.w;
+                a01 += x0.x * y1.x + x0.y * y1.y + x0.z * y1.z + x0.w * y1.w;
+                a10 += x1.x * y0.x + x1.y * y0.y + x1.z * y0.z + x1.w * y0.w;
+                a11 += x1.x * y1.x + x1.y * y1.y + x1.z * y1.z + x1.w * y1.w;
+            }
+            const float av[2][2] = {{a00, a01}, {a10, a11}};
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int w2 = 0; w2 < 2; ++w2) {
+                    const int r = trow + u, i = tcol + w2;
+                    if (hi_half) sm.P[r][i] = i <= r ? av[u][w2] : 0.f;
+                    else sm.G[r][i] = i < r ? av[u][w2] : 0.f;
+                }
+        }
         for (int idx = t; idx < C * C; idx += kThreads) {
             const int r = idx / C, i = idx % C;
-            if (i > r) sm.G[r][i] = sm.P[r][i] = sm.dP[r][i] = sm.dT[r][i] = 0.f;
-        }
-        constexpr int NPAIR = C * (C + 1) / 2;
-        for (int p0 = 4 * warp; p0 < NPAIR; p0 += 4 * kWarps) {
-            int rr[4], ii[4];
-            float gg[4], pp[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int p = p0 + u < NPAIR ? p0 + u : NPAIR - 1;
-                int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
-                while (r * (r + 1) / 2 > p) --r;
-                while ((r + 1) * (r + 2) / 2 <= p) ++r;
-                rr[u] = r;
-                ii[u] = p - r * (r + 1) / 2;
-                gg[u] = pp[u] = 0.f;
-            }
-            for (int c = lane; c < D; c += 32) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float e = __expf(sm.Gam[rr[u]][c] - sm.Gam[ii[u]][c]);
-                    const float ke = sm.K[ii[u]][c] * e;
-                    gg[u] += sm.K[rr[u]][c] * ke;
-                    pp[u] += sm.Q[rr[u]][c] * ke;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    gg[u] += __shfl_xor_sync(0xffffffffu, gg[u], o);
-                    pp[u] += __shfl_xor_sync(0xffffffffu, pp[u], o);
-                }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (lane == u && p0 + u < NPAIR) {
-                    const int r = rr[u], i = ii[u];
-                    sm.G[r][i] = i < r ? gg[u] : 0.f;
-                    sm.P[r][i] = pp[u];
-                    sm.dP[r][i] = 0.f;
-                    sm.dT[r][i] = 0.f;
-                }
+            sm.dP[r][i] = 0.f;
+            sm.dT[r][i] = 0.f;
         }
         __syncthreads();
         // ---- T = (I + diag(beta) G)^{-1}: lane j solves column j (warp 0) ----
@@ -201,16 +202,17 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
 #pragma unroll
             for (int i = 0; i < C; ++i) sm.T[i][lane] = x[i];
         }
-        float aQt[RPT], aKt[RPT], aKb[RPT];   // dQt, dKt, dKb of (or0 + RSTEP m, oc)
+        // e^{Gamma_15}-scaled accumulators: aQ = e15 . dQt, aK = e15 . dKt, aB = dKb
+        float aQ[RPT], aK[RPT], aB[RPT];
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) aQt[m] = aKt[m] = aKb[m] = 0.f;
+        for (int m = 0; m < RPT; ++m) aQ[m] = aK[m] = aB[m] = 0.f;
 
         for (int j0 = 0; j0 < D; j0 += BV) {
-            __syncthreads();   // T is ready; the previous block is done with V, dO, Y, U, dU, S0
-            // ---- this block of S0, V and dO ----
+            __syncthreads();   // T is ready; the previous block is done with its buffers
+            // ---- this block of e15 . S0, V and dO ----
             for (int idx = t; idx < D * BV; idx += kThreads) {
                 const int c = idx / BV, j = idx % BV;
-                sm.S0[c][j] = S0g ? S0g[(int64_t)c * D + j0 + j] : 0.f;
+                sm.S0[c][j] = S0g ? sm.e15[c] * S0g[(int64_t)c * D + j0 + j] : 0.f;
             }
             for (int idx = t; idx < C * BV; idx += kThreads) {
                 const int r = idx / BV, j = idx % BV;
@@ -219,50 +221,54 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 sm.dO[r][j] = r < L ? kda::ld_elem(d_out + off) : 0.f;
             }
             __syncthreads();
-            // ---- Y = V - Kt S0 (threads 0-255) and dU = Kb dS + P^T dO (threads 256-511),
-            // each thread a tile of 2 rows x 2 columns ----
+            // ---- Y = V - A1 (e15 . S0) on one half, dU = B1 (fC . dS) + P^T dO on the other ----
             {
-                const bool du_half = t >= kThreads / 2;   // warp-uniform
-                const int th = t & (kThreads / 2 - 1);
-                const int jp = (th & 15) * 2, r2 = (th >> 4) * 2;
-                const float(*A)[D] = du_half ? sm.Kb : sm.Kt;
+                const float(*Am)[D + 4] = hi_half ? sm.B1 : sm.A1;
                 float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
                 for (int c = 0; c < D; c += 4) {
-                    const float4 x0 = *reinterpret_cast<const float4 *>(&A[r2][c]);
-                    const float4 x1 = *reinterpret_cast<const float4 *>(&A[r2 + 1][c]);
+                    const float4 x0 = *reinterpret_cast<const float4 *>(&Am[trow][c]);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(&Am[trow + 1][c]);
                     float b0[4], b1[4];
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        b0[q2] = du_half ? sm.dS[c + q2][j0 + jp] : sm.S0[c + q2][jp];
-                        b1[q2] = du_half ? sm.dS[c + q2][j0 + jp + 1] : sm.S0[c + q2][jp + 1];
+                    for (int q2 = 0; q2 < 4; ++q2) {   // two adjacent columns per 8-byte load
+                        if (hi_half) {
+                            const float f = sm.fC[c + q2];
+                            const float2 d2 = *reinterpret_cast<const float2 *>(&sm.dS[c + q2][j0 + tcol]);
+                            b0[q2] = f * d2.x;
+                            b1[q2] = f * d2.y;
+                        } else {
+                            const float2 s2 = *reinterpret_cast<const float2 *>(&sm.S0[c + q2][tcol]);
+                            b0[q2] = s2.x;
+                            b1[q2] = s2.y;
+                        }
                     }
                     a00 += x0.x * b0[0] + x0.y * b0[1] + x0.z * b0[2] + x0.w * b0[3];
                     a01 += x0.x * b1[0] + x0.y * b1[1] + x0.z * b1[2] + x0.w * b1[3];
                     a10 += x1.x * b0[0] + x1.y * b0[1] + x1.z * b0[2] + x1.w * b0[3];
                     a11 += x1.x * b1[0] + x1.y * b1[1] + x1.z * b1[2] + x1.w * b1[3];
                 }
-                if (!du_half) {
-                    sm.Y[r2][jp] = sm.V[r2][jp] - a00;
-                    sm.Y[r2][jp + 1] = sm.V[r2][jp + 1] - a01;
-                    sm.Y[r2 + 1][jp] = sm.V[r2 + 1][jp] - a10;
-                    sm.Y[r2 + 1][jp + 1] = sm.V[r2 + 1][jp + 1] - a11;
+                if (!hi_half) {
+                    sm.Y[trow][tcol] = sm.V[trow][tcol] - a00;
+                    sm.Y[trow][tcol + 1] = sm.V[trow][tcol + 1] - a01;
+                    sm.Y[trow + 1][tcol] = sm.V[trow + 1][tcol] - a10;
+                    sm.Y[trow + 1][tcol + 1] = sm.V[trow + 1][tcol + 1] - a11;
                 } else {
-                    for (int rp = r2; rp < C; ++rp) {   // P^T dO (P[rp][r] is 0 for rp < r)
-                        const float p0v = sm.P[rp][r2], p1v = sm.P[rp][r2 + 1];
-                        const float o0 = sm.dO[rp][jp], o1 = sm.dO[rp][jp + 1];
+                    for (int rp = trow; rp < C; ++rp) {   // P^T dO (P[rp][r] is 0 for rp < r)
+                        const float p0v = sm.P[rp][trow], p1v = sm.P[rp][trow + 1];
+                        const float o0 = sm.dO[rp][tcol], o1 = sm.dO[rp][tcol + 1];
                         a00 += p0v * o0;
                         a01 += p0v * o1;
                         a10 += p1v * o0;
                         a11 += p1v * o1;
                     }
-                    sm.dU[r2][jp] = a00;
-                    sm.dU[r2][jp + 1] = a01;
-                    sm.dU[r2 + 1][jp] = a10;
-                    sm.dU[r2 + 1][jp + 1] = a11;
+                    sm.dU[trow][tcol] = a00;
+                    sm.dU[trow][tcol + 1] = a01;
+                    sm.dU[trow + 1][tcol] = a10;
+                    sm.dU[trow + 1][tcol + 1] = a11;
                 }
             }
             __syncthreads();
-            // ---- U = T diag(beta) Y; dB = T^T dU (in place of dU after the reads below) ----
+            // ---- U = T diag(beta) Y; dB = T^T dU (kept in registers) ----
             float dbv[C / kWarps];
 #pragma unroll
             for (int x = 0; x < C / kWarps; ++x) {
@@ -304,45 +310,43 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + j0 + j, dy);
             }
             __syncthreads();
-            // ---- dQt += dO S0^T, dKt -= dY S0^T, dKb += U dS^T (old dS), gamma_last term ----
+            // ---- aQ += dO (e15 S0)^T, aK -= dY (e15 S0)^T, aB += U dS^T (dS before the
+            // update below); the gamma_last term sum_j dS . (e15 S0) ----
             for (int j = 0; j < BV; j += 4) {
-                float s0v[4], dsv[4];
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    s0v[q2] = sm.S0[oc][j + q2];
-                    dsv[q2] = sm.dS[oc][j0 + j + q2];
-                }
+                const float4 s4 = *reinterpret_cast<const float4 *>(&sm.S0[oc][j]);
+                const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[oc][j0 + j]);
 #pragma unroll
                 for (int m = 0; m < RPT; ++m) {
                     const int r = or0 + RSTEP * m;
                     const float4 o4 = *reinterpret_cast<const float4 *>(&sm.dO[r][j]);
                     const float4 y4 = *reinterpret_cast<const float4 *>(&sm.dU[r][j]);
                     const float4 u4 = *reinterpret_cast<const float4 *>(&sm.U[r][j]);
-                    aQt[m] += o4.x * s0v[0] + o4.y * s0v[1] + o4.z * s0v[2] + o4.w * s0v[3];
-                    aKt[m] -= y4.x * s0v[0] + y4.y * s0v[1] + y4.z * s0v[2] + y4.w * s0v[3];
-                    aKb[m] += u4.x * dsv[0] + u4.y * dsv[1] + u4.z * dsv[2] + u4.w * dsv[3];
+                    aQ[m] += o4.x * s4.x + o4.y * s4.y + o4.z * s4.z + o4.w * s4.w;
+                    aK[m] -= y4.x * s4.x + y4.y * s4.y + y4.z * s4.z + y4.w * s4.w;
+                    aB[m] += u4.x * d4.x + u4.y * d4.y + u4.z * d4.z + u4.w * d4.w;
                 }
             }
             if (t < D) {
                 float s = 0.f;
-                for (int j = 0; j < BV; ++j) s += sm.dS[t][j0 + j] * sm.S0[t][j];
+                for (int j = 0; j < BV; j += 4) {
+                    const float4 s4 = *reinterpret_cast<const float4 *>(&sm.S0[t][j]);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(&sm.dS[t][j0 + j]);
+                    s += s4.x * d4.x + s4.y * d4.y + s4.z * d4.z + s4.w * d4.w;
+                }
                 sm.gsum[t] += s;
             }
             __syncthreads();
-            // ---- dS <- diag(gC) dS + Qt^T dO - Kt^T dY on this block's columns,
+            // ---- dS <- diag(gC) dS + diag(e15) (Q1^T dO - A1^T dY) on this block's columns,
             // each thread a tile of 4 channels x 2 columns (D / 4 x 16 threads:
             // all 512 for D = 128, warps 0-7 for D = 64) ----
             if (t < (D / 4) * 16) {
                 const int jp = (t & 15) * 2, c4 = (t >> 4) * 4;
                 float acc[4][2];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    acc[m][0] = sm.gC[c4 + m] * sm.dS[c4 + m][j0 + jp];
-                    acc[m][1] = sm.gC[c4 + m] * sm.dS[c4 + m][j0 + jp + 1];
-                }
+                for (int m = 0; m < 4; ++m) acc[m][0] = acc[m][1] = 0.f;
                 for (int r = 0; r < C; ++r) {
-                    const float4 qv = *reinterpret_cast<const float4 *>(&sm.Qt[r][c4]);
-                    const float4 kv = *reinterpret_cast<const float4 *>(&sm.Kt[r][c4]);
+                    const float4 qv = *reinterpret_cast<const float4 *>(&sm.Q1[r][c4]);
+                    const float4 kv = *reinterpret_cast<const float4 *>(&sm.A1[r][c4]);
                     const float o0 = sm.dO[r][jp], o1 = sm.dO[r][jp + 1];
                     const float y0 = sm.dU[r][jp], y1 = sm.dU[r][jp + 1];
                     const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w};
@@ -354,13 +358,14 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                 }
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    sm.dS[c4 + m][j0 + jp] = acc[m][0];
-                    sm.dS[c4 + m][j0 + jp + 1] = acc[m][1];
+                    const int c = c4 + m;
+                    sm.dS[c][j0 + jp] = sm.gC[c] * sm.dS[c][j0 + jp] + sm.e15[c] * acc[m][0];
+                    sm.dS[c][j0 + jp + 1] = sm.gC[c] * sm.dS[c][j0 + jp + 1] + sm.e15[c] * acc[m][1];
                 }
             }
         }
         __syncthreads();
-        // ---- dA = -T^T tril_s(dT) T^T (strict lower): M1 = tril_s(dT) T^T into dU's space ----
+        // ---- dA = -T^T tril_s(dT) T^T (strict lower): M1 = tril_s(dT) T^T into Y's space ----
         float (*M1)[BV + 1] = sm.Y;   // C x C scratch (BV == C)
 #pragma unroll
         for (int x = 0; x < C / kWarps; ++x) {
@@ -380,63 +385,68 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
             float gb = da * sm.G[r][i];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) gb += __shfl_xor_sync(0xffffffffu, gb, o);
-            __syncwarp();
             sm.G[r][i] = sm.beta[r] * da;   // dG (this thread read G[r][i] above)
             if (lane == 0) sm.dbeta[r] += gb;
         }
         __syncthreads();
-        // ---- pairwise terms, element-wise terms and dGamma for the owned (r, c) ----
+        // ---- pairwise terms R1 = dP B1, R2 = dG B1, R3 = dG^T A1 + dP^T Q1, then the
+        // gradients of the owned (x, c):
+        //   dq = e^{Gamma - Gamma_15} (aQ + R1)
+        //   dk = e^{Gamma - Gamma_15} (aK + R2) + e^{Gamma_C - Gamma} aB + e^{Gamma_15 - Gamma} R3
+        //   dGamma = Q1 (aQ + R1) + A1 (aK + R2) - B1 (fC aB + R3) ----
+        float R1[RPT], R2[RPT], R3[RPT];
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) R1[m] = R2[m] = R3[m] = 0.f;
+        for (int i = 0; i < C; i += 4) {
+            float bq[4], aq[4], qq[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                bq[q2] = sm.B1[i + q2][oc];
+                aq[q2] = sm.A1[i + q2][oc];
+                qq[q2] = sm.Q1[i + q2][oc];
+            }
+#pragma unroll
+            for (int m = 0; m < RPT; ++m) {
+                const int x = or0 + RSTEP * m;
+                const float4 p4 = *reinterpret_cast<const float4 *>(&sm.dP[x][i]);
+                const float4 g4 = *reinterpret_cast<const float4 *>(&sm.G[x][i]);
+                R1[m] += p4.x * bq[0] + p4.y * bq[1] + p4.z * bq[2] + p4.w * bq[3];
+                R2[m] += g4.x * bq[0] + g4.y * bq[1] + g4.z * bq[2] + g4.w * bq[3];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                    R3[m] += sm.G[i + q2][x] * aq[q2] + sm.dP[i + q2][x] * qq[q2];
+            }
+        }
         float dgam[RPT];
+        float kbk = 0.f;   // this thread's part of sum_i fC aB_i B1_i (the gamma_last term)
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int x = or0 + RSTEP * m, c = oc;
-            const float gx = sm.Gam[x][c], kx = sm.K[x][c], qx = sm.Q[x][c];
-            float dqx = 0.f, dkx = 0.f, dgx = 0.f;
-            // x as the later token r: pairs (x, i), i <= x
-            for (int i = 0; i <= x; ++i) {
-                const float e = __expf(gx - sm.Gam[i][c]);
-                const float ki = sm.K[i][c] * e;
-                const float dgp = sm.G[x][i], dpp = sm.dP[x][i];
-                dqx += dpp * ki;
-                dkx += dgp * ki;
-                dgx += (dgp * kx + dpp * qx) * ki;
-            }
-            // x as the earlier token i: pairs (r, x), r >= x
-            for (int r = x; r < C; ++r) {
-                const float e = __expf(sm.Gam[r][c] - gx);
-                const float dgp = sm.G[r][x], dpp = sm.dP[r][x];
-                const float w = (dgp * sm.K[r][c] + dpp * sm.Q[r][c]) * e;
-                dkx += w;
-                dgx -= w * kx;
-            }
-            const float gam = __expf(gx), kb = sm.Kb[x][c];
-            dqx += aQt[m] * gam;
-            dkx += aKt[m] * gam + aKb[m] * __expf(sm.Gam[C - 1][c] - gx);
-            dgx += aQt[m] * sm.Qt[x][c] + aKt[m] * sm.Kt[x][c] - aKb[m] * kb;
+            const float gx = sm.Gam[x][c], g15 = sm.Gam[15][c];
+            const float ex = __expf(gx - g15), ix = __expf(g15 - gx);
+            const float sq = aQ[m] + R1[m], sk = aK[m] + R2[m];
+            const float fb = sm.fC[c] * aB[m];
             if (x < L) {
                 const int64_t off = (t0 + x) * rowK + (int64_t)h * D + c;
-                kda::st_elem(dq + off, dqx);
-                kda::st_elem(dk + off, dkx);
+                kda::st_elem(dq + off, ex * sq);
+                kda::st_elem(dk + off, ex * sk + __expf(sm.Gam[C - 1][c] - gx) * aB[m] + ix * R3[m]);
             }
-            dgam[m] = dgx;
+            const float b1 = sm.B1[x][c];
+            dgam[m] = sm.Q1[x][c] * sq + sm.A1[x][c] * sk - b1 * (fb + R3[m]);
+            kbk += fb * b1;
         }
-        // the gamma_last terms: column sums of dKb . Kb, and gC sum_j dS . S0
-        __syncthreads();   // every read of Kt / Qt above is done: reuse Kt for dGamma
+        __syncthreads();   // every read of Q1 / A1 above is done: reuse them
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) sm.Kt[or0 + RSTEP * m][oc] = dgam[m];
-        // (column sums of dKb . Kb over rows: the owned rows' part, reduced below)
-        float kbk = 0.f;
-#pragma unroll
-        for (int m = 0; m < RPT; ++m) kbk += aKb[m] * sm.Kb[or0 + RSTEP * m][oc];
-        sm.Qt[or0][oc] = kbk;   // Qt is free: one partial per (row group, channel)
+        for (int m = 0; m < RPT; ++m) sm.A1[or0 + RSTEP * m][oc] = dgam[m];
+        sm.Q1[or0][oc] = kbk;   // one partial per (row group, channel)
         __syncthreads();
         // ---- dg = reverse running sum of dGamma over the chunk (thread per channel) ----
         if (t < D) {
-            float last = sm.gC[t] * sm.gsum[t];
-            for (int r0 = 0; r0 < RSTEP; ++r0) last += sm.Qt[r0][t];
+            float last = sm.fC[t] * sm.gsum[t];
+            for (int r0 = 0; r0 < RSTEP; ++r0) last += sm.Q1[r0][t];
             float run = 0.f;
             for (int r = C - 1; r >= 0; --r) {
-                run += sm.Kt[r][t] + (r == C - 1 ? last : 0.f);
+                run += sm.A1[r][t] + (r == C - 1 ? last : 0.f);
                 if (r < L) dg[(t0 + r) * rowK + (int64_t)h * D + t] = run;
             }
         }
