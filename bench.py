@@ -546,6 +546,19 @@ def run_profile_case(args, kda, synth, dev, stream):
                             cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
                             variant=args.variant, stream=stream)
         units = args.tokens
+    elif args.profile == "backward":
+        w = synth.WORKLOADS["prefill_8k"]
+        inp = synth.prefill_inputs(w, dev, lengths=(args.tokens,))
+        gen = torch.Generator(device=dev).manual_seed(87)
+        d_out = torch.randn((args.tokens, w.heads, w.d), generator=gen, device=dev).to(w.dtype)
+        _, _, cstates = kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"],
+                                                     inp["beta"], cu_seqlens=inp["cu_seqlens"],
+                                                     interval=kda.CHUNK, stream=stream)
+
+        def step():
+            kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                             cu_seqlens=inp["cu_seqlens"], chunk_states=cstates, stream=stream)
+        units = args.tokens
     else:
         wd = synth.WORKLOADS["decode_256x64"]
         dx = synth.decode_inputs(wd, dev, num_seqs=args.seqs, steps=1)
@@ -568,7 +581,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
                     help="run only one kernel family on a reduced case (for ncu)")
     ap.add_argument("--tokens", type=int, default=2048, help="--profile prefill: tokens")
     ap.add_argument("--seqs", type=int, default=64, help="--profile decode: sequences")
