@@ -208,6 +208,28 @@ kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const v
                                     void *out, float *final_state, kda_stream_t stream);
 
 /*
+ * kda_output_gate -- the output gate alone, in place: for every row (token t,
+ * head h) of `out`,
+ *
+ *   out[t,h,j] <- Sigmoid(gate_logit[t,h,j]) * out[t,h,j] / sqrt(ms + eps) * w[j],
+ *   ms = (1/d_v) sum_j out[t,h,j]^2,
+ *
+ * the same gate as kda_prefill_output_gated, for outputs that another call
+ * wrote: kda_prefill_gated's, or kda_decode's (dims->total_tokens rows).
+ *
+ *   out          device, out_dtype, [T_tot, H, d_v], read and overwritten.
+ *   gate_logit   device, in_dtype, [T_tot, H, d_v]; must not alias out.
+ *   norm_weight  device fp32 [d_v], 4-byte aligned, or NULL (weight 1).
+ *   eps          finite, > 0.
+ *
+ * dims->num_seqs and dims->variant are not used; d_k must equal d_v as
+ * everywhere.  KDA_ERR_INVALID_ARGUMENT for a bad dims, a NULL or misaligned
+ * pointer while there are rows, gate_logit == out, or a bad eps.
+ */
+kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_logit,
+                           const float *norm_weight, float eps, kda_stream_t stream);
+
+/*
  * kda_prefill_scalar_decay -- the same chunked prefill for the two special
  * cases of the recurrence the pages build KDA from ("Kimi K3.1 and the Road
  * From Softmax Attention to Kimi Delta Attention", sections "3. The delta

@@ -12,6 +12,7 @@ method and has no fallback: if the library is missing, every call raises.
     kda_prefill_output_gated(q, k, v, g, beta, gate_logit, ...)   the same, then the output gate
     kda_prefill_scalar_decay(q, k, v, g_head, beta, ...)   Gated DeltaNet / the delta rule
     kda_backward(q, k, v, g, beta, d_out, ...)   gradients of kda_prefill
+    kda_output_gate(out, gate_logit, ...)   the output gate alone, in place
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -22,7 +23,8 @@ import os
 import torch
 
 __all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
-           "kda_prefill_output_gated", "kda_prefill_scalar_decay", "kda_backward", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+           "kda_prefill_output_gated", "kda_prefill_scalar_decay", "kda_backward",
+           "kda_output_gate", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -84,6 +86,8 @@ def lib():
         L.kda_backward.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, fp,
                                    ctypes.c_int64, vp, fp, vp, vp, vp, fp, fp, fp, vp]
         L.kda_backward.restype = ctypes.c_int
+        L.kda_output_gate.argtypes = [ctypes.POINTER(Dims), vp, vp, fp, ctypes.c_float, vp]
+        L.kda_output_gate.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -322,6 +326,28 @@ def kda_backward(q, k, v, g, beta, d_out, d_final_state=None, init_state=None, c
                             _ptr(res["d_init_state"]), _stream(stream))
     _check(st, "kda_backward")
     return res
+
+
+def kda_output_gate(out, gate_logit, norm_weight=None, eps=1e-6, stream=None):
+    """The output gate in place on ``out`` [T, H, d_v] (C entry point
+    ``kda_output_gate``): out = Sigmoid(gate_logit) * out / sqrt(mean over d_v
+    of out^2 + eps) * norm_weight.  gate_logit [T, H, d_v] fp32 or bf16;
+    norm_weight fp32 [d_v] or None.  Returns ``out``."""
+    _require(out, "out", ndim=3)
+    _require(gate_logit, "gate_logit", ndim=3)
+    _require(norm_weight, "norm_weight", torch.float32, 1)
+    if out.dtype not in _DTYPES or gate_logit.dtype not in _DTYPES:
+        raise ValueError("out and gate_logit must be fp32 or bf16")
+    if gate_logit.shape != out.shape:
+        raise ValueError("gate_logit must have the shape of out")
+    T, H, dv = out.shape
+    if norm_weight is not None and norm_weight.shape[0] != dv:
+        raise ValueError("norm_weight must hold one value per value channel")
+    dims = Dims(1, T, H, dv, dv, _DTYPES[gate_logit.dtype], _DTYPES[out.dtype], 0)
+    _check(lib().kda_output_gate(ctypes.byref(dims), _ptr(out), _ptr(gate_logit),
+                                 _ptr(norm_weight), ctypes.c_float(eps), _stream(stream)),
+           "kda_output_gate")
+    return out
 
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,

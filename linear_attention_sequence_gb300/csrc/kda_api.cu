@@ -209,6 +209,25 @@ kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const v
                           stream, "kda_prefill_output_gated");
 }
 
+kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_logit,
+                           const float *norm_weight, float eps, kda_stream_t stream) {
+    kda::Problem P;
+    kda_status st = check_dims(dims, P);
+    if (st != KDA_OK) return st;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARGUMENT;
+    if (norm_weight && ((uintptr_t)norm_weight & 3u)) return KDA_ERR_INVALID_ARGUMENT;
+    if (P.T == 0) return KDA_OK;
+    if (!out || !gate_logit || gate_logit == (const void *)out) return KDA_ERR_INVALID_ARGUMENT;
+    const uintptr_t ga = P.in_dtype == KDA_DTYPE_BF16 ? 1u : 3u, oa = P.out_dtype == KDA_DTYPE_BF16 ? 1u : 3u;
+    if (((uintptr_t)gate_logit & ga) || ((uintptr_t)out & oa)) return KDA_ERR_INVALID_ARGUMENT;
+    P.ogate = gate_logit;
+    P.onorm_w = norm_weight;
+    P.oeps = eps;
+    cudaError_t e = kda_launch_output_gate(P, out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_output_gate");
+    return KDA_OK;
+}
+
 kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const void *k,
                                     const void *v, const float *g_head, const float *beta,
                                     const float *init_state, const int32_t *cu_seqlens,

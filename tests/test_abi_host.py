@@ -253,6 +253,25 @@ def test_backward_empty_batch_is_ok(L):
                     db=None) == OK
 
 
+@pytest.mark.parametrize("dims,over", [
+    (None, {}), (D(num_heads=0), {}), (D(), {"out": None}), (D(), {"gl": None}),
+    (D(), {"gl": ctypes.c_void_p(0x20000)}),                    # gate aliases out
+    (D(), {"gl": ctypes.c_void_p(0x60001)}), (D(), {"out": ctypes.c_void_p(0x20001)}),
+    (D(), {"w": ctypes.c_void_p(0x80002)}), (D(), {"eps": 0.0}), (D(), {"eps": float("nan")}),
+])
+def test_output_gate_rejects(L, dims, over):
+    args = dict(out=ctypes.c_void_p(0x20000), gl=ctypes.c_void_p(0x60000), w=None, eps=1e-6)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    assert L.kda_output_gate(d, args["out"], args["gl"], args["w"], ctypes.c_float(args["eps"]),
+                             None) == INVALID
+
+
+def test_output_gate_no_rows_is_ok(L):
+    assert L.kda_output_gate(ctypes.byref(D(total_tokens=0)), None, None, None,
+                             ctypes.c_float(1e-6), None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

@@ -504,3 +504,26 @@ def test_scalar_decay_equals_prefill_of_broadcast_decay(variant):
                                      init_state=inp["init_state"], out_dtype=torch.float32,
                                      variant=variant)
         assert torch.equal(out, out0) and torch.equal(fin, fin0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_output_gate_alone_on_decode_and_gated_outputs(dtype):
+    """kda_output_gate in place equals the oracle's gate on the same ungated
+    values: on a decode step's output and on kda_prefill_gated's output."""
+    T, H, d = 70, 2, 128
+    og = synth.output_gate_inputs(T, H, d, dtype=dtype, seed=95, device=DEV)
+    inp = synth.random_inputs(T, H, d, dtype=dtype, seed=96, device=DEV)
+    gl = synth.gate_logits(T, H, d, dtype=dtype, seed=97, device=DEV)
+    o, _ = kda.kda_prefill_gated(inp["q"], inp["k"], inp["v"], gl["z"], gl["a_log"],
+                                 gl["beta_logit"], out_dtype=torch.float32)
+    ref = oracle.output_gate(host64(o), host64(og["gate"]), host64(og["norm_weight"]), OG_EPS)
+    kda.kda_output_gate(o, og["gate"], og["norm_weight"], OG_EPS)
+    assert rel_err(host64(o), ref) <= 1e-5
+    N = 16
+    dec = synth.random_inputs(N, H, d, dtype=dtype, seed=98, device=DEV, num_seqs=N, init_std=0.05)
+    state = dec["init_state"].clone()
+    od = kda.kda_decode(dec["q"], dec["k"], dec["v"], dec["g"], dec["beta"], state,
+                        out_dtype=torch.float32)
+    ref = oracle.output_gate(host64(od), host64(og["gate"][:N]), None, OG_EPS)
+    kda.kda_output_gate(od, og["gate"][:N].contiguous(), None, OG_EPS)
+    assert rel_err(host64(od), ref) <= 1e-5
