@@ -105,3 +105,20 @@ def test_backward_layer_1k_sampled_heads():
     ref = _oracle_grads(inp, d_out, d_fin, None, heads=heads)
     errs = _check(res, ref, TOL[torch.bfloat16], heads=heads)
     print("backward 1k layer (3 heads): " + " ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+
+
+def test_backward_8k_layer_sampled_heads():
+    """The 8K layer's gradients in the launch the benchmark times (all 96 heads,
+    chunk states from the tensor-core forward): two heads against the oracle's
+    reverse mode over all 8192 tokens (which keeps every state: about 1 GB of
+    host memory per head)."""
+    w = synth.WORKLOADS["prefill_8k"]
+    inp = synth.prefill_inputs(w, DEV)
+    T, H, d = inp["q"].shape
+    d_out, d_fin = _upstream(T, H, 1, d, w.dtype, 119)
+    res = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                           cu_seqlens=inp["cu_seqlens"], grad_dtype=torch.float32)
+    heads = [0, 95]
+    ref = _oracle_grads(inp, d_out, d_fin, None, heads=heads)
+    errs = _check(res, ref, TOL[torch.bfloat16], heads=heads)
+    print("backward 8k layer (2 heads): " + " ".join(f"{k} {v:.2e}" for k, v in errs.items()))
