@@ -19,9 +19,13 @@
 //                                           reads the state after its write)
 //
 // The u_r form is a forward substitution with the unit lower-triangular
-// (I + Akk), the "triangular solve" of the chunkwise form.  Every decay factor
-// is an exponential of a non-positive number, so nothing overflows for any
-// chunk length.  Rows past the end of a sequence are loaded as zeros (k = q =
+// (I + Akk), the "triangular solve" of the chunkwise form.  The Gram matrices
+// are products of factors taken against the chunk midpoint Gamma_15:
+// k_r e^{Gamma_r - Gamma_15} and q_r e^{Gamma_r - Gamma_15} against
+// k_i e^{Gamma_15 - Gamma_i}.  With g >= -5 and C = 32 every such factor is
+// within e^{+-80} ("Understanding Kimi K3's Attention", log-decay bound), inside
+// the fp32 range; the other decay factors are exponentials of non-positive
+// numbers.  Rows past the end of a sequence are loaded as zeros (k = q =
 // v = 0, g = 0, beta = 0): they neither decay nor write the state, and their
 // outputs are not stored, so sequence lengths need not divide C.
 //
@@ -39,9 +43,12 @@ constexpr int BV = 32;  // state columns per CTA (one per lane)
 
 template <int DK, int C>
 struct Smem {
-    float G[C][DK];    // Gamma, then e^{Gamma} . k
-    float K[C][DK];    // k, then e^{Gamma_last - Gamma} . k
-    float Q[C][DK];    // q, then e^{Gamma} . q
+    // rows of DK + 4 floats: 16-byte aligned, and rows four banks apart
+    float G[C][DK + 4];    // Gamma, then e^{Gamma} . k
+    float K[C][DK + 4];    // k, then k e^{Gamma - Gamma_15}, then e^{Gamma_last - Gamma} . k
+    float Q[C][DK + 4];    // q, then q e^{Gamma - Gamma_15}, then e^{Gamma} . q
+    float B1[C][DK + 4];   // k e^{Gamma_15 - Gamma}: the Gram's right factor
+    float e15[DK], eC15[DK];   // e^{Gamma_15}, e^{Gamma_last - Gamma_15}
     float S[DK][BV];   // state slice (fp32)
     float U[C][BV];    // v, then v', then u
     float Akk[C][C + 1];
@@ -86,26 +93,42 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     for (int64_t t0 = a; t0 < b; t0 += C, ++chunk) {
         const int L = (int)((b - t0) < C ? (b - t0) : C);
         __syncthreads();  // previous chunk done with every buffer
-        // ---- load the chunk (rows >= L are zeros) ----
-        for (int idx = t; idx < C * DK; idx += kThreads) {
-            const int r = idx / DK, c = idx % DK;
-            float gv = 0.f, kv = 0.f, qv = 0.f;
-            if (r < L) {
-                const int64_t off = (t0 + r) * rowK + (int64_t)h * DK + c;
-                // the decay: from its logits, one per (token, head), or per channel
-                gv = z        ? kda::gate_g(kda::ld_elem(z + off), gscale)
-                     : sdecay ? (g_head ? g_head[(t0 + r) * H + h] : 0.f)
-                              : g[off];
-                kv = kda::ld_elem(k + off);
-                qv = kda::ld_elem(q + off);
+        // ---- load the chunk (rows >= L are zeros): every load of a thread is
+        // issued before its first store, so their latencies overlap ----
+        {
+            constexpr int PER = C * DK / kThreads, PERV = C * BV / kThreads;
+            float gv[PER], kv[PER], qv[PER], vv[PERV];
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const int idx = t + m * kThreads, r = idx / DK, c = idx % DK;
+                gv[m] = kv[m] = qv[m] = 0.f;
+                if (r < L) {
+                    const int64_t off = (t0 + r) * rowK + (int64_t)h * DK + c;
+                    // the decay: from its logits, one per (token, head), or per channel
+                    gv[m] = z        ? kda::gate_g(kda::ld_elem(z + off), gscale)
+                            : sdecay ? (g_head ? g_head[(t0 + r) * H + h] : 0.f)
+                                     : g[off];
+                    kv[m] = kda::ld_elem(k + off);
+                    qv[m] = kda::ld_elem(q + off);
+                }
             }
-            sm.G[r][c] = gv;
-            sm.K[r][c] = kv;
-            sm.Q[r][c] = qv;
-        }
-        for (int idx = t; idx < C * BV; idx += kThreads) {
-            const int r = idx / BV, j = idx % BV;
-            sm.U[r][j] = r < L ? kda::ld_elem(v + (t0 + r) * rowV + (int64_t)h * DV + j0 + j) : 0.f;
+#pragma unroll
+            for (int m = 0; m < PERV; ++m) {
+                const int idx = t + m * kThreads, r = idx / BV, j = idx % BV;
+                vv[m] = r < L ? kda::ld_elem(v + (t0 + r) * rowV + (int64_t)h * DV + j0 + j) : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const int idx = t + m * kThreads, r = idx / DK, c = idx % DK;
+                sm.G[r][c] = gv[m];
+                sm.K[r][c] = kv[m];
+                sm.Q[r][c] = qv[m];
+            }
+#pragma unroll
+            for (int m = 0; m < PERV; ++m) {
+                const int idx = t + m * kThreads, r = idx / BV, j = idx % BV;
+                sm.U[r][j] = vv[m];
+            }
         }
         if (t < C) {
             const float bt = t < L ? beta[(t0 + t) * H + h] : 0.f;
@@ -124,42 +147,57 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
         }
         __syncthreads();
 
-        // ---- Gram matrices Akk (strict, beta rows) and Aqk (inclusive) ----
-        constexpr int NPAIR = C * (C + 1) / 2;
-        for (int p = warp; p < NPAIR; p += kWarps) {
-            int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
-            while (r * (r + 1) / 2 > p) --r;
-            while ((r + 1) * (r + 2) / 2 <= p) ++r;
-            const int i = p - r * (r + 1) / 2;
-            float akk = 0.f, aqk = 0.f;
-#pragma unroll 4
-            for (int c = lane; c < DK; c += 32) {
-                const float e = __expf(sm.G[r][c] - sm.G[i][c]);
-                const float ke = sm.K[i][c] * e;
-                akk += sm.K[r][c] * ke;
-                aqk += sm.Q[r][c] * ke;
+        // ---- the Gram factors around the midpoint Gamma_15 ----
+        for (int idx = t; idx < C * DK; idx += kThreads) {
+            const int r = idx / DK, c = idx % DK;
+            const float d1 = sm.G[r][c] - sm.G[15][c];
+            const float e = __expf(d1), kv = sm.K[r][c];
+            sm.K[r][c] = kv * e;                // k e^{Gamma - Gamma_15}
+            sm.Q[r][c] *= e;                    // q e^{Gamma - Gamma_15}
+            sm.B1[r][c] = kv * __expf(-d1);     // k e^{Gamma_15 - Gamma}
+        }
+        if (t < DK) {
+            sm.e15[t] = __expf(sm.G[15][t]);
+            sm.eC15[t] = __expf(sm.glast[t] - sm.G[15][t]);
+        }
+        __syncthreads();
+
+        // ---- Gram matrices Akk = diag(beta) tril_s(K1 B1^T) on threads 0-127 and
+        // Aqk = tril(Q1 B1^T) on 128-255: lane i takes column i, each thread 8 rows
+        // (rows of B1 are four banks apart, so the column reads do not conflict) ----
+        {
+            const bool qhalf = t >= kThreads / 2;   // warp-uniform
+            const int th = t & (kThreads / 2 - 1);
+            const int i = th & 31, r8 = (th >> 5) * 8;
+            const float(*Am)[DK + 4] = qhalf ? sm.Q : sm.K;
+            float acc[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+            for (int c = 0; c < DK; c += 4) {
+                const float4 y = *reinterpret_cast<const float4 *>(&sm.B1[i][c]);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float4 x = *reinterpret_cast<const float4 *>(&Am[r8 + u][c]);
+                    acc[u] += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+                }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                akk += __shfl_xor_sync(0xffffffffu, akk, o);
-                aqk += __shfl_xor_sync(0xffffffffu, aqk, o);
-            }
-            if (lane == 0) {
-                sm.Akk[r][i] = i < r ? sm.beta[r] * akk : 0.f;
-                sm.Aqk[r][i] = aqk;
+            for (int u = 0; u < 8; ++u) {
+                const int r = r8 + u;
+                if (qhalf) sm.Aqk[r][i] = i <= r ? acc[u] : 0.f;
+                else sm.Akk[r][i] = i < r ? sm.beta[r] * acc[u] : 0.f;
             }
         }
         __syncthreads();
 
-        // ---- decay-weighted operands for the state terms ----
+        // ---- decay-weighted operands for the state terms (from the factored copies
+        // and the per-channel factors) ----
         for (int idx = t; idx < C * DK; idx += kThreads) {
             const int r = idx / DK, c = idx % DK;
-            const float gam = sm.G[r][c];
-            const float e = __expf(gam);
-            const float kv = sm.K[r][c];
-            sm.Q[r][c] *= e;
-            sm.G[r][c] = kv * e;
-            sm.K[r][c] = kv * __expf(sm.glast[c] - gam);
+            const float k1 = sm.K[r][c];
+            sm.G[r][c] = k1 * sm.e15[c];               // e^{Gamma} . k
+            sm.Q[r][c] *= sm.e15[c];                   // e^{Gamma} . q
+            sm.K[r][c] = sm.B1[r][c] * sm.eC15[c];     // e^{Gamma_last - Gamma} . k
         }
         __syncthreads();
 
@@ -184,13 +222,19 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
         }
         __syncthreads();
 
-        // ---- forward substitution: u_r = beta_r v'_r - sum_{i<r} Akk[r,i] u_i ----
+        // ---- forward substitution: u_r = beta_r v'_r - sum_{i<r} Akk[r,i] u_i, the
+        // column of lane j held in registers ----
         if (warp == 0) {
+            float u[C];
+#pragma unroll
             for (int r = 0; r < C; ++r) {
                 float acc = sm.beta[r] * sm.U[r][lane];
-                for (int i = 0; i < r; ++i) acc -= sm.Akk[r][i] * sm.U[i][lane];
-                sm.U[r][lane] = acc;
+#pragma unroll
+                for (int i = 0; i < r; ++i) acc -= sm.Akk[r][i] * u[i];
+                u[r] = acc;
             }
+#pragma unroll
+            for (int r = 0; r < C; ++r) sm.U[r][lane] = u[r];
         }
         __syncthreads();
 
