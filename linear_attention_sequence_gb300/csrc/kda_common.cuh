@@ -64,6 +64,34 @@ constexpr float kGMin = -5.f;
 __device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float gate_g(float z, float scale) { return kGMin * sigmoid_f(scale * z); }
 
+// Longest-first order of the sequences of a packed batch: the sequence that the
+// CTAs of scheduling slot `slot` process.  Slots are launched in order, so the
+// longest sequences start first and the shortest fill in at the end.  Each
+// thread of the block ranks one sequence (by descending length, ties by index)
+// and the one ranked `slot` answers through `*answer` (shared memory).  A batch
+// of equal lengths (cu == nullptr) or of more sequences than threads keeps the
+// given order.  Every thread of the block must call it.
+__device__ __forceinline__ int longest_first(const int32_t *cu, int N, int64_t total,
+                                             int64_t seq_len, int slot, int *answer) {
+    if (!cu || N > (int)blockDim.x) return slot;
+    const int m = threadIdx.x;
+    if (m < N) {
+        int64_t a, b;
+        seq_bounds(cu, m, total, seq_len, a, b);
+        const int64_t len = b - a;
+        int rank = 0;
+        for (int m2 = 0; m2 < N; ++m2) {
+            int64_t a2, b2;
+            seq_bounds(cu, m2, total, seq_len, a2, b2);
+            const int64_t len2 = b2 - a2;
+            rank += (len2 > len || (len2 == len && m2 < m)) ? 1 : 0;
+        }
+        if (rank == slot) *answer = m;
+    }
+    __syncthreads();
+    return *answer;
+}
+
 // Row of the first checkpoint of sequence n: the checkpoints of the earlier
 // sequences come first, floor(length / interval) of them each.
 __device__ __forceinline__ int64_t ckpt_first_row(const int32_t *cu, int n, int64_t total,

@@ -55,6 +55,7 @@ struct Smem {
     float Aqk[C][C + 1];
     float beta[C];
     float glast[DK];   // Gamma of the last row
+    int seq_of_slot;   // the sequence this CTA runs (longest first)
 };
 
 template <int DK, int C, typename IN_T, typename OUT_T>
@@ -71,7 +72,9 @@ kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<DK, C> &sm = *reinterpret_cast<Smem<DK, C> *>(smem_raw);
 
-    const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int vb = blockIdx.x, h = blockIdx.y;
+    const int n = kda::longest_first(cu, (int)gridDim.z, total, seq_len, blockIdx.z,
+                                     &sm.seq_of_slot);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int j0 = vb * BV;
 

@@ -142,6 +142,7 @@ struct alignas(1024) TcSmem {
     uint32_t tma_awaited[2];
     uint32_t tmem_base;
     int abort;
+    int seq_of_slot;            // the sequence this CTA runs (longest first)
 };
 
 // Stores into K-major SW128 operand blocks (plain C++ stores, so the
@@ -826,7 +827,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
 
     const int t = threadIdx.x, warp = t >> 5;
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int h = blockIdx.x % H;
+    const int n = kda::longest_first(cu, (int)(gridDim.x / H), total, seq_len, blockIdx.x / H,
+                                     &sm.seq_of_slot);
     int64_t a, b;
     kda::seq_bounds(cu, n, total, seq_len, a, b);
     const int nchunks = (int)((b - a + C - 1) / C);
