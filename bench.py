@@ -42,6 +42,11 @@ GATED_BYTES_PER_TOKEN = 5 * 96 * 128 * 2 + 96 * 4  # 123264
 OGATED_BYTES_PER_TOKEN = 147840 + 96 * 128 * 2  # 172416
 # the scalar-decay call (Gated DeltaNet) reads one fp32 log-decay per (token, head) instead of g
 SDECAY_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 2 * 96 * 4  # 99072
+# the q, k, v prologue (ShortConv, Swish, L2Norm): three bf16 projections read and
+# three bf16 results written per (token, head, channel); its fp32 conv weights
+# [3, 96, 128, 4] are read once per launch
+PROLOGUE_BYTES_PER_TOKEN = 6 * 96 * 128 * 2  # 147456
+PROLOGUE_WEIGHT_BYTES = 3 * 96 * 128 * 4 * 4  # 589824
 # the end-to-end leg streams the layer from host memory in this many segments
 E2E_SEGMENTS = 4
 # backward: algorithmic fp32 flops per (chunk, head) of the chunked backward (C = 32,
@@ -419,6 +424,34 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": SDECAY_BYTES_PER_TOKEN * T}}
     del gh
 
+    # ---------------- the q, k, v prologue of the same layer ----------------
+    pj = synth.qkv_projections(T, w.heads, w.d, dtype=w.dtype, seed=89, device=dev)
+    pq, pk, pv = (torch.empty_like(pj["x_q"]) for _ in range(3))
+
+    def prologue_step():
+        kda.kda_qkv_prologue(pj["x_q"], pj["x_k"], pj["x_v"], pj["conv_weight"],
+                             cu_seqlens=inp["cu_seqlens"], q=pq, k=pk, v=pv,
+                             return_conv_state=False, stream=stream)
+
+    ms_pr, _, _ = time_steps(prologue_step, ck_steps, max(args.warmup, 3), world, stream)
+    pr_bytes = PROLOGUE_BYTES_PER_TOKEN * T + PROLOGUE_WEIGHT_BYTES
+    pr_ach = pr_bytes / (ms_pr * 1e-3) / 1e9
+    qkv_prologue = {
+        "value": T * world / (ms_pr * 1e-3), "unit": UNIT, "ms_per_step": ms_pr,
+        "steps": ck_steps,
+        "config": {"workload": "prefill_8k shapes: projections x_q, x_k, x_v ~ N(0, 1) bf16 "
+                               "[8192, 96, 128], conv weights ~ U(-1/2, 1/2) fp32, no carried "
+                               "state; bf16 q, k, v out"},
+        "roofline": {"bound": "hbm", "achieved": pr_ach, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": pr_ach / hbm_gbs, "peak_source": peak_src,
+                     "kernel": "kda_qkv_prologue_kernel",
+                     "traffic": profiled_traffic(
+                         "kda_qkv_prologue_kernel",
+                         "linear_attention_sequence_gb300/csrc/kda_qkv_prologue.cu",
+                         "prologue_8k"),
+                     "algorithmic_bytes_per_launch": pr_bytes}}
+    del pj, pq, pk, pv
+
     # ---------------- the backward pass (gradients of the same layer) ----------------
     gen = torch.Generator(device=dev).manual_seed(87)
     d_out = torch.randn((T, w.heads, w.d), generator=gen, device=dev).to(w.dtype)
@@ -552,7 +585,7 @@ def run_gpu(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
             "checkpointed": checkpointed, "gated": gated, "output_gated": output_gated,
-            "scalar_decay": scalar_decay, "backward": backward,
+            "scalar_decay": scalar_decay, "backward": backward, "qkv_prologue": qkv_prologue,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -577,6 +610,14 @@ def run_profile_case(args, kda, synth, dev, stream):
             kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
                             cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
                             variant=args.variant, stream=stream)
+        units = args.tokens
+    elif args.profile == "prologue":
+        w = synth.WORKLOADS["prefill_8k"]
+        pj = synth.qkv_projections(args.tokens, w.heads, w.d, dtype=w.dtype, seed=89, device=dev)
+
+        def step():
+            kda.kda_qkv_prologue(pj["x_q"], pj["x_k"], pj["x_v"], pj["conv_weight"],
+                                 return_conv_state=False, stream=stream)
         units = args.tokens
     elif args.profile == "backward":
         w = synth.WORKLOADS["prefill_8k"]
@@ -613,7 +654,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward", "prologue"],
+                    default=None,
                     help="run only one kernel family on a reduced case (for ncu)")
     ap.add_argument("--tokens", type=int, default=2048, help="--profile prefill: tokens")
     ap.add_argument("--seqs", type=int, default=64, help="--profile decode: sequences")

@@ -230,6 +230,55 @@ kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_log
                            const float *norm_weight, float eps, kda_stream_t stream);
 
 /*
+ * kda_qkv_prologue -- q, k and v from their projections: for every stream
+ * (q, k, v), token t, head h and channel j,
+ *
+ *   c[t,h,j] = sum_{i=0..3} w[s,h,j,3-i] * x_s[t-i,h,j]
+ *   y        = c * Sigmoid(c)                                  (Swish)
+ *   q, k     = y / sqrt(sum_j y[t,h,j]^2 + eps)                 v = y
+ *
+ * The pages define q, k = L2Norm(Swish(ShortConv(W x))) and v =
+ * Swish(ShortConv(W_v x)) ("Understanding Kimi K3's Attention", symbol
+ * table), with a convolution of width 4 ("Inside Kimi K3", section "Sequence
+ * mixing: fixed-state KDA alongside global MLA") that is causal ("Hybrid
+ * Attention", section "KDA: don't write the same information twice").
+ * Here it is a per-channel convolution over the tokens of one sequence, with
+ * no bias, and L2Norm is taken over one head's d channels with eps inside
+ * the root.  The projections W x stay with the caller.
+ *
+ *   dims        num_seqs N, total_tokens T, num_heads H, d_k = d_v = d (64 or
+ *               128); in_dtype is the type of x_*, out_dtype that of q, k, v;
+ *               variant is not used.
+ *   x_q, x_k, x_v  device, in_dtype, [T, H, d]: the projections.
+ *   conv_weight device fp32 [3, H, d, 4], 16-byte aligned: streams q, k, v;
+ *               tap 3 multiplies the current token, tap 3-i the token i places
+ *               earlier.
+ *   conv_state_in  device fp32 [N, 3, 3, H, d] or NULL (zeros): for each
+ *               sequence and stream, the three inputs before its first token,
+ *               entry 0 the oldest.  Aligned to d/32 floats.
+ *   cu_seqlens  device int32 [N+1] as in kda_prefill, or NULL (N equal
+ *               sequences).  The convolution restarts at every sequence start.
+ *   q, k, v     device, out_dtype, [T, H, d]: written.
+ *   conv_state_out device fp32 [N, 3, 3, H, d] or NULL: the last three inputs
+ *               of each sequence, entry 0 the oldest (taken from
+ *               conv_state_in, or 0, where a sequence is shorter than three).
+ *               This is the conv_state_in of the next segment: a decode step
+ *               is a call with one token per sequence.
+ *   eps         finite, > 0.
+ *
+ * x_* and q, k, v must be aligned to d/32 elements.  No output may overlap an
+ * input or another output (the two conv states included); alternate two state
+ * buffers between calls.  KDA_ERR_INVALID_ARGUMENT for a bad dims, a bad eps,
+ * a NULL or misaligned pointer that is needed, or an overlap;
+ * KDA_ERR_UNSUPPORTED for d other than 64 or 128, or sizes beyond one grid.
+ */
+kda_status kda_qkv_prologue(const kda_dims *dims, const void *x_q, const void *x_k,
+                            const void *x_v, const float *conv_weight,
+                            const float *conv_state_in, const int32_t *cu_seqlens, void *q,
+                            void *k, void *v, float *conv_state_out, float eps,
+                            kda_stream_t stream);
+
+/*
  * kda_prefill_scalar_decay -- the same chunked prefill for the two special
  * cases of the recurrence the pages build KDA from ("Kimi K3.1 and the Road
  * From Softmax Attention to Kimi Delta Attention", sections "3. The delta

@@ -13,6 +13,7 @@ method and has no fallback: if the library is missing, every call raises.
     kda_prefill_scalar_decay(q, k, v, g_head, beta, ...)   Gated DeltaNet / the delta rule
     kda_backward(q, k, v, g, beta, d_out, ...)   gradients of kda_prefill
     kda_output_gate(out, gate_logit, ...)   the output gate alone, in place
+    kda_qkv_prologue(x_q, x_k, x_v, conv_weight, ...)   ShortConv, Swish, L2Norm -> q, k, v
     kda_decode(q, k, v, g, beta, state) one-token in-place state update
 """
 from __future__ import annotations
@@ -24,7 +25,8 @@ import torch
 
 __all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
            "kda_prefill_output_gated", "kda_prefill_scalar_decay", "kda_backward",
-           "kda_output_gate", "checkpoint_count", "kda_decode", "kda_status_string", "lib", "library_path",
+           "kda_output_gate", "kda_qkv_prologue", "checkpoint_count", "kda_decode",
+           "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
            "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "Dims"]
 
@@ -88,6 +90,9 @@ def lib():
         L.kda_backward.restype = ctypes.c_int
         L.kda_output_gate.argtypes = [ctypes.POINTER(Dims), vp, vp, fp, ctypes.c_float, vp]
         L.kda_output_gate.restype = ctypes.c_int
+        L.kda_qkv_prologue.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, vp, vp, vp,
+                                       vp, fp, ctypes.c_float, vp]
+        L.kda_qkv_prologue.restype = ctypes.c_int
         L.kda_decode.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp]
         L.kda_decode.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -348,6 +353,62 @@ def kda_output_gate(out, gate_logit, norm_weight=None, eps=1e-6, stream=None):
                                  _ptr(norm_weight), ctypes.c_float(eps), _stream(stream)),
            "kda_output_gate")
     return out
+
+
+def kda_qkv_prologue(x_q, x_k, x_v, conv_weight, cu_seqlens=None, conv_state=None, *,
+                     num_seqs=None, eps=1e-6, out_dtype=None, q=None, k=None, v=None,
+                     conv_state_out=None, return_conv_state=True, stream=None):
+    """q, k, v from their projections (C entry point ``kda_qkv_prologue``):
+    per channel the causal width-4 convolution over each sequence, Swish, and
+    for q and k the L2 normalisation over the head's d channels.
+
+    x_q, x_k, x_v [T, H, d] fp32 or bf16 (one dtype); conv_weight fp32
+    [3, H, d, 4] (streams q, k, v; tap 3 on the current token); cu_seqlens
+    int32 [N+1] or None (``num_seqs`` equal sequences, default 1); conv_state
+    fp32 [N, 3, 3, H, d] or None (zeros).  Returns ``(q, k, v, conv_state_out)``
+    (the last, fp32 [N, 3, 3, H, d], is None unless ``return_conv_state`` or
+    a buffer is given)."""
+    for t, n in ((x_q, "x_q"), (x_k, "x_k"), (x_v, "x_v")):
+        _require(t, n, ndim=3)
+    _require(conv_weight, "conv_weight", torch.float32, 4)
+    _require(conv_state, "conv_state", torch.float32, 5)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    if x_q.dtype not in _DTYPES or x_k.dtype != x_q.dtype or x_v.dtype != x_q.dtype:
+        raise ValueError("x_q, x_k, x_v must share one dtype, fp32 or bf16")
+    if x_k.shape != x_q.shape or x_v.shape != x_q.shape:
+        raise ValueError("x_q, x_k, x_v must have one shape [T, H, d]")
+    T, H, d = x_q.shape
+    if conv_weight.shape != (3, H, d, 4):
+        raise ValueError("conv_weight must be [3, H, d, 4]")
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    if conv_state is not None and conv_state.shape != (N, 3, 3, H, d):
+        raise ValueError("conv_state must be [N, 3, 3, H, d]")
+    odt = x_q.dtype if out_dtype is None else out_dtype
+    if odt not in _DTYPES:
+        raise ValueError("out_dtype must be fp32 or bf16")
+    outs = []
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t is None:
+            t = torch.empty((T, H, d), dtype=odt, device=x_q.device)
+        _require(t, n, odt, 3)
+        if t.shape != (T, H, d):
+            raise ValueError(f"{n} must be [T, H, d]")
+        outs.append(t)
+    if conv_state_out is None and return_conv_state:
+        conv_state_out = torch.empty((N, 3, 3, H, d), dtype=torch.float32, device=x_q.device)
+    _require(conv_state_out, "conv_state_out", torch.float32, 5)
+    if conv_state_out is not None and conv_state_out.shape != (N, 3, 3, H, d):
+        raise ValueError("conv_state_out must be [N, 3, 3, H, d]")
+    dims = Dims(N, T, H, d, d, _DTYPES[x_q.dtype], _DTYPES[odt], 0)
+    _check(lib().kda_qkv_prologue(ctypes.byref(dims), _ptr(x_q), _ptr(x_k), _ptr(x_v),
+                                  _ptr(conv_weight), _ptr(conv_state), _ptr(cu_seqlens),
+                                  _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]),
+                                  _ptr(conv_state_out), ctypes.c_float(eps), _stream(stream)),
+           "kda_qkv_prologue")
+    return outs[0], outs[1], outs[2], conv_state_out
 
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,

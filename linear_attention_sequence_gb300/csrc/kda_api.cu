@@ -1,6 +1,7 @@
 // kda_api.cu -- the C ABI front end: argument validation, kernel selection,
 // launch and error mapping.  Declarations and semantics: include/kda.h.
 
+#include <initializer_list>
 #include <math.h>
 #include <stdio.h>
 #include <string.h>
@@ -270,6 +271,71 @@ kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, cons
                                         chunk_capacity, d_out, d_final_state, dq, dk, dv, dg,
                                         dbeta, d_init_state, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kda_backward");
+    return KDA_OK;
+}
+
+namespace {
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const char *x = (const char *)a, *y = (const char *)b;
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+kda_status kda_qkv_prologue(const kda_dims *dims, const void *x_q, const void *x_k,
+                            const void *x_v, const float *conv_weight,
+                            const float *conv_state_in, const int32_t *cu_seqlens, void *q,
+                            void *k, void *v, float *conv_state_out, float eps,
+                            kda_stream_t stream) {
+    kda::Problem P;
+    kda_status st = check_dims(dims, P);
+    if (st != KDA_OK) return st;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens) {
+        if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
+        P.seq_len = P.N ? P.T / P.N : 0;
+    }
+    if (P.N == 0 && P.T == 0) return KDA_OK;
+    if (P.T > 0 && (!conv_weight || !x_q || !x_k || !x_v || !q || !k || !v))
+        return KDA_ERR_INVALID_ARGUMENT;
+    // vector accesses: a lane moves d/32 consecutive elements of a row
+    const int per = P.dk / 32;
+    const uintptr_t in_al = (uintptr_t)per * (P.in_dtype == KDA_DTYPE_BF16 ? 2 : 4) - 1;
+    const uintptr_t out_al = (uintptr_t)per * (P.out_dtype == KDA_DTYPE_BF16 ? 2 : 4) - 1;
+    const uintptr_t st_al = (uintptr_t)per * 4 - 1;
+    for (const void *p : {x_q, x_k, x_v})
+        if ((uintptr_t)p & in_al) return KDA_ERR_INVALID_ARGUMENT;
+    for (const void *p : {(const void *)q, (const void *)k, (const void *)v})
+        if ((uintptr_t)p & out_al) return KDA_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)conv_weight & 15u) || ((uintptr_t)conv_state_in & st_al) ||
+        ((uintptr_t)conv_state_out & 3u))
+        return KDA_ERR_INVALID_ARGUMENT;
+    // no output may overlap an input (neighbouring tiles read each other's rows)
+    const size_t row_elems = (size_t)P.T * P.H * P.dk;
+    const size_t in_b = row_elems * (P.in_dtype == KDA_DTYPE_BF16 ? 2 : 4);
+    const size_t out_b = row_elems * (P.out_dtype == KDA_DTYPE_BF16 ? 2 : 4);
+    const size_t w_b = (size_t)3 * P.H * P.dk * 4 * sizeof(float);
+    const size_t st_b = (size_t)P.N * 9 * P.H * P.dk * sizeof(float);
+    const void *ins[] = {x_q, x_k, x_v, conv_weight, conv_state_in};
+    const size_t in_sz[] = {in_b, in_b, in_b, w_b, conv_state_in ? st_b : 0};
+    const void *outs[] = {q, k, v, conv_state_out};
+    const size_t out_sz[] = {out_b, out_b, out_b, conv_state_out ? st_b : 0};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return KDA_ERR_INVALID_ARGUMENT;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlaps(outs[o], out_sz[o], outs[o2], out_sz[o2])) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    // grid sizes (16 tokens x one (stream, head) per warp, 4 warps a block)
+    const int64_t blocks = ((int64_t)P.T + 15) / 16 * 3 * P.H / 4 + 1;
+    const int64_t st_blocks = ((int64_t)P.N * 9 * P.H * P.dk + 255) / 256;
+    if (blocks > INT32_MAX || st_blocks > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    cudaError_t e = kda_launch_qkv_prologue(P, x_q, x_k, x_v, conv_weight, conv_state_in,
+                                            cu_seqlens, q, k, v, conv_state_out, eps,
+                                            (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_qkv_prologue");
     return KDA_OK;
 }
 

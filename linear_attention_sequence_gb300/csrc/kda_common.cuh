@@ -126,6 +126,10 @@ cudaError_t kda_launch_backward(const kda::Problem &P, const void *q, const void
                                 const void *d_out, const float *d_final, void *dq, void *dk,
                                 void *dv, float *dg, float *dbeta, float *d_init,
                                 cudaStream_t stream);
+cudaError_t kda_launch_qkv_prologue(const kda::Problem &P, const void *xq, const void *xk,
+                                    const void *xv, const float *w, const float *cin,
+                                    const int32_t *cu, void *q, void *k, void *v, float *cout,
+                                    float eps, cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
 cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,

@@ -166,3 +166,19 @@ def scalar_decay(T, H, mu=2.0, seed=0, device="cpu"):
     gen = _gen(seed, device)
     x = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32) + mu
     return torch.clamp(torch.nn.functional.logsigmoid(x), min=-5.0)
+
+
+def qkv_projections(T, H, d, N=1, dtype=torch.float32, seed=0, device="cpu"):
+    """Inputs of the q, k, v prologue: the projections W_{q,k,v} x_t ~ N(0, 1)
+    per (token, head, channel) in the activation dtype; conv weights
+    ~ U(-1/2, 1/2) (the usual fan-in bound 1/sqrt(width) of a width-4
+    depthwise convolution), fp32 [3, H, d, 4]; a carried conv state
+    ~ N(0, 1), fp32 [N, 3, 3, H, d], rounded through the activation dtype (it
+    holds earlier inputs)."""
+    gen = _gen(seed, device)
+    xs = [torch.randn((T, H, d), generator=gen, device=device, dtype=torch.float32).to(dtype)
+          for _ in range(3)]
+    w = torch.rand((3, H, d, 4), generator=gen, device=device, dtype=torch.float32) - 0.5
+    state = torch.randn((N, 3, 3, H, d), generator=gen, device=device,
+                        dtype=torch.float32).to(dtype).float()
+    return dict(x_q=xs[0], x_k=xs[1], x_v=xs[2], conv_weight=w, conv_state=state)

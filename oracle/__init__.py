@@ -63,6 +63,9 @@ class Oracle:
         lib.kda_oracle_gate.argtypes = [i32, i32, i32, dp, dp, dp, dp, dp]
         lib.kda_oracle_output_gate.argtypes = [i32, i32, i32, dp, dp, dp, ctypes.c_double, dp]
         lib.kda_oracle_gate.restype = ctypes.c_int
+        lib.kda_oracle_qkv_prologue.argtypes = [i32, i32, i32, i32, ip, dp, dp, dp,
+                                                ctypes.c_double, dp, dp]
+        lib.kda_oracle_qkv_prologue.restype = ctypes.c_int
         self.lib = lib
 
     def num_cpus(self) -> int:
@@ -167,6 +170,32 @@ class Oracle:
             raise ValueError("kda_oracle_output_gate rejected its arguments (eps must be > 0)")
         return y
 
+    def qkv_prologue(self, x_q, x_k, x_v, conv_weight, cu_seqlens=None, conv_state=None,
+                     eps: float = 1e-6):
+        """q, k, v from their projections: per channel the causal width-4
+        convolution over each sequence, Swish, and for q and k the L2
+        normalisation over the head's d channels (C function
+        ``kda_oracle_qkv_prologue``).  x_* [T, H, d]; conv_weight [3, H, d, 4]
+        (streams q, k, v; tap 3 on the current token); cu_seqlens int32 [N+1]
+        or None (one sequence); conv_state [N, 3, 3, H, d] or None (zeros).
+        Returns (q, k, v, conv_state_out), fp64."""
+        x = _f64(np.stack([_f64(x_q), _f64(x_k), _f64(x_v)]))
+        w = _f64(conv_weight)
+        _, T, H, d = x.shape
+        cu = (np.array([0, T], np.int32) if cu_seqlens is None
+              else np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32)))
+        N = cu.shape[0] - 1
+        assert w.shape == (3, H, d, 4)
+        cs = _f64(conv_state)
+        assert cs is None or cs.shape == (N, 3, 3, H, d)
+        y = np.empty_like(x)
+        cout = np.empty((N, 3, 3, H, d))
+        rc = self.lib.kda_oracle_qkv_prologue(N, T, H, d, _ptr(cu, ctypes.c_int32), _ptr(x),
+                                              _ptr(w), _ptr(cs), float(eps), _ptr(y), _ptr(cout))
+        if rc != 0:
+            raise ValueError("kda_oracle_qkv_prologue rejected its arguments")
+        return y[0], y[1], y[2], cout
+
     def decode(self, q, k, v, g, beta, state, num_threads: int = 0, inplace: bool = False):
         """One decode step for N sequences: q, k, g [N, H, d_k]; v [N, H, d_v];
         beta [N, H]; state [N, H, d_k, d_v].  Returns (out, new_state), fp64.
@@ -232,6 +261,10 @@ def gate(*args, **kwargs):
 
 def output_gate(*args, **kwargs):
     return _load().output_gate(*args, **kwargs)
+
+
+def qkv_prologue(*args, **kwargs):
+    return _load().qkv_prologue(*args, **kwargs)
 
 
 def decode(*args, **kwargs):

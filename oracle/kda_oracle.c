@@ -457,6 +457,69 @@ int kda_oracle_output_gate(int32_t total_tokens, int32_t num_heads, int32_t d_v,
     return 0;
 }
 
+/*
+ * The q, k, v prologue ("Understanding Kimi K3's Attention", symbol table:
+ * q, k = L2Norm(Swish(ShortConv(W x))), v = Swish(ShortConv(W_v x)); "Inside
+ * Kimi K3", section "Sequence mixing": the convolution has width 4; "Hybrid
+ * Attention", section "KDA: don't write the same information twice": it is
+ * causal).  Read as a per-channel causal convolution over the tokens of one
+ * sequence, no bias, followed by Swish(c) = c Sigmoid(c), and for q and k a
+ * division by sqrt(sum of squares over the head's channels + eps).
+ *
+ * Stream s = 0, 1, 2 is q, k, v.  x, y: [3][T][H][d]; conv_weight:
+ * [3][H][d][4], tap 3 on the current token, tap 3 - i on the token i places
+ * earlier.  conv_state_in / conv_state_out: [N][3][3][H][d], the three
+ * inputs before a sequence's first token (entry 0 the oldest) and the last
+ * three inputs of the sequence; a NULL state in reads as zeros.
+ */
+int kda_oracle_qkv_prologue(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                            int32_t d, const int32_t *cu_seqlens, const double *x,
+                            const double *conv_weight, const double *conv_state_in, double eps,
+                            double *y, double *conv_state_out) {
+    if (num_seqs < 0 || total_tokens < 0 || num_heads < 1 || d < 1 || !(eps > 0.0) ||
+        !cu_seqlens || !conv_weight || (total_tokens > 0 && (!x || !y)))
+        return -1;
+    if (cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != total_tokens) return -1;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    const int64_t H = num_heads, D = d, T = total_tokens;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        const int64_t a = cu_seqlens[n], b = cu_seqlens[n + 1];
+        for (int s = 0; s < 3; ++s) {
+            /* input of stream s at token u of this sequence, head h, channel j */
+#define XIN(u, h, j)                                                                        \
+    ((u) >= a ? x[((s * T + (u)) * H + (h)) * D + (j)]                                      \
+              : (conv_state_in                                                              \
+                     ? conv_state_in[((((int64_t)n * 3 + s) * 3 + ((u) - a + 3)) * H + (h)) * D + (j)] \
+                     : 0.0))
+            for (int64_t t = a; t < b; ++t)
+                for (int64_t h = 0; h < H; ++h) {
+                    double *row = y + ((s * T + t) * H + h) * D;
+                    for (int64_t j = 0; j < D; ++j) {
+                        const double *w = conv_weight + ((s * H + h) * D + j) * 4;
+                        double c = 0.0;
+                        for (int i = 0; i < 4; ++i) c += w[3 - i] * XIN(t - i, h, j);
+                        row[j] = c * sigmoid(c);
+                    }
+                    if (s < 2) {
+                        double ss = 0.0;
+                        for (int64_t j = 0; j < D; ++j) ss += row[j] * row[j];
+                        const double inv = 1.0 / sqrt(ss + eps);
+                        for (int64_t j = 0; j < D; ++j) row[j] *= inv;
+                    }
+                }
+            if (conv_state_out)
+                for (int p = 0; p < 3; ++p)
+                    for (int64_t h = 0; h < H; ++h)
+                        for (int64_t j = 0; j < D; ++j)
+                            conv_state_out[((((int64_t)n * 3 + s) * 3 + p) * H + h) * D + j] =
+                                XIN(b - 3 + p, h, j);
+#undef XIN
+        }
+    }
+    return 0;
+}
+
 int kda_oracle_decode(int32_t num_seqs, int32_t num_heads, int32_t d_k, int32_t d_v,
                       const double *q, const double *k, const double *v,
                       const double *g, const double *beta, double *state_inout,

@@ -67,6 +67,19 @@ int kda_oracle_output_gate(int32_t total_tokens, int32_t num_heads, int32_t d_v,
                            const double *o, const double *gate_logit,
                            const double *norm_weight, double eps, double *y);
 
+/* q, k, v prologue: per channel, the causal width-4 convolution over the
+ * tokens of each sequence (the three inputs before a sequence's start come
+ * from conv_state_in, or are 0 if it is NULL), then Swish(c) = c Sigmoid(c),
+ * then for q and k (streams 0, 1; v is stream 2) division by sqrt(sum over
+ * the head's d channels of the square + eps).  x, y [3][T][H][d]; conv_weight
+ * [3][H][d][4] (tap 3 on the current token); conv states [N][3][3][H][d]
+ * (entry 0 the oldest); conv_state_out may be NULL.  cu_seqlens [N+1] is
+ * required.  Returns -1 on a bad argument, else 0. */
+int kda_oracle_qkv_prologue(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                            int32_t d, const int32_t *cu_seqlens, const double *x,
+                            const double *conv_weight, const double *conv_state_in, double eps,
+                            double *y, double *conv_state_out);
+
 #ifdef __cplusplus
 }
 #endif

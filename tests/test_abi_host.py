@@ -272,6 +272,46 @@ def test_output_gate_no_rows_is_ok(L):
                              ctypes.c_float(1e-6), None) == OK
 
 
+def prologue(L, dims, **over):
+    args = dict(xq=ctypes.c_void_p(0x100000), xk=ctypes.c_void_p(0x200000),
+                xv=ctypes.c_void_p(0x300000), w=ctypes.c_void_p(0x400000), cin=None, cu=None,
+                q=ctypes.c_void_p(0x500000), k=ctypes.c_void_p(0x600000),
+                v=ctypes.c_void_p(0x700000), cout=None, eps=1e-6)
+    args.update(over)
+    d = None if dims is None else ctypes.byref(dims)
+    return L.kda_qkv_prologue(d, args["xq"], args["xk"], args["xv"], args["w"], args["cin"],
+                              args["cu"], args["q"], args["k"], args["v"], args["cout"],
+                              ctypes.c_float(args["eps"]), None)
+
+
+@pytest.mark.parametrize("dims,over,want", [
+    (None, {}, INVALID), (D(num_heads=0), {}, INVALID),
+    (D(d_k=96, d_v=96), {}, UNSUPPORTED),
+    (D(num_seqs=3), {}, INVALID),                                   # 16 tokens, 3 sequences
+    (D(), {"eps": 0.0}, INVALID), (D(), {"eps": float("nan")}, INVALID),
+    (D(), {"eps": float("inf")}, INVALID),
+    (D(), {"xk": None}, INVALID), (D(), {"v": None}, INVALID), (D(), {"w": None}, INVALID),
+    (D(), {"xk": ctypes.c_void_p(0x200004)}, INVALID),             # bf16 x 4 needs 8 bytes
+    (D(in_dtype=0), {"xk": ctypes.c_void_p(0x200008)}, INVALID),   # fp32 x 4 needs 16
+    (D(), {"q": ctypes.c_void_p(0x500002)}, INVALID),
+    (D(), {"w": ctypes.c_void_p(0x400008)}, INVALID),
+    (D(), {"cin": ctypes.c_void_p(0x800008)}, INVALID),
+    (D(), {"cout": ctypes.c_void_p(0x800002)}, INVALID),
+    (D(), {"q": ctypes.c_void_p(0x100100)}, INVALID),              # q overlaps x_q
+    (D(), {"k": ctypes.c_void_p(0x500000)}, INVALID),              # k is q
+    (D(), {"v": ctypes.c_void_p(0x400010)}, INVALID),              # v overlaps the weights
+    (D(), {"cin": ctypes.c_void_p(0x800000), "cout": ctypes.c_void_p(0x800100)}, INVALID),
+    (D(), {"cout": ctypes.c_void_p(0x300000)}, INVALID),           # state out overlaps x_v
+])
+def test_qkv_prologue_rejects(L, dims, over, want):
+    assert prologue(L, dims, **over) == want
+
+
+def test_qkv_prologue_empty_batch_is_ok(L):
+    assert prologue(L, D(num_seqs=0, total_tokens=0), xq=None, xk=None, xv=None, w=None,
+                    q=None, k=None, v=None) == OK
+
+
 def test_checkpoint_count():
     cu = torch.tensor([0, 100, 164, 164, 364], dtype=torch.int32)
     assert kda.checkpoint_count(364, 32, cu) == 3 + 2 + 0 + 6

@@ -361,10 +361,106 @@ def pin_backward_beta_zero_closed_form(orc):
     assert np.all(r["dk"] == 0.0) and np.all(r["dv"] == 0.0)
 
 
+def _conv_ref(x_seq, state, w):
+    """Causal width-4 convolution of one channel's inputs by numpy's own
+    convolution: the three carried inputs first, then the sequence; tap 3 of
+    w multiplies the current token, so the kernel is w reversed."""
+    full = np.concatenate([state, x_seq])
+    return np.convolve(full, w[::-1])[3:3 + len(x_seq)]
+
+
+def pin_qkv_prologue_convolution(orc):
+    """The short convolution ("Inside Kimi K3", section "Sequence mixing":
+    width 4; "Hybrid Attention", section "KDA: don't write the same
+    information twice": causal), seen through the value stream.  Since
+    Swish(c) - Swish(-c) = c (Sigmoid(c) + Sigmoid(-c) = 1) and the
+    convolution is linear, v(x) - v(-x) is the convolution itself:
+    - an impulse at token 2 returns the taps newest first, nothing before it;
+    - a packed batch (an empty sequence included) matches numpy's
+      convolution of each sequence, restarted at each sequence start, with
+      the carried conv state in front;
+    - the state out is the last three inputs of [state; sequence]."""
+    T, H, d = 8, 1, 2
+    rng = np.random.default_rng(21)
+    w = rng.standard_normal((3, H, d, 4))
+    x = np.zeros((T, H, d))
+    x[2, 0, 0] = 1.5
+    z = np.zeros_like(x)
+    v1 = orc.qkv_prologue(z, z, x, w)[2]
+    v2 = orc.qkv_prologue(z, z, -x, w)[2]
+    c = v1 - v2
+    want = np.zeros(T)
+    want[2:6] = 1.5 * w[2, 0, 0, ::-1]
+    assert np.allclose(c[:, 0, 0], want, rtol=0, atol=1e-14)
+    assert np.all(c[:, 0, 1] == 0.0)
+    lens = [5, 0, 2, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T, H, d = int(cu[-1]), 2, 3
+    x = rng.standard_normal((T, H, d))
+    w = rng.standard_normal((3, H, d, 4))
+    st = rng.standard_normal((len(lens), 3, 3, H, d))
+    z = np.zeros_like(x)
+    for state in (None, st):
+        v1 = orc.qkv_prologue(z, z, x, w, cu_seqlens=cu, conv_state=state)
+        v2 = orc.qkv_prologue(z, z, -x, w, cu_seqlens=cu,
+                              conv_state=None if state is None else -state)
+        c = v1[2] - v2[2]
+        for n, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+            for h in range(H):
+                for j in range(d):
+                    s0 = np.zeros(3) if state is None else state[n, 2, :, h, j]
+                    assert np.allclose(c[a:b, h, j], _conv_ref(x[a:b, h, j], s0, w[2, h, j]),
+                                       rtol=1e-13, atol=1e-13)
+                    full = np.concatenate([s0, x[a:b, h, j]])
+                    assert np.array_equal(v1[3][n, 2, :, h, j], full[-3:])
+
+
+def pin_qkv_prologue_swish_norm(orc):
+    """Swish and L2Norm ("Understanding Kimi K3's Attention", symbol table:
+    q, k = L2Norm(Swish(ShortConv(.))), v = Swish(ShortConv(.))):
+    - a current-token tap of 1 and an input of ln 3 give ln 3 Sigmoid(ln 3)
+      = 0.75 ln 3 on v; an input of 0 gives 0 on every stream;
+    - q is v's row, computed from q's own input and weights, divided by its
+      norm over the head's channels (heads of very different scale each end
+      with norm 1), and with eps = 3 |v|^2 by 2 |v|; the same for k;
+    - v is not normalised."""
+    T, H, d = 3, 2, 4
+    w = np.zeros((3, H, d, 4))
+    w[..., 3] = 1.0
+    x = np.full((T, H, d), np.log(3.0))
+    z = np.zeros_like(x)
+    q, k, v, _ = orc.qkv_prologue(z, z, x, w)
+    assert np.allclose(v, 0.75 * np.log(3.0), rtol=1e-15, atol=0)
+    assert np.all(q == 0.0) and np.all(k == 0.0)
+    rng = np.random.default_rng(22)
+    T, H, d = 6, 3, 5
+    xs = [rng.standard_normal((T, H, d)) * np.array([1e-3, 1.0, 30.0])[None, :, None]
+          for _ in range(3)]
+    w = rng.standard_normal((3, H, d, 4))
+    q, k, v, _ = orc.qkv_prologue(*xs, w, eps=1e-30)
+    assert not np.allclose(np.linalg.norm(v, axis=-1), 1.0)
+    for s, got in ((0, q), (1, k)):
+        w2 = w.copy()
+        w2[2] = w[s]
+        ref = orc.qkv_prologue(np.zeros((T, H, d)), xs[1], xs[s], w2, eps=1e-30)[2]
+        nrm = np.linalg.norm(ref, axis=-1, keepdims=True)
+        assert np.allclose(got, ref / nrm, rtol=1e-12, atol=0)
+        big = orc.qkv_prologue(*xs, w, eps=1.0)[s]
+        assert np.allclose(big, ref / np.sqrt(nrm ** 2 + 1.0), rtol=1e-12, atol=0)
+    one = [xs[0][:, :1], xs[1][:, :1], xs[2][:, :1]]
+    vv = orc.qkv_prologue(*one, w[:, :1], eps=1e-30)[2]
+    w2 = w[:, :1].copy()
+    w2[0] = w2[2]
+    e3 = 3.0 * float((vv[0, 0] ** 2).sum())
+    qq = orc.qkv_prologue(one[2], one[1], one[2], w2, eps=e3)[0]
+    assert np.allclose(qq[0, 0], vv[0, 0] / (2.0 * np.sqrt(e3 / 3.0)), rtol=1e-12, atol=0)
+
+
 PINS = [pin_worked_example, pin_beta_one_reads_back_v, pin_beta_zero_closed_form,
         pin_toy_memory, pin_brute_force, pin_gradient_step, pin_norm_bound,
         pin_gate_closed_forms, pin_output_gate_closed_forms, pin_scalar_decay_closed_forms,
-        pin_backward_finite_differences, pin_backward_beta_zero_closed_form]
+        pin_backward_finite_differences, pin_backward_beta_zero_closed_form,
+        pin_qkv_prologue_convolution, pin_qkv_prologue_swish_norm]
 
 
 def _run_pin(pin, orc, golden):
@@ -496,6 +592,16 @@ MUTANTS = {
                              "const double w = 1.0;"),
     "ogate_norm_over_heads": ("            double ss = 0.0;\n            for (int32_t j = 0; j < d_v; ++j) ss += o[row + j] * o[row + j];",
                               "            double ss = 0.0;\n            for (int32_t j = 0; j < d_v; ++j) ss += o[t * num_heads * (int64_t)d_v + j] * o[t * num_heads * (int64_t)d_v + j];"),
+    "conv_taps_reversed": ("c += w[3 - i] * XIN(t - i, h, j);", "c += w[i] * XIN(t - i, h, j);"),
+    "conv_not_restarted": ("((u) >= a ? x[", "((u) >= 0 ? x["),
+    "conv_state_reversed": ("((u) - a + 3)) * H", "(a - (u) - 1)) * H"),
+    "conv_state_out_reversed": ("XIN(b - 3 + p, h, j);", "XIN(b - 1 - p, h, j);"),
+    "swish_without_gate": ("row[j] = c * sigmoid(c);", "row[j] = c;"),
+    "swish_gate_sign": ("row[j] = c * sigmoid(c);", "row[j] = c * sigmoid(-c);"),
+    "l2norm_eps_outside_root": ("const double inv = 1.0 / sqrt(ss + eps);",
+                                "const double inv = 1.0 / (sqrt(ss) + eps);"),
+    "l2norm_on_v": ("            if (s < 2) {", "            if (s < 3) {"),
+    "l2norm_not_on_k": ("            if (s < 2) {", "            if (s < 1) {"),
 }
 
 
