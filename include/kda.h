@@ -258,6 +258,7 @@ kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_log
  *               entry 0 the oldest.  Aligned to d/32 floats.
  *   cu_seqlens  device int32 [N+1] as in kda_prefill, or NULL (N equal
  *               sequences).  The convolution restarts at every sequence start.
+ *               With N = 0 the call does nothing and returns KDA_OK.
  *   q, k, v     device, out_dtype, [T, H, d]: written.
  *   conv_state_out device fp32 [N, 3, 3, H, d] or NULL: the last three inputs
  *               of each sequence, entry 0 the oldest (taken from

@@ -297,7 +297,8 @@ kda_status kda_qkv_prologue(const kda_dims *dims, const void *x_q, const void *x
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
         P.seq_len = P.N ? P.T / P.N : 0;
     }
-    if (P.N == 0 && P.T == 0) return KDA_OK;
+    // no sequence: no token belongs to one and no state is carried (as in kda_prefill)
+    if (P.N == 0) return KDA_OK;
     if (P.T > 0 && (!conv_weight || !x_q || !x_k || !x_v || !q || !k || !v))
         return KDA_ERR_INVALID_ARGUMENT;
     // vector accesses: a lane moves d/32 consecutive elements of a row

@@ -307,6 +307,12 @@ def test_qkv_prologue_rejects(L, dims, over, want):
     assert prologue(L, dims, **over) == want
 
 
+def test_qkv_prologue_no_sequences_is_ok(L):
+    # tokens but no sequence (cu_seqlens = [0]): nothing belongs to a sequence,
+    # nothing is launched, cu_seqlens is not read past its one entry
+    assert prologue(L, D(num_seqs=0, total_tokens=16), cu=ctypes.c_void_p(0x900000)) == OK
+
+
 def test_qkv_prologue_empty_batch_is_ok(L):
     assert prologue(L, D(num_seqs=0, total_tokens=0), xq=None, xk=None, xv=None, w=None,
                     q=None, k=None, v=None) == OK
