@@ -2,7 +2,8 @@
 and k) through the C ABI against the fp64 oracle: a ragged packed batch with
 empty and short sequences, both head sizes, every dtype pair, with and without
 a carried conv state; the conv state carried across calls (a decode step is a
-one-token call) bit-for-bit; the 8K-token, 96-head layer on sampled heads.
+one-token call) bit-for-bit; the 8K-token, 96-head layer on sampled heads;
+windows of the 262,144-token layer on all heads.
 
 Bounds, elementwise: the kernel computes in fp32 (four fused multiply-adds,
 one fast exponential, one division, a 128-term sum of squares and a
@@ -147,3 +148,29 @@ def test_layer_8k_sampled_heads():
     sub["conv_weight"] = p["conv_weight"][:, heads].contiguous()
     outs = (q[:, heads], k[:, heads], v[:, heads], cs[:, :, :, heads])
     check_against_oracle(sub, None, None, outs)
+
+
+def test_layer_256k_sampled_windows():
+    """The longest workload's shapes (262,144 tokens, 96 heads, bf16; 38.7 GB
+    in and out).  The convolution looks back three tokens only, so a window
+    [t0, t0 + 48) is exactly the oracle's run over that window with the three
+    inputs before it as the carried state.  Windows at the start, at a tile
+    edge, in the middle and at the end, on all heads."""
+    T, H, d = 262144, 96, 128
+    p = synth.qkv_projections(T, H, d, dtype=BF16, seed=53, device=DEV)
+    q, k, v, cs = kda.kda_qkv_prologue(p["x_q"], p["x_k"], p["x_v"], p["conv_weight"])
+    torch.cuda.synchronize()
+    for t0 in (0, 4096 * 16 + 13, 131072, T - 48):
+        t1 = t0 + 48
+        sub = {n: p[n][t0:t1] for n in ("x_q", "x_k", "x_v")}
+        sub["conv_weight"] = p["conv_weight"]
+        state = torch.zeros((1, 3, 3, H, d), device=DEV)
+        for si, n in enumerate(("x_q", "x_k", "x_v")):
+            for j in range(3):
+                u = t0 - 3 + j
+                if u >= 0:
+                    state[0, si, j] = p[n][u].float()
+        outs = (q[t0:t1], k[t0:t1], v[t0:t1], cs if t1 == T else None)
+        check_against_oracle(sub, None, state, outs)
+    del p, q, k, v, cs
+    torch.cuda.empty_cache()
