@@ -48,7 +48,7 @@ SDECAY_BYTES_PER_TOKEN = 4 * 96 * 128 * 2 + 2 * 96 * 4  # 99072
 PROLOGUE_BYTES_PER_TOKEN = 6 * 96 * 128 * 2  # 147456
 PROLOGUE_WEIGHT_BYTES = 3 * 96 * 128 * 4 * 4  # 589824
 # the end-to-end leg streams the layer from host memory in this many segments
-E2E_SEGMENTS = 4
+E2E_SEGMENTS = 8
 # backward: algorithmic fp32 flops per (chunk, head) of the chunked backward (C = 32,
 # d = 128), counted as 2 per multiply-add over the products it forms:
 #   G, P (pairwise, C(C+1)/2 pairs x 2 d)      135,168 MACs
