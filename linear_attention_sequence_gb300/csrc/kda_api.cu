@@ -20,6 +20,13 @@ kda_status cuda_fail(cudaError_t e, const char *where) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Do the byte ranges [a, a + na) and [b, b + nb) share a byte?
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const char *x = (const char *)a, *y = (const char *)b;
+    return x < y + nb && y < x + na;
+}
+
 bool valid_dtype(int32_t d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16; }
 
 // Shared checks of the dims struct.  Fills P on success.
@@ -273,16 +280,6 @@ kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, cons
     if (e != cudaSuccess) return cuda_fail(e, "kda_backward");
     return KDA_OK;
 }
-
-namespace {
-
-bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-    if (!a || !b || na == 0 || nb == 0) return false;
-    const char *x = (const char *)a, *y = (const char *)b;
-    return x < y + nb && y < x + na;
-}
-
-}  // namespace
 
 kda_status kda_qkv_prologue(const kda_dims *dims, const void *x_q, const void *x_k,
                             const void *x_v, const float *conv_weight,
