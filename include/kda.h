@@ -101,9 +101,14 @@ typedef struct {
  *               device and a decreasing pair is read as an empty sequence, so
  *               a malformed array can never cause an out-of-bounds access.
  *               An empty sequence copies init_state (or zeros) to final_state.
- *   out         device, out_dtype [T_tot, H, d_v]; must not alias any input.
+ *   out         device, out_dtype [T_tot, H, d_v].
  *   final_state device fp32 [N, H, d_k, d_v] or NULL.  May alias init_state
  *               exactly (each slice is read before it is written).
+ *
+ * No output (out, final_state, and the checkpoints of the calls below) may
+ * share a byte with an input or with another output, except final_state ==
+ * init_state: the kernels read later chunks' inputs while they write earlier
+ * outputs.  KDA_ERR_INVALID_ARGUMENT if one does.
  *
  * Accumulation is fp32; a bf16 `out` is the round-to-nearest-even of the
  * value an fp32 `out` would hold.
@@ -160,8 +165,8 @@ kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const v
  * as kda_prefill.  g never goes through memory; z costs 2 bytes per channel
  * in bf16 where g costs 4.
  *
- *   z           device, in_dtype, [T_tot, H, d_k]: the decay logits; must not
- *               alias `out`.
+ *   z           device, in_dtype, [T_tot, H, d_k]: the decay logits (an input:
+ *               must not overlap `out`).
  *   a_log       device fp32 [H]: the per-head log-scales A_h.
  *   beta_logit  device fp32 [T_tot, H].
  *
@@ -188,8 +193,8 @@ kda_status kda_prefill_gated(const kda_dims *dims, const void *q, const void *k,
  * root and an optional per-channel weight.  The projections W_g, W_o stay
  * with the caller.
  *
- *   gate_logit  device, in_dtype, [T_tot, H, d_v]: W_g x_t per head; must not
- *               alias `out`.
+ *   gate_logit  device, in_dtype, [T_tot, H, d_v]: W_g x_t per head (an input:
+ *               must not overlap `out`).
  *   norm_weight device fp32 [d_v], 4-byte aligned, or NULL (weight 1).
  *   eps         finite, > 0.
  *
@@ -218,13 +223,14 @@ kda_status kda_prefill_output_gated(const kda_dims *dims, const void *q, const v
  * wrote: kda_prefill_gated's, or kda_decode's (dims->total_tokens rows).
  *
  *   out          device, out_dtype, [T_tot, H, d_v], read and overwritten.
- *   gate_logit   device, in_dtype, [T_tot, H, d_v]; must not alias out.
+ *   gate_logit   device, in_dtype, [T_tot, H, d_v]; must not overlap out.
  *   norm_weight  device fp32 [d_v], 4-byte aligned, or NULL (weight 1).
  *   eps          finite, > 0.
  *
  * dims->num_seqs and dims->variant are not used; d_k must equal d_v as
  * everywhere.  KDA_ERR_INVALID_ARGUMENT for a bad dims, a NULL or misaligned
- * pointer while there are rows, gate_logit == out, or a bad eps.
+ * pointer while there are rows, out overlapping gate_logit or norm_weight,
+ * or a bad eps.
  */
 kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_logit,
                            const float *norm_weight, float eps, kda_stream_t stream);
@@ -327,11 +333,12 @@ kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const v
  *   dg             device fp32 [T_tot, H, d_k];  dbeta  device fp32 [T_tot, H].
  *   d_init_state   device fp32 [N, H, d_k, d_v] or NULL (not written).
  *
- * The gradients must not alias any input.  Arithmetic is fp32 on CUDA cores.
+ * No gradient may share a byte with an input or with another gradient.
+ * Arithmetic is fp32 on CUDA cores.
  * Every other argument (q, k, v, g, beta, init_state, cu_seqlens, dims) and
  * every other error is as in kda_prefill; KDA_ERR_INVALID_ARGUMENT also if
  * chunk_capacity < 0, chunk_states is NULL or misaligned where it is needed,
- * or a gradient pointer equals an input pointer.
+ * or a gradient overlaps an input or another gradient.
  */
 kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, const void *v,
                         const float *g, const float *beta, const float *init_state,
@@ -353,7 +360,10 @@ kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, cons
  *   q, k, v     device, in_dtype, [N, H, d]; g device fp32 [N, H, d_k];
  *               beta device fp32 [N, H].
  *   state_inout device fp32 [N, H, d_k, d_v], updated in place.
- *   out         device, out_dtype [N, H, d_v]; must not alias any input.
+ *   out         device, out_dtype [N, H, d_v].
+ *
+ * Neither out nor the state may share a byte with an input or with each
+ * other (KDA_ERR_INVALID_ARGUMENT).
  */
 kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const void *v,
                       const float *g, const float *beta, float *state_inout, void *out,

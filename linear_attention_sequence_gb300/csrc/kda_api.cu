@@ -27,6 +27,27 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// A buffer a call touches: its address and size in bytes (a NULL buffer is empty).
+struct Span {
+    const void *p;
+    size_t n;
+};
+
+// Does a written buffer share a byte with a read buffer or with another
+// written buffer?  The kernels read inputs (some by TMA, chunks ahead) while
+// they write outputs, so any such overlap would be a race.
+bool conflict(std::initializer_list<Span> writes, std::initializer_list<Span> reads) {
+    for (const Span *w = writes.begin(); w != writes.end(); ++w) {
+        for (const Span &r : reads)
+            if (overlaps(w->p, w->n, r.p, r.n)) return true;
+        for (const Span *w2 = w + 1; w2 != writes.end(); ++w2)
+            if (overlaps(w->p, w->n, w2->p, w2->n)) return true;
+    }
+    return false;
+}
+
+size_t esize(int32_t dtype) { return dtype == KDA_DTYPE_BF16 ? 2 : 4; }
+
 bool valid_dtype(int32_t d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16; }
 
 // Shared checks of the dims struct.  Fills P on success.
@@ -119,12 +140,24 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
         P.seq_len = P.N ? P.T / P.N : 0;
     }
-    if (P.T > 0 && out == (const void *)q) return KDA_ERR_INVALID_ARGUMENT;
-    if (final_state && init_state && final_state != init_state) {
-        // partial overlap of the two state arrays is not supported
-        const char *a = (const char *)init_state, *b = (const char *)final_state;
-        const size_t bytes = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
-        if (a < b + bytes && b < a + bytes) return KDA_ERR_INVALID_ARGUMENT;
+    {
+        // outputs against inputs; final_state may be init_state itself (each
+        // slice is read before it is written), but not overlap it otherwise
+        const size_t tk = (size_t)P.T * P.H * P.dk, tv = (size_t)P.T * P.H * P.dv;
+        const size_t sb = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
+        const size_t gb = x.scalar_decay ? (size_t)P.T * P.H * 4 : a_log ? tk * esize(P.in_dtype) : tk * 4;
+        const void *gp = x.scalar_decay ? (const void *)x.g_head : g_in;
+        const float *init_read = final_state == init_state ? nullptr : init_state;
+        if (conflict({{out, tv * esize(P.out_dtype)}, {final_state, sb},
+                      {x.ckpt_capacity > 0 ? x.ckpt : nullptr,
+                       (size_t)x.ckpt_capacity * P.H * P.dk * P.dv * sizeof(float)}},
+                     {{q, tk * esize(P.in_dtype)}, {k, tk * esize(P.in_dtype)},
+                      {v, tv * esize(P.in_dtype)}, {gp, gb}, {beta, (size_t)P.T * P.H * 4},
+                      {a_log, (size_t)P.H * 4}, {init_read, sb},
+                      {cu_seqlens, cu_seqlens ? (size_t)(P.N + 1) * 4 : 0},
+                      {x.ogate, x.ogate ? tv * esize(P.in_dtype) : 0},
+                      {x.onorm_w, x.onorm_w ? (size_t)P.dv * 4 : 0}}))
+            return KDA_ERR_INVALID_ARGUMENT;
     }
     P.z = a_log ? z : nullptr;
     P.a_log = a_log;
@@ -225,7 +258,14 @@ kda_status kda_output_gate(const kda_dims *dims, void *out, const void *gate_log
     if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARGUMENT;
     if (norm_weight && ((uintptr_t)norm_weight & 3u)) return KDA_ERR_INVALID_ARGUMENT;
     if (P.T == 0) return KDA_OK;
-    if (!out || !gate_logit || gate_logit == (const void *)out) return KDA_ERR_INVALID_ARGUMENT;
+    if (!out || !gate_logit) return KDA_ERR_INVALID_ARGUMENT;
+    {
+        const size_t tv = (size_t)P.T * P.H * P.dv;
+        if (conflict({{out, tv * esize(P.out_dtype)}},
+                     {{gate_logit, tv * esize(P.in_dtype)},
+                      {norm_weight, norm_weight ? (size_t)P.dv * 4 : 0}}))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
     const uintptr_t ga = P.in_dtype == KDA_DTYPE_BF16 ? 1u : 3u, oa = P.out_dtype == KDA_DTYPE_BF16 ? 1u : 3u;
     if (((uintptr_t)gate_logit & ga) || ((uintptr_t)out & oa)) return KDA_ERR_INVALID_ARGUMENT;
     P.ogate = gate_logit;
@@ -267,12 +307,20 @@ kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, cons
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
         P.seq_len = P.N ? P.T / P.N : 0;
     }
-    // the gradients must not overwrite what the kernel still reads
-    const void *ins[] = {q, k, v, g, beta, d_out, chunk_states, init_state, d_final_state};
-    const void *outs[] = {dq, dk, dv, dg, dbeta};
-    for (const void *o : outs)
-        for (const void *i : ins)
-            if (P.T > 0 && o && o == i) return KDA_ERR_INVALID_ARGUMENT;
+    {
+        // the gradients must not overwrite what the kernel still reads, nor each other
+        const size_t tk = (size_t)P.T * P.H * P.dk, tv = (size_t)P.T * P.H * P.dv;
+        const size_t sb = (size_t)P.N * P.H * P.dk * P.dv * sizeof(float);
+        const size_t ei = esize(P.in_dtype), eo = esize(P.out_dtype);
+        if (conflict({{dq, tk * eo}, {dk, tk * eo}, {dv, tv * eo}, {dg, tk * 4},
+                      {dbeta, (size_t)P.T * P.H * 4}, {d_init_state, sb}},
+                     {{q, tk * ei}, {k, tk * ei}, {v, tv * ei}, {g, tk * 4},
+                      {beta, (size_t)P.T * P.H * 4}, {d_out, tv * ei}, {init_state, sb},
+                      {d_final_state, sb},
+                      {chunk_states, (size_t)chunk_capacity * P.H * P.dk * P.dv * sizeof(float)},
+                      {cu_seqlens, cu_seqlens ? (size_t)(P.N + 1) * 4 : 0}}))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
     if (P.N == 0) return KDA_OK;
     cudaError_t e = kda_launch_backward(P, q, k, v, g, beta, init_state, cu_seqlens, chunk_states,
                                         chunk_capacity, d_out, d_final_state, dq, dk, dv, dg,
@@ -347,7 +395,15 @@ kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const 
     if (P.N == 0) return KDA_OK;
     if (!q || !k || !v || !g || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARGUMENT;
     if (!aligned16(state_inout)) return KDA_ERR_INVALID_ARGUMENT;  // 16-byte vector access
-    if (out == (const void *)state_inout) return KDA_ERR_INVALID_ARGUMENT;
+    {
+        // the state is updated in place; out and the state must not overlap an input or each other
+        const size_t nk = (size_t)P.N * P.H * P.dk, nv = (size_t)P.N * P.H * P.dv;
+        const size_t ei = esize(P.in_dtype);
+        if (conflict({{out, nv * esize(P.out_dtype)}, {state_inout, nk * P.dv * sizeof(float)}},
+                     {{q, nk * ei}, {k, nk * ei}, {v, nv * ei}, {g, nk * 4},
+                      {beta, (size_t)P.N * P.H * 4}}))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
     cudaError_t e = kda_launch_decode(P, q, k, v, g, beta, state_inout, out, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kda_decode");
     return KDA_OK;

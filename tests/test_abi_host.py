@@ -222,7 +222,7 @@ def test_prefill_scalar_decay_empty_batch_is_ok(L):
 
 def backward(L, dims, cap=4, **over):
     args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, init=None, cu=None,
-                cs=ctypes.c_void_p(0x90000), do=ctypes.c_void_p(0x98000), dfin=None,
+                cs=ctypes.c_void_p(0x1000000), do=ctypes.c_void_p(0x98000), dfin=None,
                 dq=ctypes.c_void_p(0xa0000), dk=ctypes.c_void_p(0xa8000),
                 dv=ctypes.c_void_p(0xb0000), dg=ctypes.c_void_p(0xb8000),
                 db=ctypes.c_void_p(0xc0000), dinit=None)
@@ -316,6 +316,51 @@ def test_qkv_prologue_no_sequences_is_ok(L):
 def test_qkv_prologue_empty_batch_is_ok(L):
     assert prologue(L, D(num_seqs=0, total_tokens=0), xq=None, xk=None, xv=None, w=None,
                     q=None, k=None, v=None) == OK
+
+
+# Partial overlaps of an output with an input (or another output): each case
+# moves one buffer so that it shares bytes with another; the rest of the call
+# is valid, so the overlap is the only reason to reject it.
+@pytest.mark.parametrize("over", [
+    {"out": ctypes.c_void_p(0x10000 + 4096)},                   # out over the tail of q/k/v
+    {"out": ctypes.c_void_p(0x10000 + 12288)},                  # out over the fp32 g only
+    {"fin": ctypes.c_void_p(0x20000 + 256)},                    # final state over out
+    {"init": ctypes.c_void_p(0x40000), "fin": ctypes.c_void_p(0x40000 - 64)},
+    {"cu": ctypes.c_void_p(0x20000 + 64)},                      # out over cu_seqlens
+])
+def test_prefill_rejects_overlaps(L, over):
+    base = dict(fin=None)
+    base.update(over)
+    assert prefill(L, D(), **base) == INVALID
+
+
+def test_prefill_checkpoints_must_not_overlap_out(L):
+    assert prefill_ckpt(L, D(), ckpt=ctypes.c_void_p(0x20000 - 1024)) == INVALID
+
+
+@pytest.mark.parametrize("over", [
+    {"dk": ctypes.c_void_p(0xa0000 + 4096)},                    # two gradients overlap
+    {"dg": ctypes.c_void_p(0x1000000 + 8192)},                  # dg over the chunk states
+    {"db": ctypes.c_void_p(0x98000 + 128)},                     # dbeta over d_out
+    {"dinit": ctypes.c_void_p(0x10000)},                        # d_init over the inputs
+])
+def test_backward_rejects_overlaps(L, over):
+    assert backward(L, D(), **over) == INVALID
+
+
+@pytest.mark.parametrize("over", [
+    {"out": ctypes.c_void_p(0x30000 + 1024)},                   # out inside the state
+    {"state": ctypes.c_void_p(0x10000 - 256)},                  # state over q/k/v/g
+])
+def test_decode_rejects_overlaps(L, over):
+    assert decode(L, D(num_seqs=4, total_tokens=4), **over) == INVALID
+
+
+def test_output_gate_rejects_overlaps(L):
+    # out (8 KB bf16 at 0x20000) over the norm weight
+    assert L.kda_output_gate(ctypes.byref(D()), ctypes.c_void_p(0x20000),
+                             ctypes.c_void_p(0x60000), ctypes.c_void_p(0x21000),
+                             ctypes.c_float(1e-6), None) == INVALID
 
 
 def test_checkpoint_count():
