@@ -291,19 +291,38 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         }
         if (named_sync_or(BAR_PREP, kPrep, aborted(sm))) break;
 
+        // ---- a1 (gate prologue): g = g_min Sigmoid(e^{A_h} z) from the bf16 logits,
+        // on all eight warps: rows 0-15 on warps 0-3, rows 16-31 on warps 4-7, which
+        // hand theirs over through the upper half of the g slot (the bf16 logits
+        // fill only the lower half).  The barrier also orders every read of z
+        // before Gamma (fp32) overwrites the slot. ----
+        float zg[C / 2];
+        if (gated) {
+            const int c = P & (D - 1), hf = P / D;
+#pragma unroll
+            for (int r = 0; r < C / 2; ++r)
+                zg[r] = kda::gate_g(ld_bf16(in.g, (C / 2) * hf + r, c), gscale);
+            float *handoff = reinterpret_cast<float *>(in.g + kTileBf16);   // [C / 2][D]
+            if (hf) {
+#pragma unroll
+                for (int r = 0; r < C / 2; ++r) handoff[r * D + c] = zg[r];
+            }
+            named_sync(BAR_PREP, kPrep);
+        }
+
         // ---- a1: Gamma = running sum of g per key channel (all loads first) ----
         if (P < D) {
             const int c = P;
             float *g = reinterpret_cast<float *>(in.g);
             float gv[C];
             if (gated) {
-                // g = g_min Sigmoid(e^{A_h} z) from the bf16 logits; every z is read
-                // before Gamma (fp32) overwrites the tile they sit in
+                const float *handoff = reinterpret_cast<const float *>(in.g + kTileBf16);
 #pragma unroll
-                for (int r = 0; r < C; ++r) gv[r] = ld_bf16(in.g, r, c);
-                named_sync(BAR_A1, D);
-#pragma unroll
-                for (int r = 0; r < C; ++r) gv[r] = kda::gate_g(gv[r], gscale);
+                for (int r = 0; r < C / 2; ++r) {
+                    gv[r] = zg[r];
+                    gv[C / 2 + r] = handoff[r * D + c];
+                }
+                named_sync(BAR_A1, D);   // every hand-off value is read before Gamma overwrites it
             } else if (SDECAY) {
                 // one log-decay per token, the same for every key channel
                 const float *gh = sm.ghS[n % kBetaRing];
