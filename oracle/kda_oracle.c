@@ -362,10 +362,12 @@ int kda_oracle_backward(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     if (nt > J.n_items) nt = (int)(J.n_items > 0 ? J.n_items : 1);
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
     int started = 0;
-    if (th)
-        for (int i = 1; i < nt; ++i)
+    if (th) {
+        for (int i = 1; i < nt; ++i) {
             if (pthread_create(&th[i], NULL, bwd_worker, &J) == 0) ++started;
             else break;
+        }
+    }
     if (bwd_worker(&J) != NULL) rc = -1;
     for (int i = 1; i <= started; ++i) {
         void *ret = NULL;
