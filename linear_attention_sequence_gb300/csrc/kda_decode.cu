@@ -39,7 +39,6 @@ kda_decode_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
     __shared__ float red_r[RPP][D];
     __shared__ float red_kq[RPP];
     __shared__ float s_u[D];
-    __shared__ float s_kq;
 
     const int64_t nh = blockIdx.x;           // n * H + h
     const int t = threadIdx.x;
