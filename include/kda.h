@@ -16,7 +16,11 @@
  * Conventions shared by every entry point
  * ----------------------------------------
  *  - All tensors are row-major and contiguous, in DEVICE memory, owned by
- *    the caller.  The library allocates no device memory on these paths.
+ *    the caller.  The library allocates no device memory, with one exception:
+ *    the KDA_PREFILL_TC_SPLIT prefill variant takes stream-ordered scratch
+ *    (its ring of chunk operands, about 0.28 MB per (sequence, head) it runs
+ *    at once, at most 27 MB) from a memory pool of the library's own, and
+ *    returns it on the same stream when the call's work is done.
  *  - q, k  [T_tot, H, d_k];  v, out [T_tot, H, d_v];  g [T_tot, H, d_k] fp32
  *    (log-decay); beta [T_tot, H] fp32; states [N, H, d_k, d_v] fp32 with row
  *    i = key channel i (the decay scales rows: "Hybrid Attention", section
@@ -54,15 +58,18 @@ typedef enum {
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
-/* Prefill kernel selection.  KDA_PREFILL_DEFAULT picks the tensor-core
- * kernel where it supports the call, else the fp32 CUDA-core one.  The
- * tensor-core kernel takes d_k = d_v = 128, bf16 q/k/v, and q, k, v, g (or z)
- * and out 16-byte aligned; KDA_PREFILL_TC on any other call returns
- * KDA_ERR_UNSUPPORTED. */
+/* Prefill kernel selection: a diagnostic and test selector, not a tuning
+ * knob.  KDA_PREFILL_DEFAULT (what callers should pass) picks the first of
+ * TC_SPLIT, TC, FP32 that supports the call.  The tensor-core kernels take
+ * d_k = d_v = 128, bf16 q/k/v, and q, k, v, g (or z) and out 16-byte aligned;
+ * TC_SPLIT also needs a device that supports cooperative launches.  Naming a
+ * variant that does not support the call returns KDA_ERR_UNSUPPORTED. */
 typedef enum {
     KDA_PREFILL_DEFAULT = 0,
-    KDA_PREFILL_FP32 = 1,  /* CUDA-core fp32 chunked kernel (any supported shape) */
-    KDA_PREFILL_TC = 2     /* tcgen05 tensor-core chunked kernel (d = 128) */
+    KDA_PREFILL_FP32 = 1,     /* CUDA-core fp32 chunked kernel (any supported shape) */
+    KDA_PREFILL_TC = 2,       /* tcgen05 kernel, one CTA per (sequence, head) (d = 128) */
+    KDA_PREFILL_TC_SPLIT = 3  /* tcgen05 kernel with the state recurrence and the intra-chunk
+                                 work on different SMs, one cooperative launch (d = 128) */
 } kda_prefill_variant;
 
 typedef void *kda_stream_t; /* a cudaStream_t */

@@ -56,7 +56,7 @@ kda_status check_dims(const kda_dims *d, kda::Problem &P) {
     if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads < 1 || d->d_k < 1 || d->d_v < 1)
         return KDA_ERR_INVALID_ARGUMENT;
     if (!valid_dtype(d->in_dtype) || !valid_dtype(d->out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
-    if (d->variant < KDA_PREFILL_DEFAULT || d->variant > KDA_PREFILL_TC) return KDA_ERR_INVALID_ARGUMENT;
+    if (d->variant < KDA_PREFILL_DEFAULT || d->variant > KDA_PREFILL_TC_SPLIT) return KDA_ERR_INVALID_ARGUMENT;
     if (d->d_k != d->d_v || (d->d_k != 64 && d->d_k != 128)) return KDA_ERR_UNSUPPORTED;
     // element counts must fit the kernels' 64-bit index arithmetic comfortably
     const int64_t elems = (int64_t)d->total_tokens * d->num_heads * d->d_k;
@@ -172,18 +172,27 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
         P.oeps = x.oeps;
     }
     const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in, out);
+    const bool split_ok = tc_ok && kda_prefill_chain_supported(P, q, k, v, (const float *)g_in, out);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    if (P.variant == KDA_PREFILL_TC_SPLIT && !split_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
-    // the tensor-core kernel gates its bf16 output before the store (the gate
-    // tile arrives by TMA); every other case gates `out` in place afterwards
-    P.ogate_fused = P.ogate && use_tc && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
-                    aligned16(P.ogate);
-    cudaError_t e = use_tc ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,
-                                                   out, final_state, s)
-                           : kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state, cu_seqlens,
-                                                     out, final_state, s);
+    // the default takes the split tensor-core kernel, then the one-CTA-per-head
+    // tensor-core kernel, then the CUDA-core kernel, whichever first supports the call
+    const bool use_split =
+        P.variant == KDA_PREFILL_TC_SPLIT || (P.variant == KDA_PREFILL_DEFAULT && split_ok);
+    const bool use_tc = !use_split && (P.variant == KDA_PREFILL_TC ||
+                                       (P.variant == KDA_PREFILL_DEFAULT && tc_ok));
+    // the tensor-core kernels gate a bf16 output before the store (the one-CTA
+    // kernel loads the gate tile by TMA); every other case gates `out` in place afterwards
+    P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
+                    (use_split || (use_tc && aligned16(P.ogate)));
+    cudaError_t e = use_split ? kda_launch_prefill_chain(P, q, k, v, g, beta, init_state, cu_seqlens, out,
+                                                         final_state, s)
+                    : use_tc  ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,
+                                                      out, final_state, s)
+                              : kda_launch_prefill_fp32(P, q, k, v, g, beta, init_state,
+                                                        cu_seqlens, out, final_state, s);
     if (e == cudaSuccess && P.ogate && !P.ogate_fused) e = kda_launch_output_gate(P, out, s);
     if (e != cudaSuccess) return cuda_fail(e, where);
     return KDA_OK;

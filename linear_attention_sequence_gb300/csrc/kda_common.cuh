@@ -132,6 +132,13 @@ cudaError_t kda_launch_qkv_prologue(const kda::Problem &P, const void *xq, const
                                     float eps, cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
 cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
+bool kda_prefill_chain_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
+                                 const float *g, const void *out);
+cudaError_t kda_launch_prefill_chain(const kda::Problem &P, const void *q, const void *k,
+                                     const void *v, const float *g, const float *beta,
+                                     const float *init_state, const int32_t *cu, void *out,
+                                     float *final_state, cudaStream_t stream);
+cudaError_t kda_chain_read_status(unsigned *status);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
                                     const void *v, const float *g, const float *beta,
                                     const float *init_state, const int32_t *cu, void *out,

@@ -1069,5 +1069,7 @@ cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
     e = cudaMemcpyFromSymbol(status, g_kda_device_status, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(unsigned));
+    e = cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    return kda_chain_read_status(status);   // the split kernel's status word
 }

@@ -13,13 +13,13 @@ from kda_testutil import TOL, rel_err, host64
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-VARIANTS = [kda.PREFILL_DEFAULT, kda.PREFILL_FP32, kda.PREFILL_TC]
+VARIANTS = [kda.PREFILL_DEFAULT, kda.PREFILL_FP32, kda.PREFILL_TC, kda.PREFILL_TC_SPLIT]
 
 
 def supported(variant, d, dtype):
     """The tensor-core kernel takes d = 128 with bf16 inputs only (its tf32
     operands cannot meet the 1e-4 bound of fp32 inputs)."""
-    if variant == kda.PREFILL_TC:
+    if variant in (kda.PREFILL_TC, kda.PREFILL_TC_SPLIT):
         return d == 128 and dtype == torch.bfloat16
     return True
 
