@@ -59,11 +59,12 @@ typedef enum {
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
 /* Prefill kernel selection: a diagnostic and test selector, not a tuning
- * knob.  KDA_PREFILL_DEFAULT (what callers should pass) picks the first of
- * TC_SPLIT, TC, FP32 that supports the call.  The tensor-core kernels take
- * d_k = d_v = 128, bf16 q/k/v, and q, k, v, g (or z) and out 16-byte aligned;
- * TC_SPLIT also needs a device that supports cooperative launches.  Naming a
- * variant that does not support the call returns KDA_ERR_UNSUPPORTED. */
+ * knob.  KDA_PREFILL_DEFAULT (what callers should pass) picks TC where it
+ * supports the call, else FP32.  TC_SPLIT runs only when named (it is slower
+ * than TC on the 96-head layer).  The tensor-core kernels take d_k = d_v =
+ * 128, bf16 q/k/v, and q, k, v, g (or z) and out 16-byte aligned; TC_SPLIT
+ * also needs a device that supports cooperative launches.  Naming a variant
+ * that does not support the call returns KDA_ERR_UNSUPPORTED. */
 typedef enum {
     KDA_PREFILL_DEFAULT = 0,
     KDA_PREFILL_FP32 = 1,     /* CUDA-core fp32 chunked kernel (any supported shape) */

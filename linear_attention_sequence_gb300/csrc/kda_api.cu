@@ -177,12 +177,10 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     if (P.variant == KDA_PREFILL_TC_SPLIT && !split_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
-    // the default takes the split tensor-core kernel, then the one-CTA-per-head
-    // tensor-core kernel, then the CUDA-core kernel, whichever first supports the call
-    const bool use_split =
-        P.variant == KDA_PREFILL_TC_SPLIT || (P.variant == KDA_PREFILL_DEFAULT && split_ok);
-    const bool use_tc = !use_split && (P.variant == KDA_PREFILL_TC ||
-                                       (P.variant == KDA_PREFILL_DEFAULT && tc_ok));
+    // the default takes the one-CTA-per-head tensor-core kernel where it supports the
+    // call, else the CUDA-core kernel; the split kernel runs only when it is named
+    const bool use_split = P.variant == KDA_PREFILL_TC_SPLIT;
+    const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
     // the tensor-core kernels gate a bf16 output before the store (the one-CTA
     // kernel loads the gate tile by TMA); every other case gates `out` in place afterwards
     P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
