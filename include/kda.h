@@ -126,6 +126,38 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                        const int32_t *cu_seqlens, void *out, float *final_state,
                        kda_stream_t stream);
 
+/*
+ * kda_prefill_noalloc -- kda_prefill that allocates nothing.
+ *
+ * The pages have no counterpart of this call: it is an interface addition for
+ * callers that may not allocate device memory during a call -- hosts whose own
+ * caching allocator owns all of the GPU's memory from start-up (an allocation
+ * outside it can fail or fragment it) and latency-bound services that keep
+ * allocation off their serving path.
+ *
+ * Same arguments, layouts, semantics and errors as kda_prefill; dims->variant
+ * is ignored.  It always runs the KDA_PREFILL_TC_SPLIT kernel, with that
+ * kernel's scratch (ring of chunk operands, hand-off words, step table) in a
+ * fixed array of the library (about 5 MB, which every device that loads the
+ * library keeps until the process exits) instead of pool memory.  That array
+ * limits a call to at most 16 chains of at most 4096 (sequence, head) pairs
+ * each and at most 65536 sequences; a batch beyond that, or one the split
+ * kernel does not take (d_k = d_v != 128, fp32 inputs, q/k/v/g/out not
+ * 16-byte aligned, a device without cooperative launches), returns
+ * KDA_ERR_UNSUPPORTED and launches nothing.
+ *
+ * The first call on a device looks up the device address of the array
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture on the device.  Every call shares the one array
+ * and clears the parts that must start at zero itself; calls that overlap on
+ * the GPU (on different streams or from different host threads) race on it
+ * and must be serialised by the caller.
+ */
+kda_status kda_prefill_noalloc(const kda_dims *dims, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, const float *init_state,
+                               const int32_t *cu_seqlens, void *out, float *final_state,
+                               kda_stream_t stream);
+
 /* Chunk length of the prefill kernels; checkpoint intervals are multiples of it. */
 #define KDA_CHUNK 32
 

@@ -7,6 +7,7 @@ same names and raises on a non-OK status.  It performs no arithmetic of the
 method and has no fallback: if the library is missing, every call raises.
 
     kda_prefill(q, k, v, g, beta, ...)  chunk-parallel prefill, packed batch
+    kda_prefill_noalloc(...)            the same, allocating nothing (fixed scratch array)
     kda_prefill_checkpointed(...)       the same, plus state checkpoints every `interval` tokens
     kda_prefill_gated(q, k, v, z, a_log, beta_logit, ...)   the same, from gate logits
     kda_prefill_output_gated(q, k, v, g, beta, gate_logit, ...)   the same, then the output gate
@@ -23,7 +24,7 @@ import os
 
 import torch
 
-__all__ = ["KdaError", "kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated",
+__all__ = ["KdaError", "kda_prefill", "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_prefill_gated",
            "kda_prefill_output_gated", "kda_prefill_scalar_decay", "kda_backward",
            "kda_output_gate", "kda_qkv_prologue", "checkpoint_count", "kda_decode",
            "kda_status_string", "lib", "library_path",
@@ -73,6 +74,8 @@ def lib():
         vp, fp = ctypes.c_void_p, ctypes.c_void_p
         L.kda_prefill.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp, fp, vp]
         L.kda_prefill.restype = ctypes.c_int
+        L.kda_prefill_noalloc.argtypes = L.kda_prefill.argtypes
+        L.kda_prefill_noalloc.restype = ctypes.c_int
         L.kda_prefill_checkpointed.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, fp, fp, fp, vp, vp,
                                                fp, fp, ctypes.c_int64, ctypes.c_int64, vp]
         L.kda_prefill_checkpointed.restype = ctypes.c_int
@@ -428,6 +431,24 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=
                            _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                            _stream(stream))
     _check(st, "kda_prefill")
+    return out, final_state
+
+
+def kda_prefill_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, *, num_seqs=None,
+                        out=None, final_state=None, out_dtype=None, return_final_state=True,
+                        stream=None):
+    """kda_prefill through the C entry point ``kda_prefill_noalloc``: the split
+    kernel on the library's fixed scratch array, for callers that may not
+    allocate device memory during a call.  The library allocates nothing; pass
+    ``out`` (and ``final_state``) to allocate nothing here either.  Calls that
+    overlap on the GPU share the array and must be serialised."""
+    dims, out, final_state = _prefill_args(q, k, v, g, beta, init_state, cu_seqlens, num_seqs,
+                                           out, final_state, out_dtype, PREFILL_TC_SPLIT,
+                                           return_final_state)
+    st = lib().kda_prefill_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+                                   _ptr(final_state), _stream(stream))
+    _check(st, "kda_prefill_noalloc")
     return out, final_state
 
 

@@ -119,6 +119,7 @@ struct Extras {
     float oeps = 0.f;
     bool scalar_decay = false;        // one log-decay per (token, head) instead of g
     const float *g_head = nullptr;    // (nullptr: no decay, the delta rule)
+    bool noalloc = false;             // the split kernel on the library's fixed scratch array
 };
 
 kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, const void *v,
@@ -172,7 +173,8 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
         P.oeps = x.oeps;
     }
     const bool tc_ok = kda_prefill_tc_supported(P, q, k, v, (const float *)g_in, out);
-    const bool split_ok = tc_ok && kda_prefill_chain_supported(P, q, k, v, (const float *)g_in, out);
+    const bool split_ok = x.noalloc ? kda_prefill_noalloc_fits(P, q, k, v, (const float *)g_in, out)
+                                    : tc_ok && kda_prefill_chain_supported(P, q, k, v, (const float *)g_in, out);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.variant == KDA_PREFILL_TC_SPLIT && !split_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
@@ -185,7 +187,9 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     // kernel loads the gate tile by TMA); every other case gates `out` in place afterwards
     P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
                     (use_split || (use_tc && aligned16(P.ogate)));
-    cudaError_t e = use_split ? kda_launch_prefill_chain(P, q, k, v, g, beta, init_state, cu_seqlens, out,
+    cudaError_t e = x.noalloc ? kda_launch_prefill_noalloc(P, q, k, v, g, beta, init_state, cu_seqlens,
+                                                           out, final_state, s)
+                    : use_split ? kda_launch_prefill_chain(P, q, k, v, g, beta, init_state, cu_seqlens, out,
                                                          final_state, s)
                     : use_tc  ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                       out, final_state, s)
@@ -204,6 +208,19 @@ kda_status kda_prefill(const kda_dims *dims, const void *q, const void *k, const
                        kda_stream_t stream) {
     return prefill_common(dims, q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
                           Extras(), stream, "kda_prefill");
+}
+
+kda_status kda_prefill_noalloc(const kda_dims *dims, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, const float *init_state,
+                               const int32_t *cu_seqlens, void *out, float *final_state,
+                               kda_stream_t stream) {
+    if (!dims) return KDA_ERR_INVALID_ARGUMENT;
+    kda_dims d = *dims;
+    d.variant = KDA_PREFILL_TC_SPLIT;   // the one kernel this entry point runs
+    Extras x;
+    x.noalloc = true;
+    return prefill_common(&d, q, k, v, g, beta, init_state, cu_seqlens, out, final_state, x, stream,
+                          "kda_prefill_noalloc");
 }
 
 kda_status kda_prefill_checkpointed(const kda_dims *dims, const void *q, const void *k,

@@ -139,6 +139,12 @@ cudaError_t kda_launch_prefill_chain(const kda::Problem &P, const void *q, const
                                      const float *init_state, const int32_t *cu, void *out,
                                      float *final_state, cudaStream_t stream);
 cudaError_t kda_chain_read_status(unsigned *status);
+bool kda_prefill_noalloc_fits(const kda::Problem &P, const void *q, const void *k, const void *v,
+                              const float *g, const void *out);
+cudaError_t kda_launch_prefill_noalloc(const kda::Problem &P, const void *q, const void *k,
+                                       const void *v, const float *g, const float *beta,
+                                       const float *init_state, const int32_t *cu, void *out,
+                                       float *final_state, cudaStream_t stream);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
                                     const void *v, const float *g, const float *beta,
                                     const float *init_state, const int32_t *cu, void *out,

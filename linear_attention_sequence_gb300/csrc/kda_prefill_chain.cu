@@ -1176,3 +1176,130 @@ cudaError_t kda_chain_read_status(unsigned *status) {
     *status |= st;
     return e;
 }
+
+// ---------------------------------------------------------------- kda_prefill_noalloc
+//
+// The same kernel with its scratch in a fixed array of this library instead of
+// memory taken from a pool: for callers that may not allocate device memory
+// during a call -- hosts whose own caching allocator owns all of the GPU's memory
+// from start-up (a call that allocates outside it can fail or fragment it), and
+// latency-bound services that keep allocation off their serving path.  The
+// array holds the ring, hand-off words, step table and sequence order of at
+// most kNaChains chains, each with at most kNaPairsPerChain (sequence, head)
+// pairs, for batches of at most kNaSeqs sequences: about 5 MB, which every
+// device that loads the library keeps until the process exits.
+
+namespace {
+
+constexpr int kNaChains = 16;
+constexpr int kNaPairsPerChain = 4096;
+constexpr int kNaSeqs = 65536;
+constexpr size_t kNaRingOff = 0;
+constexpr size_t kNaReadyOff = kNaRingOff + (size_t)kNaChains * kRing * kSlotStride;
+constexpr size_t kNaProgOff = kNaReadyOff + 256;
+constexpr size_t kNaFsOff = kNaProgOff + 256;
+constexpr size_t kNaOrderOff = kNaFsOff + ((size_t)kNaChains * (kNaPairsPerChain + 1) * 4 + 255) / 256 * 256;
+constexpr size_t kNaCtrlOff = kNaOrderOff + (size_t)kNaSeqs * 4;
+constexpr size_t kNaBytes = kNaCtrlOff + 256;
+static_assert(kNaChains * kRing * 4 <= 256 && kNaChains * 4 <= 256, "hand-off words fit their blocks");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
+
+// Per device: the SM count, cooperative-launch support and the device address of
+// g_noalloc_scratch (cudaGetSymbolAddress with the device current; the host-side
+// name of the array is not a device address).  Done once, by the first call on
+// the device.
+struct NaDev {
+    unsigned char *ptr = nullptr;
+    int sms = 0;
+    bool coop = false;
+    cudaError_t err = cudaSuccess;
+};
+
+NaDev &noalloc_dev(int dev) {
+    static NaDev info[64];
+    static std::once_flag once[64];
+    std::call_once(once[dev & 63], [dev] {
+        NaDev &d = info[dev & 63];
+        int coop = 0;
+        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        d.coop = coop != 0;
+        if (d.err == cudaSuccess) {
+            void *p = nullptr;
+            d.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            d.ptr = static_cast<unsigned char *>(p);
+        }
+    });
+    return info[dev & 63];
+}
+
+}  // namespace
+
+// Does the fixed array hold this call, and does the split kernel take it?
+bool kda_prefill_noalloc_fits(const kda::Problem &P, const void *q, const void *k, const void *v,
+                              const float *g, const void *out) {
+    auto al16 = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
+    if (!(P.dk == 128 && P.dv == 128 && P.in_dtype == KDA_DTYPE_BF16)) return false;
+    if (P.N == 0) return true;   // nothing to run
+    if (!(al16(q) && al16(k) && al16(v) && (P.scalar_decay || al16(g)) && al16(out))) return false;
+    if (P.N > kNaSeqs) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const NaDev &d = noalloc_dev(dev);
+    if (d.err != cudaSuccess || !d.coop || d.sms < 2) return false;
+    const int64_t pairs = (int64_t)P.N * P.H;
+    int nc = chain_count(d.sms, (int)(pairs < (1 << 30) ? pairs : (1 << 30)));
+    if (nc > kNaChains) nc = kNaChains;
+    return (pairs + nc - 1) / nc <= kNaPairsPerChain;
+}
+
+// Launch the split kernel on the fixed array.  Calls no allocation routine.
+cudaError_t kda_launch_prefill_noalloc(const kda::Problem &P, const void *q, const void *k,
+                                       const void *v, const float *g, const float *beta,
+                                       const float *init_state, const int32_t *cu, void *out,
+                                       float *final_state, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    NaDev &d = noalloc_dev(dev);
+    if (d.err != cudaSuccess) return d.err;
+    const int pairs = P.N * P.H;
+    const int grid = d.sms;
+    int NC = chain_count(grid, pairs);
+    if (NC > kNaChains) NC = kNaChains;
+    const int KMAX = (pairs + NC - 1) / NC;
+    if (KMAX > kNaPairsPerChain || P.N > kNaSeqs) return cudaErrorInvalidValue;
+    Scratch sc;
+    sc.ring = d.ptr + kNaRingOff;
+    sc.ready = reinterpret_cast<uint32_t *>(d.ptr + kNaReadyOff);
+    sc.progress = reinterpret_cast<uint32_t *>(d.ptr + kNaProgOff);
+    sc.first_step = reinterpret_cast<uint32_t *>(d.ptr + kNaFsOff);
+    sc.order = reinterpret_cast<int32_t *>(d.ptr + kNaOrderOff);
+    sc.ctrl = reinterpret_cast<uint32_t *>(d.ptr + kNaCtrlOff);
+    // the array keeps the last call's contents: the set-up kernel clears the
+    // hand-off words and rewrites the step table before the main kernel reads them
+    chain_setup_kernel<<<1, 1024, 0, stream>>>(cu, P.N, P.H, (int64_t)P.T, P.seq_len, NC, KMAX, sc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    Params prm = {};
+    prm.q = static_cast<const __nv_bfloat16 *>(q);
+    prm.k = static_cast<const __nv_bfloat16 *>(k);
+    prm.v = static_cast<const __nv_bfloat16 *>(v);
+    prm.g = g;
+    prm.beta = beta;
+    prm.init = init_state;
+    prm.cu = cu;
+    prm.out = out;
+    prm.fin = final_state;
+    prm.ckpt_every = 1;
+    prm.N = P.N;
+    prm.H = P.H;
+    prm.total = P.T;
+    prm.seq_len = P.seq_len;
+    prm.NC = NC;
+    prm.KMAX = KMAX;
+    prm.sc = sc;
+    return P.out_dtype == KDA_DTYPE_BF16 ? launch_out<__nv_bfloat16>(prm, grid, kDecayTile, false, stream)
+                                         : launch_out<float>(prm, grid, kDecayTile, false, stream);
+}
