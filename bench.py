@@ -59,8 +59,9 @@ BWD_C, BWD_D = 32, 128
 BWD_MACS_PER_CHUNK_HEAD = (BWD_C * (BWD_C + 1) // 2 * 2 * BWD_D + 7 * BWD_C * BWD_D * BWD_D
                            + 5 * BWD_C * BWD_C * BWD_D // 2 + 2 * BWD_C ** 3 // 3
                            + 3 * BWD_C * BWD_C * BWD_D)
-# fp32 CUDA-core peak of the part: 152 SMs x 128 fp32 lanes x 2 flops per FMA x SM clock
-FP32_LANES = 152 * 128
+# fp32 CUDA-core peak of the part: SMs (read from the device) x 128 fp32 lanes x 2 flops
+# per FMA x SM clock
+FP32_LANES_PER_SM = 128
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -294,6 +295,28 @@ def run_reference(args):
     return 0
 
 
+def leg_summary(ms, units, nbytes, hbm_gbs, steps, kernel, extra=None):
+    """A compact record of one secondary leg: time per step, units/s, and the
+    HBM roofline fraction over its algorithmic bytes (of the measured peak)."""
+    ach = nbytes / (ms * 1e-3) / 1e9
+    d = {"ms": round(ms, 4), "tok_s": round(units / (ms * 1e-3)), "frac": round(ach / hbm_gbs, 4),
+         "gbs": round(ach, 1), "bytes": int(nbytes), "steps": steps, "kernel": kernel}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def check_device_status(kda, stream, leg: str):
+    """A bounded device-side wait that gave up ends its kernel early: a step
+    that stopped would look faster.  Any nonzero status ends the run."""
+    st = kda.kda_get_last_device_error(stream)
+    if st != 0:
+        print(json.dumps({"error": f"device status {st} ({kda.kda_status_string(st)}) after the "
+                                   f"{leg} leg: a bounded wait gave up; no result is reported"}),
+              flush=True)
+        sys.exit(3)
+
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -312,8 +335,10 @@ def run_gpu(args):
 
     stream = torch.cuda.current_stream()
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     if args.profile:
         return run_profile_case(args, kda, synth, dev, stream)
+    check_device_status(kda, stream, "start")
 
     # ---------------- prefill (headline) ----------------
     w = synth.WORKLOADS["prefill_8k"]
@@ -330,6 +355,7 @@ def run_gpu(args):
     sampler = ClockSampler(local).start() if rank == 0 else None
     ms, t0, t1 = time_steps(prefill_step, args.steps, args.warmup, world, stream)
     clocks = sampler.summary(t0, t1) if sampler else None
+    check_device_status(kda, stream, "prefill_8k")
     value = T * world / (ms * 1e-3)
     achieved = PREFILL_BYTES_PER_TOKEN * T / (ms * 1e-3) / 1e9
     kernel_src = "linear_attention_sequence_gb300/csrc/kda_prefill_tc.cu"
@@ -338,6 +364,19 @@ def run_gpu(args):
                 "kernel": "kda_prefill_tc_kernel",
                 "traffic": profiled_traffic("kda_prefill_tc_kernel", kernel_src, "prefill_8k"),
                 "algorithmic_bytes_per_launch": PREFILL_BYTES_PER_TOKEN * T}
+    legs = {}
+    short = max(3, min(args.steps, 20))
+
+    # ---------------- the same layer through the split kernel (state chain / intra-chunk SMs) ----
+    def split_step():
+        kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                        cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
+                        variant=kda.PREFILL_TC_SPLIT, stream=stream)
+
+    ms_sp, _, _ = time_steps(split_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "split")
+    legs["split"] = leg_summary(ms_sp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
+                                "kda_prefill_chain_kernel")
 
     # ---------------- the same layer with state checkpoints every 1024 tokens ----------------
     interval = 1024
@@ -349,18 +388,11 @@ def run_gpu(args):
                                      cu_seqlens=inp["cu_seqlens"], interval=interval,
                                      checkpoints=ck, out=out, final_state=fin, stream=stream)
 
-    ck_steps = max(3, min(args.steps, 20))
-    ms_ck, _, _ = time_steps(checkpointed_step, ck_steps, max(args.warmup, 3), world, stream)
+    ms_ck, _, _ = time_steps(checkpointed_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "checkpointed")
     ck_bytes = ck.numel() * ck.element_size()
-    ck_ach = (PREFILL_BYTES_PER_TOKEN * T + ck_bytes) / (ms_ck * 1e-3) / 1e9
-    checkpointed = {"value": T * world / (ms_ck * 1e-3), "unit": UNIT, "ms_per_step": ms_ck,
-                    "steps": ck_steps, "interval_tokens": interval,
-                    "checkpoint_bytes_per_step": ck_bytes,
-                    "roofline": {"bound": "hbm", "achieved": ck_ach, "peak": hbm_gbs,
-                                 "unit": "GB/s", "frac": ck_ach / hbm_gbs,
-                                 "peak_source": peak_src, "kernel": "kda_prefill_tc_kernel",
-                                 "algorithmic_bytes_per_launch":
-                                     PREFILL_BYTES_PER_TOKEN * T + ck_bytes}}
+    legs["checkpointed"] = leg_summary(ms_ck, T * world, PREFILL_BYTES_PER_TOKEN * T + ck_bytes,
+                                       hbm_gbs, short, "kda_prefill_tc_kernel")
     del ck
 
     # ---------------- the same layer through the fused gate prologue ----------------
@@ -371,19 +403,13 @@ def run_gpu(args):
                               gl["beta_logit"], cu_seqlens=inp["cu_seqlens"], out=out,
                               final_state=fin, stream=stream)
 
-    ms_gt, _, _ = time_steps(gated_step, ck_steps, max(args.warmup, 3), world, stream)
-    gt_ach = GATED_BYTES_PER_TOKEN * T / (ms_gt * 1e-3) / 1e9
-    gated = {"value": T * world / (ms_gt * 1e-3), "unit": UNIT, "ms_per_step": ms_gt,
-             "steps": ck_steps,
-             "config": {"workload": "prefill_8k inputs with gate logits: bf16 z ~ N(-3.6, 1), "
-                                    "A_h ~ 0.1 N(0, 1), beta logits ~ N(0, 1)"},
-             "roofline": {"bound": "hbm", "achieved": gt_ach, "peak": hbm_gbs, "unit": "GB/s",
-                          "frac": gt_ach / hbm_gbs, "peak_source": peak_src,
-                          "kernel": "kda_prefill_tc_kernel",
-                          "algorithmic_bytes_per_launch": GATED_BYTES_PER_TOKEN * T}}
+    ms_gt, _, _ = time_steps(gated_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "gated")
+    legs["gated"] = leg_summary(ms_gt, T * world, GATED_BYTES_PER_TOKEN * T, hbm_gbs, short,
+                                "kda_prefill_tc_kernel")
     del gl
 
-    # ---------------- the same layer with the output gate fused into the store ----------------
+    # ---------------- the output gate: the entry point, and the unfused pair ----------------
     og = synth.output_gate_inputs(T, w.heads, w.d, dtype=w.dtype, seed=83, device=dev)
 
     def ogated_step():
@@ -392,16 +418,19 @@ def run_gpu(args):
                                      cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
                                      stream=stream)
 
-    ms_og, _, _ = time_steps(ogated_step, ck_steps, max(args.warmup, 3), world, stream)
-    og_ach = OGATED_BYTES_PER_TOKEN * T / (ms_og * 1e-3) / 1e9
-    output_gated = {
-        "value": T * world / (ms_og * 1e-3), "unit": UNIT, "ms_per_step": ms_og, "steps": ck_steps,
-        "config": {"workload": "prefill_8k inputs with output-gate logits: bf16 ~ N(0, 1), "
-                               "norm weight ~ U(0.5, 1.5), eps 1e-6; bf16 out (fused epilogue)"},
-        "roofline": {"bound": "hbm", "achieved": og_ach, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": og_ach / hbm_gbs, "peak_source": peak_src,
-                     "kernel": "kda_prefill_tc_kernel",
-                     "algorithmic_bytes_per_launch": OGATED_BYTES_PER_TOKEN * T}}
+    def ogate_pair_step():
+        prefill_step()
+        kda.kda_output_gate(out, og["gate"], og["norm_weight"], 1e-6, stream=stream)
+
+    ms_og, _, _ = time_steps(ogated_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "output_gated")
+    ms_op, _, _ = time_steps(ogate_pair_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "output_gate_pair")
+    legs["output_gated"] = leg_summary(ms_og, T * world, OGATED_BYTES_PER_TOKEN * T, hbm_gbs,
+                                       short, "kda_prefill_tc_kernel + kda_output_gate_kernel")
+    legs["output_gate_pair"] = leg_summary(
+        ms_op, T * world, OGATED_BYTES_PER_TOKEN * T, hbm_gbs, short,
+        "kda_prefill then kda_output_gate (two calls)")
     del og
 
     # ---------------- Gated DeltaNet: one decay per head and step ----------------
@@ -412,16 +441,10 @@ def run_gpu(args):
                                      cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
                                      stream=stream)
 
-    ms_sd, _, _ = time_steps(sdecay_step, ck_steps, max(args.warmup, 3), world, stream)
-    sd_ach = SDECAY_BYTES_PER_TOKEN * T / (ms_sd * 1e-3) / 1e9
-    scalar_decay = {
-        "value": T * world / (ms_sd * 1e-3), "unit": UNIT, "ms_per_step": ms_sd, "steps": ck_steps,
-        "config": {"workload": "prefill_8k inputs, one log-decay per (token, head): "
-                               "max(-5, log Sigmoid(x)), x ~ N(2, 1)"},
-        "roofline": {"bound": "hbm", "achieved": sd_ach, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": sd_ach / hbm_gbs, "peak_source": peak_src,
-                     "kernel": "kda_prefill_tc_kernel",
-                     "algorithmic_bytes_per_launch": SDECAY_BYTES_PER_TOKEN * T}}
+    ms_sd, _, _ = time_steps(sdecay_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "scalar_decay")
+    legs["scalar_decay"] = leg_summary(ms_sd, T * world, SDECAY_BYTES_PER_TOKEN * T, hbm_gbs,
+                                       short, "kda_prefill_tc_kernel")
     del gh
 
     # ---------------- the q, k, v prologue of the same layer ----------------
@@ -433,23 +456,14 @@ def run_gpu(args):
                              cu_seqlens=inp["cu_seqlens"], q=pq, k=pk, v=pv,
                              return_conv_state=False, stream=stream)
 
-    ms_pr, _, _ = time_steps(prologue_step, ck_steps, max(args.warmup, 3), world, stream)
+    ms_pr, _, _ = time_steps(prologue_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "qkv_prologue")
     pr_bytes = PROLOGUE_BYTES_PER_TOKEN * T + PROLOGUE_WEIGHT_BYTES
-    pr_ach = pr_bytes / (ms_pr * 1e-3) / 1e9
-    qkv_prologue = {
-        "value": T * world / (ms_pr * 1e-3), "unit": UNIT, "ms_per_step": ms_pr,
-        "steps": ck_steps,
-        "config": {"workload": "prefill_8k shapes: projections x_q, x_k, x_v ~ N(0, 1) bf16 "
-                               "[8192, 96, 128], conv weights ~ U(-1/2, 1/2) fp32, no carried "
-                               "state; bf16 q, k, v out"},
-        "roofline": {"bound": "hbm", "achieved": pr_ach, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": pr_ach / hbm_gbs, "peak_source": peak_src,
-                     "kernel": "kda_qkv_prologue_kernel",
-                     "traffic": profiled_traffic(
-                         "kda_qkv_prologue_kernel",
-                         "linear_attention_sequence_gb300/csrc/kda_qkv_prologue.cu",
-                         "prologue_8k"),
-                     "algorithmic_bytes_per_launch": pr_bytes}}
+    legs["qkv_prologue"] = leg_summary(
+        ms_pr, T * world, pr_bytes, hbm_gbs, short, "kda_qkv_prologue_kernel",
+        {"traffic": profiled_traffic("kda_qkv_prologue_kernel",
+                                     "linear_attention_sequence_gb300/csrc/kda_qkv_prologue.cu",
+                                     "prologue_8k")})
     del pj, pq, pk, pv
 
     # ---------------- the backward pass (gradients of the same layer) ----------------
@@ -465,20 +479,16 @@ def run_gpu(args):
 
     bw_steps = 3
     ms_bw, _, _ = time_steps(backward_step, bw_steps, 2, world, stream)
+    check_device_status(kda, stream, "backward")
     bw_flops = 2.0 * BWD_MACS_PER_CHUNK_HEAD * ((T + BWD_C - 1) // BWD_C) * w.heads
     sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
-    fp32_peak = FP32_LANES * 2 * sm_mhz * 1e6 / 1e12
+    fp32_peak = sm_count * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
     bw_ach = bw_flops / (ms_bw * 1e-3) / 1e12
-    backward = {
-        "value": T * world / (ms_bw * 1e-3), "unit": UNIT, "ms_per_step": ms_bw,
-        "steps": bw_steps,
-        "config": {"workload": "prefill_8k inputs, upstream gradient of out ~ N(0, 1) (bf16), "
-                               "chunk states from kda_prefill_checkpointed (interval 32); "
-                               "fp32 gradients of q, k, v, g, beta"},
-        "roofline": {"bound": "alu", "achieved": bw_ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                     "frac": bw_ach / fp32_peak,
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 x sampled SM clock",
-                     "kernel": "kda_backward_kernel", "algorithmic_flops_per_launch": bw_flops}}
+    legs["backward"] = {"ms": round(ms_bw, 3), "tok_s": round(T * world / (ms_bw * 1e-3)),
+                        "bound": "alu", "tflops": round(bw_ach, 2),
+                        "peak_tflops": round(fp32_peak, 2),
+                        "frac": round(bw_ach / fp32_peak, 4), "steps": bw_steps,
+                        "kernel": "kda_backward_kernel"}
     del cstates, d_out
 
     # ---------------- e2e through the public API, host buffers ----------------
@@ -522,15 +532,58 @@ def run_gpu(args):
         stream.wait_stream(d2h_stream)
         stream.wait_stream(h2d_stream)
 
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = short
     ms_e2e, _, _ = time_steps(e2e_step, e2e_steps, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "e2e")
     d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
     e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": in_bytes,
            "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "pipeline": f"{len(bounds)} segments of {seg_len} tokens, state carried through "
-                       "final_state; host-to-device and device-to-host copies on their own "
-                       "streams, overlapping the kernels"}
+                       "final_state; copies on their own streams, overlapping the kernels"}
     del host, dbuf, out_h, fin_h, inp, out, fin, h2d_stream, d2h_stream
+    torch.cuda.empty_cache()
+
+    # ---------------- packed variable-length batch (8 sequences, 1K-32K tokens) ----------------
+    wv = synth.WORKLOADS["varlen_8seq"]
+    vi = synth.prefill_inputs(wv, dev)
+    Tv = wv.total_tokens
+    vout = torch.empty((Tv, wv.heads, wv.d), dtype=wv.dtype, device=dev)
+    vfin = torch.empty((wv.num_seqs, wv.heads, wv.d, wv.d), dtype=torch.float32, device=dev)
+
+    def varlen_step():
+        kda.kda_prefill(vi["q"], vi["k"], vi["v"], vi["g"], vi["beta"],
+                        init_state=vi["init_state"], cu_seqlens=vi["cu_seqlens"], out=vout,
+                        final_state=vfin, stream=stream)
+
+    v_steps = max(3, min(args.steps, 10))
+    ms_v, _, _ = time_steps(varlen_step, v_steps, 3, world, stream)
+    check_device_status(kda, stream, "varlen_8seq")
+    st_bytes = 2 * vfin.numel() * vfin.element_size()   # initial states read, final written
+    legs["varlen_8seq"] = leg_summary(
+        ms_v, Tv * world, PREFILL_BYTES_PER_TOKEN * Tv + st_bytes, hbm_gbs, v_steps,
+        "kda_prefill_tc_kernel",
+        {"tokens": Tv, "longest": max(wv.lengths),
+         "longest_seq_ms_at_8k_rate": round(ms * max(wv.lengths) / T, 3)})
+    del vi, vout, vfin
+    torch.cuda.empty_cache()
+
+    # ---------------- long context: one 262,144-token sequence ----------------
+    wl = synth.WORKLOADS["prefill_256k"]
+    li = synth.prefill_inputs(wl, dev)
+    Tl = wl.total_tokens
+    lout = torch.empty((Tl, wl.heads, wl.d), dtype=wl.dtype, device=dev)
+    lfin = torch.empty((1, wl.heads, wl.d, wl.d), dtype=torch.float32, device=dev)
+
+    def long_step():
+        kda.kda_prefill(li["q"], li["k"], li["v"], li["g"], li["beta"],
+                        cu_seqlens=li["cu_seqlens"], out=lout, final_state=lfin, stream=stream)
+
+    l_steps = 3
+    ms_l, _, _ = time_steps(long_step, l_steps, 3, world, stream)
+    check_device_status(kda, stream, "prefill_256k")
+    legs["prefill_256k"] = leg_summary(ms_l, Tl * world, PREFILL_BYTES_PER_TOKEN * Tl, hbm_gbs,
+                                       l_steps, "kda_prefill_tc_kernel", {"tokens": Tl})
+    del li, lout, lfin
     torch.cuda.empty_cache()
 
     # ---------------- decode ----------------
@@ -549,24 +602,19 @@ def run_gpu(args):
     # that dominates the run's GPU time
     d_rounds = 1
     ms_round, dt0, dt1 = time_steps(decode_round, d_rounds, 1, world, stream)
+    check_device_status(kda, stream, "decode")
     dclocks = sampler.summary(dt0, dt1) if sampler else None
     ms_dstep = ms_round / wd.steps
     d_tokens = wd.num_seqs
-    d_ach = DECODE_BYTES_PER_HEAD_STEP * wd.num_seqs * wd.heads / (ms_dstep * 1e-3) / 1e9
-    decode = {"value": d_tokens * world / (ms_dstep * 1e-3), "unit": UNIT,
-              "ms_per_step": ms_dstep, "steps_per_round": wd.steps, "rounds": d_rounds,
-              "config": {"workload": "decode_256x64: 256 sequences x 64 single-token steps, "
-                                     "H=96, d=128, fp32 state 1.61 GB (> L2), bf16 q/k/v/o"},
-              "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm_gbs, "unit": "GB/s",
-                           "frac": d_ach / hbm_gbs, "peak_source": peak_src,
-                           "kernel": "kda_decode_kernel",
-                           "traffic": profiled_traffic(
-                               "kda_decode_kernel",
-                               "linear_attention_sequence_gb300/csrc/kda_decode.cu",
-                               "decode_256x64"),
-                           "algorithmic_bytes_per_launch":
-                               DECODE_BYTES_PER_HEAD_STEP * wd.num_seqs * wd.heads},
-              "gpu_launches": d_rounds * wd.steps, "clocks": dclocks}
+    d_bytes = DECODE_BYTES_PER_HEAD_STEP * wd.num_seqs * wd.heads
+    d_ach = d_bytes / (ms_dstep * 1e-3) / 1e9
+    decode = {"tok_s": round(d_tokens * world / (ms_dstep * 1e-3)), "ms_per_step": round(ms_dstep, 5),
+              "frac": round(d_ach / hbm_gbs, 4), "gbs": round(d_ach, 1), "bytes": d_bytes,
+              "peak_gbs": hbm_gbs, "steps": wd.steps * d_rounds, "kernel": "kda_decode_kernel",
+              "traffic": profiled_traffic("kda_decode_kernel",
+                                          "linear_attention_sequence_gb300/csrc/kda_decode.cu",
+                                          "decode_256x64"),
+              "sm_mhz": (dclocks or {}).get("sm_mhz")}
     if sampler:
         sampler.stop()
 
@@ -581,11 +629,13 @@ def run_gpu(args):
                                    "fp32 g/beta/state, zero initial state",
                        "l2": f"inputs {in_bytes / 1e9:.2f} GB > L2 {L2_BYTES / 2**20:.0f} MiB; "
                              "no flush between steps",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "sms": sm_count},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks, "decode": decode,
-            "checkpointed": checkpointed, "gated": gated, "output_gated": output_gated,
-            "scalar_decay": scalar_decay, "backward": backward, "qkv_prologue": qkv_prologue,
+            "gpu_launches": args.steps, "clocks": clocks,
+            "legs": legs,
+            "decode_tokens_per_s": decode["tok_s"], "decode_roofline_frac": decode["frac"],
+            "decode": decode,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

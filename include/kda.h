@@ -365,8 +365,13 @@ kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const v
  *                  kda_prefill_checkpointed writes with interval = KDA_CHUNK
  *                  for the same inputs (row layout as there).  It may be NULL
  *                  only if T_tot <= KDA_CHUNK (then no sequence has a second
- *                  chunk).  Rows at or past chunk_capacity are treated as zero
- *                  states, never read.
+ *                  chunk).  Rows at or past chunk_capacity are never read.  With
+ *                  cu_seqlens NULL a capacity below the rows the batch needs
+ *                  returns KDA_ERR_INVALID_ARGUMENT; with cu_seqlens (lengths
+ *                  known only on the device) a needed row past the capacity is
+ *                  recorded in the device status word, which
+ *                  kda_get_last_device_error then reports as
+ *                  KDA_ERR_INVALID_ARGUMENT (those gradients are not valid).
  *   d_out          device, in_dtype, [T_tot, H, d_v].
  *   d_final_state  device fp32 [N, H, d_k, d_v] or NULL.
  *   dq, dk, dv     device, out_dtype: [T_tot, H, d_k], [T_tot, H, d_k], [T_tot, H, d_v].
@@ -412,13 +417,16 @@ kda_status kda_decode(const kda_dims *dims, const void *q, const void *k, const 
 /*
  * kda_get_last_device_error -- report, then clear, the device-side status.
  *
- * The tensor-core prefill kernel waits on its own asynchronous copies and
- * tensor-core operations with bounded waits; a wait that gives up makes the
- * kernel stop early (outputs of the affected sequences are then incomplete)
- * and records a status word on the device instead of trapping.  This call
- * synchronises `stream`, returns KDA_ERR_TIMEOUT if any kernel recorded such
- * an event since the previous call (else KDA_OK), and resets the word.
- * KDA_ERR_CUDA if the synchronisation itself fails.
+ * The tensor-core prefill kernels wait on their own asynchronous copies,
+ * tensor-core operations and (the split kernel) on each other's CTAs with
+ * bounded waits; a wait that gives up makes the kernel stop early (outputs of
+ * the affected sequences are then incomplete) and records a status word on
+ * the device instead of trapping.  kda_backward records a device-side
+ * argument check there too (a needed chunk-state row past chunk_capacity).
+ * This call synchronises `stream` and, since the previous call, returns
+ * KDA_ERR_INVALID_ARGUMENT if the backward's check failed, else
+ * KDA_ERR_TIMEOUT if any wait gave up, else KDA_OK; then it resets the
+ * words.  KDA_ERR_CUDA if the synchronisation itself fails.
  */
 kda_status kda_get_last_device_error(kda_stream_t stream);
 

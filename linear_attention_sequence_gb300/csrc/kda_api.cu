@@ -103,6 +103,7 @@ kda_status kda_get_last_device_error(kda_stream_t stream) {
     unsigned status = 0;
     cudaError_t e = kda_read_device_status((cudaStream_t)stream, &status);
     if (e != cudaSuccess) return cuda_fail(e, "kda_get_last_device_error");
+    if (status & kda::kBwdMissingState) return KDA_ERR_INVALID_ARGUMENT;
     return status ? KDA_ERR_TIMEOUT : KDA_OK;
 }
 
@@ -183,10 +184,11 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
     // call, else the CUDA-core kernel; the split kernel runs only when it is named
     const bool use_split = P.variant == KDA_PREFILL_TC_SPLIT;
     const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
-    // the tensor-core kernels gate a bf16 output before the store (the one-CTA
-    // kernel loads the gate tile by TMA); every other case gates `out` in place afterwards
-    P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 &&
-                    (use_split || (use_tc && aligned16(P.ogate)));
+    // The split kernel gates a bf16 output in its epilogue, off the state chain's
+    // critical path.  Every other case gates `out` in place after the prefill:
+    // on the one-CTA-per-head kernel the fused epilogue sat on the chain warps and
+    // made the call slower than the two calls.
+    P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 && use_split;
     cudaError_t e = x.noalloc ? kda_launch_prefill_noalloc(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                            out, final_state, s)
                     : use_split ? kda_launch_prefill_chain(P, q, k, v, g, beta, init_state, cu_seqlens, out,
@@ -330,6 +332,11 @@ kda_status kda_backward(const kda_dims *dims, const void *q, const void *k, cons
     if (!cu_seqlens) {
         if (P.N == 0 ? P.T != 0 : P.T % P.N != 0) return KDA_ERR_INVALID_ARGUMENT;
         P.seq_len = P.N ? P.T / P.N : 0;
+        // equal lengths: the chunk-state rows needed are known here.  Sequence n's
+        // rows start at n * floor(T / C) and it reads ceil(T / C) - 1 of them.
+        const int64_t per = P.seq_len / KDA_CHUNK, nch = (P.seq_len + KDA_CHUNK - 1) / KDA_CHUNK;
+        if (P.N > 0 && nch > 1 && chunk_capacity < (int64_t)(P.N - 1) * per + nch - 1)
+            return KDA_ERR_INVALID_ARGUMENT;
     }
     {
         // the gradients must not overwrite what the kernel still reads, nor each other

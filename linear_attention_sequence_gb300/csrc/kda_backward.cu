@@ -39,6 +39,11 @@
 
 #include "kda_common.cuh"
 
+// Device-side argument check of the backward: set when a chunk-state row the
+// gradients need lies past chunk_capacity (only checkable on the device when the
+// sequence lengths come from cu_seqlens).
+__device__ unsigned int g_kda_bwd_status;
+
 namespace {
 
 constexpr int C = 32;          // tokens per chunk (the checkpoint interval)
@@ -111,6 +116,9 @@ kda_backward_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                            : (chunk_states && crow < chunk_capacity)
                                ? chunk_states + (crow * H + h) * sdd
                                : nullptr;
+        // a needed row the caller did not provide: the gradients are wrong, and
+        // kda_get_last_device_error reports KDA_ERR_INVALID_ARGUMENT
+        if (ch > 0 && S0g == nullptr && t == 0) atomicOr(&g_kda_bwd_status, kda::kBwdMissingState);
         __syncthreads();   // the previous chunk is done with every buffer
 
         // ---- load q (into Q1), k (into A1), g (into Gam); rows past the end are 0 ----
@@ -514,4 +522,15 @@ cudaError_t kda_launch_backward(const kda::Problem &P, const void *q, const void
                              dk, dv, dg, dbeta, d_init, stream);
     return dispatch<64>(P, q, k, v, g, beta, init_state, cu, chunk_states, chunk_capacity, d_out, d_final, dq, dk,
                         dv, dg, dbeta, d_init, stream);
+}
+
+// Read and clear the backward's status word (ORed into *status).
+cudaError_t kda_bwd_read_status(unsigned *status) {
+    unsigned st = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&st, g_kda_bwd_status, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_kda_bwd_status, &zero, sizeof(unsigned));
+    *status |= st;
+    return e;
 }

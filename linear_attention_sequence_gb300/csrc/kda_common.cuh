@@ -32,6 +32,11 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int n, int64_t tot
     }
 }
 
+// Bit of the device status word set by a device-side argument check (the
+// backward's missing chunk-state rows); the other bits are bounded waits that
+// gave up.
+constexpr unsigned kBwdMissingState = 0x1000u;
+
 // Host-side launch parameters after validation.
 struct Problem {
     int32_t N, T, H, dk, dv;
@@ -139,6 +144,7 @@ cudaError_t kda_launch_prefill_chain(const kda::Problem &P, const void *q, const
                                      const float *init_state, const int32_t *cu, void *out,
                                      float *final_state, cudaStream_t stream);
 cudaError_t kda_chain_read_status(unsigned *status);
+cudaError_t kda_bwd_read_status(unsigned *status);
 bool kda_prefill_noalloc_fits(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const void *out);
 cudaError_t kda_launch_prefill_noalloc(const kda::Problem &P, const void *q, const void *k,

@@ -62,9 +62,9 @@ template <int DK, int C, typename IN_T, typename OUT_T>
 __global__ void __launch_bounds__(kThreads)
 kda_prefill_fp32_kernel(const IN_T *__restrict__ q, const IN_T *__restrict__ k,
                         const IN_T *__restrict__ v, const float *__restrict__ g,
-                        const float *__restrict__ beta, const float *__restrict__ init_state,
+                        const float *__restrict__ beta, const float *init_state,
                         const int32_t *__restrict__ cu, OUT_T *__restrict__ out,
-                        float *__restrict__ final_state, int H, int DV, int64_t total,
+                        float *final_state, int H, int DV, int64_t total,
                         int64_t seq_len, float *__restrict__ ckpt, int64_t ckpt_every,
                         int64_t ckpt_cap, const IN_T *__restrict__ z,
                         const float *__restrict__ a_log, int sdecay,

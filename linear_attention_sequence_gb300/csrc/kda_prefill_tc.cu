@@ -122,22 +122,19 @@ static_assert(4 * 64 * 32 * 4 <= sizeof(Stage), "readout operand fits in a stage
 
 struct alignas(1024) TcSmem {
     Stage in[2];                // TMA destinations, double-buffered
-    unsigned char ostage[2][kTileF32];   // output rows of a full chunk, stored by TMA (SW128);
-                                         // with a bf16 output and the output gate, the gate
-                                         // logits of the chunk in the upper half
+    unsigned char ostage[2][kTileF32];   // output rows of a full chunk, stored by TMA (SW128)
     float gramA[4 * 64 * 32];   // staging of the Gram A operand [k~ ; q~] (tf32), copied to TMEM
     float gramB[4 * 32 * 32];   // Gram B operand k e^{Gamma_15 - Gamma}
     float kbaq[2][160 * 32];    // [Kbar^T ; Aqk]: B operand of the state-carry + readout MMA
     float tmat[2][32 * 32];     // T diag(beta): B operand of the U' MMA and, negated, of the U MMA
     float akkT[32][32];         // solve scratch: (beta-scaled strict lower Akk)^T
     float tsc[3][16][20];       // solve scratch: T11 by rows, T22^T, A21 T11 (rows padded)
-    float ored[4][32];          // output gate: per-warp partial sums of o~^2 by row
     float betaS[kBetaRing][C];
     float ghS[kBetaRing][C];    // one log-decay per token (scalar-decay variants), like beta
     float gamC[2][D];           // e^{Gamma_last}: state decay over the chunk
     float gref[D], e01[D], e1l[D];
     uint64_t bar_tma[2], bar_gram[2], bar_bxfull[2], bar_gops[2], bar_akempty[2];
-    uint64_t bar_x, bar_u, bar_s, bar_fin[3], bar_og[2];
+    uint64_t bar_x, bar_u, bar_s, bar_fin[3];
     uint32_t tma_issued[2];     // stage loads issued / awaited (for the drain after a stop)
     uint32_t tma_awaited[2];
     uint32_t tmem_base;
@@ -519,22 +516,18 @@ __device__ __forceinline__ void scale_state(TcSmem &sm, uint32_t tl, int st) {
 // Chain warps (8-11): everything of chunk n from its Gram on.  Thread j owns
 // TMEM lane j = value index j; warps 8 and 9 read the Gram rows (lanes 0-63).
 // ---------------------------------------------------------------------------
-template <typename OUT_T, bool OGATE>
+template <typename OUT_T>
 __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, const CUtensorMap *mk,
                                            const CUtensorMap *mv, const CUtensorMap *mg,
-                                           const CUtensorMap *mo, const CUtensorMap *mog,
-                                           OUT_T *__restrict__ out, int H, int h,
-                                           int64_t a, int64_t b, int nchunks, uint32_t tb,
+                                           const CUtensorMap *mo, OUT_T *__restrict__ out, int H,
+                                           int h, int64_t a, int64_t b, int nchunks, uint32_t tb,
                                            float *__restrict__ ckpt, int64_t ckpt_every,
-                                           int64_t ckpt_cap, int64_t ck_row0, int gmode, float wj,
-                                           float oeps) {
-    static_assert(!OGATE || sizeof(OUT_T) == 2, "the fused output gate stages a bf16 output");
+                                           int64_t ckpt_cap, int64_t ck_row0, int gmode) {
     const int j = threadIdx.x - kPrep;   // 0..127
     const int warp = threadIdx.x >> 5, cw = j >> 5, lane = j & 31;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const bool issuer = j == 0, xissuer = j == 96, ostorer = j == 32;
     uint32_t bxf_par[2] = {0, 0}, gops_par[2] = {0, 0}, gram_par[2] = {0, 0}, x_par = 0, u_par = 0, s_par = 0;
-    uint32_t og_par[2] = {0, 0}, og_issued[2] = {0, 0}, og_awaited[2] = {0, 0};   // output gate tiles
 
     for (int n = 0; n < nchunks; ++n) {
         const int st = n & 1;
@@ -551,13 +544,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             // the state and the readout operand, so it runs while warps 8, 9
             // extract and solve; then S^T <- S^T Diag(e^{Gamma_last}) on lanes 64-127. ----
             if (xissuer) {
-                if (OGATE) {
-                    // the gate logits of chunk n into the upper half of its staging tile
-                    // (that half was last read by the epilogue of chunk n-2)
-                    mbar_arrive_expect_tx(&sm.bar_og[st], kTileBf16);
-                    tma_load_3d(sm.ostage[st] + kTileBf16, mog, &sm.bar_og[st], 0, (int)t0, 2 * h);
-                    og_issued[st] += 1;
-                }
                 if (wait_phase(sm, &sm.bar_bxfull[st], bxf_par[st], 64u)) {
                     tc_fence_after();
                     const uint64_t dX = sdesc_sw128(smem_u32(&sm.in[st]));   // the chunk's stage
@@ -723,10 +709,8 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
         }
         // the output staging buffer of this parity was last stored for chunk n-2
         if (ostorer) bulk_wait_group_read<1>();
-        if (OGATE && xissuer && wait_phase(sm, &sm.bar_og[st], og_par[st], 16u)) og_awaited[st] += 1;
         __syncwarp();
         s_par ^= 1u;
-        if (OGATE) og_par[st] ^= 1u;
         named_sync(BAR_CHAIN, kChain);
         tc_fence_after();
 
@@ -735,40 +719,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
         float o0[16], o1[16];
         tmem_ld16x2(tb + lane_off + TM_X, tb + lane_off + TM_X + 16, o0, o1);
         tc_fence_before();
-        if (OGATE) {
-            // output gate: o_r <- Sigmoid(gate_r) o_r / sqrt(mean_j o_rj^2 + eps) w_j.
-            // Sum of squares of row r over the 128 value channels: a reduce-scatter
-            // inside each warp (lane L ends with the warp's sum for row L), then
-            // the four warps' partial sums through shared memory.
-            float a2[32];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                a2[r] = o0[r] * o0[r];
-                a2[16 + r] = o1[r] * o1[r];
-            }
-#pragma unroll
-            for (int sh = 16; sh >= 1; sh >>= 1) {
-                const bool up = (lane & sh) != 0;
-#pragma unroll
-                for (int i = 0; i < sh; ++i) {
-                    const float send = up ? a2[i] : a2[i + sh];
-                    const float keep = up ? a2[i + sh] : a2[i];
-                    a2[i] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
-                }
-            }
-            sm.ored[cw][lane] = a2[0];
-            named_sync(BAR_CHAIN, kChain);
-            const float ms = (sm.ored[0][lane] + sm.ored[1][lane] + sm.ored[2][lane] +
-                              sm.ored[3][lane]) * (1.f / D);
-            const float rinv = rsqrtf(ms + oeps);   // of row `lane`, broadcast below
-            const unsigned char *gt = sm.ostage[st] + kTileBf16;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                o0[r] *= __shfl_sync(0xffffffffu, rinv, r) * wj * kda::sigmoid_f(ld_bf16(gt, r, j));
-                o1[r] *= __shfl_sync(0xffffffffu, rinv, 16 + r) * wj *
-                         kda::sigmoid_f(ld_bf16(gt, 16 + r, j));
-            }
-        }
         if (L == C) {
             // a full chunk: rows into the staging tile, one TMA store
             unsigned char *stg = sm.ostage[st];
@@ -814,10 +764,6 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
         }
     }
     if (ostorer) bulk_wait_group_all();   // every output store has been performed
-    if (OGATE && xissuer)                 // gate tiles loaded but not awaited (after a stop)
-        for (int s2 = 0; s2 < 2; ++s2)
-            if (og_issued[s2] > og_awaited[s2])
-                mbar_wait_bounded(&sm.bar_og[s2], (og_issued[s2] - 1) & 1u, kPollLimit);
     if (issuer || xissuer) {   // every MMA issued here has completed
         uint64_t *fin = &sm.bar_fin[issuer ? 1 : 2];
         mma_commit(fin);
@@ -825,19 +771,19 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
     }
 }
 
-template <typename OUT_T, bool GATED, bool OGATE, bool SDECAY>
+// init_state and final_state may be the same array (each CTA reads its slice
+// before it writes it), so neither is declared __restrict__.
+template <typename OUT_T, bool GATED, bool SDECAY>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_g,
-                      const __grid_constant__ CUtensorMap tm_o,
-                      const __grid_constant__ CUtensorMap tm_og, const float *__restrict__ beta,
-                      const float *__restrict__ init_state, const int32_t *__restrict__ cu,
-                      OUT_T *__restrict__ out, float *__restrict__ final_state, int H,
+                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ beta,
+                      const float *init_state, const int32_t *__restrict__ cu,
+                      OUT_T *__restrict__ out, float *final_state, int H,
                       int64_t total, int64_t seq_len, float *__restrict__ ckpt,
                       int64_t ckpt_every, int64_t ckpt_cap, const float *__restrict__ a_log,
-                      const float *__restrict__ onorm_w, float oeps,
                       const float *__restrict__ g_head) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // Round up to 1024 bytes by pointer arithmetic on the shared array itself
@@ -863,8 +809,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&sm.bar_fin[s], 1);
         }
         mbar_init(&sm.bar_fin[2], 1);
-        mbar_init(&sm.bar_og[0], 1);
-        mbar_init(&sm.bar_og[1], 1);
         mbar_init(&sm.bar_x, 1);
         mbar_init(&sm.bar_u, 1);
         mbar_init(&sm.bar_s, 1);
@@ -877,7 +821,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
         prefetch_tmap(&tm_o);
-        if (OGATE) prefetch_tmap(&tm_og);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -918,11 +861,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         prep_loop<GATED, SDECAY>(sm, &tm_q, &tm_k, &tm_v, &tm_g, beta, g_head, H, h, a, b, nchunks,
                                  tb, GATED ? __expf(a_log[h]) : 0.f);
     else
-        chain_loop<OUT_T, OGATE>(sm, &tm_q, &tm_k, &tm_v, &tm_g, &tm_o, &tm_og, out, H, h, a, b,
-                                 nchunks, tb, ckpt, ckpt_every, ckpt_cap,
-                                 ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0,
-                                 GATED ? kDecayLogits : SDECAY ? kDecayScalar : kDecayTile,
-                                 OGATE && onorm_w ? onorm_w[t - kPrep] : 1.f, oeps);
+        chain_loop<OUT_T>(sm, &tm_q, &tm_k, &tm_v, &tm_g, &tm_o, out, H, h, a, b, nchunks, tb,
+                          ckpt, ckpt_every, ckpt_cap,
+                          ckpt ? kda::ckpt_first_row(cu, n, total, seq_len, ckpt_every * C) : 0,
+                          GATED ? kDecayLogits : SDECAY ? kDecayScalar : kDecayTile);
 
     tc_fence_before();
     __syncthreads();
@@ -987,7 +929,7 @@ template <typename OUT_T>
 cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const void *v,
                    const float *g, const float *beta, const float *init_state, const int32_t *cu,
                    void *out, float *final_state, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv, mg, mo, mog;
+    CUtensorMap mq, mk, mv, mg, mo;
     if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
@@ -997,29 +939,18 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
         !(sizeof(OUT_T) == 2 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
                              : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
         return cudaErrorInvalidValue;
-    mog = mq;   // not read unless the output gate is fused
-    auto kern = P.a_log          ? kda_prefill_tc_kernel<OUT_T, true, false, false>
-                : P.scalar_decay ? kda_prefill_tc_kernel<OUT_T, false, false, true>
-                                 : kda_prefill_tc_kernel<OUT_T, false, false, false>;
-    if constexpr (sizeof(OUT_T) == 2) {
-        // the output gate, fused for a bf16 output (with plain g and beta)
-        if (P.ogate_fused) {
-            if (P.a_log || P.scalar_decay ||
-                !make_map(&mog, P.ogate, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H))
-                return cudaErrorInvalidValue;
-            kern = kda_prefill_tc_kernel<OUT_T, false, true, false>;
-        }
-    }
+    auto kern = P.a_log          ? kda_prefill_tc_kernel<OUT_T, true, false>
+                : P.scalar_decay ? kda_prefill_tc_kernel<OUT_T, false, true>
+                                 : kda_prefill_tc_kernel<OUT_T, false, false>;
     const size_t smem = sizeof(TcSmem) + 1024;
     static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned blocks = (unsigned)((int64_t)P.N * P.H);
-    kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, mo, mog, beta, init_state, cu,
+    kern<<<blocks, kThreads, smem, stream>>>(mq, mk, mv, mg, mo, beta, init_state, cu,
                                              (OUT_T *)out, final_state, P.H, (int64_t)P.T,
                                              P.seq_len, P.ckpt, P.ckpt ? P.ckpt_interval / C : 1,
-                                             P.ckpt_capacity, P.a_log, P.onorm_w, P.oeps,
-                                             P.g_head);
+                                             P.ckpt_capacity, P.a_log, P.g_head);
     return cudaGetLastError();
 }
 
@@ -1071,5 +1002,7 @@ cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(unsigned));
     if (e != cudaSuccess) return e;
-    return kda_chain_read_status(status);   // the split kernel's status word
+    e = kda_chain_read_status(status);   // the split kernel's status word
+    if (e != cudaSuccess) return e;
+    return kda_bwd_read_status(status);  // the backward's argument check
 }

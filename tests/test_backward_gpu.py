@@ -122,3 +122,27 @@ def test_backward_8k_layer_sampled_heads():
     ref = _oracle_grads(inp, d_out, d_fin, None, heads=heads)
     errs = _check(res, ref, TOL[torch.bfloat16], heads=heads)
     print("backward 8k layer (2 heads): " + " ".join(f"{k} {v:.2e}" for k, v in errs.items()))
+
+
+def test_missing_chunk_states_are_reported():
+    """Chunk-state rows past chunk_capacity: rejected on the host when the lengths
+    are known there (no cu_seqlens), reported by the device status otherwise."""
+    dev = "cuda"
+    inp = synth.random_inputs(96, 2, 128, dtype=torch.bfloat16, seed=31, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(32)
+    d_out = torch.randn(inp["q"].shape, generator=gen, device=dev).to(torch.bfloat16)
+    _, _, cs = kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                            interval=kda.CHUNK)
+    short = cs[:1].contiguous()   # 96 tokens need 2 rows (the starts of chunks 1 and 2)
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                         chunk_states=short)
+    assert e.value.status == 1
+    cu = torch.tensor([0, 96], dtype=torch.int32, device=dev)
+    kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                     cu_seqlens=cu, chunk_states=short)
+    assert kda.kda_get_last_device_error() == 1      # KDA_ERR_INVALID_ARGUMENT
+    assert kda.kda_get_last_device_error() == 0      # cleared by the read
+    kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
+                     cu_seqlens=cu, chunk_states=cs)
+    assert kda.kda_get_last_device_error() == 0

@@ -121,6 +121,23 @@ def test_final_state_may_alias_init(variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+def test_final_state_may_alias_init_packed(variant):
+    """In place over a packed batch of several multi-chunk sequences: every
+    (sequence, head) slice is read before it is overwritten."""
+    lens = [70, 33, 130, 0, 64]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    inp = synth.random_inputs(sum(lens), 3, 128, dtype=torch.bfloat16, seed=9, device=DEV,
+                              num_seqs=len(lens), init_std=0.05)
+    out_a, fin_a = run_gpu(inp, variant, cu=cu)
+    st = inp["init_state"].clone()
+    out_b, _ = kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                               init_state=st, final_state=st, cu_seqlens=cu,
+                               out_dtype=torch.float32, variant=variant)
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(fin_a, st)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_zero_tokens_copies_state(variant):
     N, H, d = 3, 2, 128
     init = torch.randn(N, H, d, d, device=DEV)
@@ -384,7 +401,7 @@ def check_bf16_out(out, y_ref, dtype):
 def test_output_gated_matches_oracle(variant, d, dtype, out_dtype):
     """kda_prefill_output_gated on a ragged packed batch against the oracle's
     prefill followed by the oracle's output gate.  A bf16 output on the
-    tensor-core path takes the fused epilogue; the other cases gate in place."""
+    split kernel takes the fused epilogue; the other cases gate in place."""
     if not supported(variant, d, dtype):
         pytest.skip("variant does not take this shape/dtype")
     H = 2
@@ -412,8 +429,8 @@ def test_output_gate_of_the_kernels_own_readout(variant, out_dtype):
     """The epilogue alone: the gated output equals the gate applied in fp64 to
     the ungated fp32 readout the same kernel writes (kda_prefill), to fp32
     rounding (fp32 out).  A bf16 out is one bf16 rounding away on the fused
-    tensor-core path, and at most two on the in-place path (o~ itself goes
-    through bf16 there).  Full chunks and a ragged tail; no weight, then a
+    path (the split kernel), and at most two on the in-place path (o~ itself
+    goes through bf16 there).  Full chunks and a ragged tail; no weight, then a
     weight."""
     T, H, d = 150, 3, 128
     dtype = torch.float32 if supported(variant, d, torch.float32) else torch.bfloat16
@@ -431,7 +448,9 @@ def test_output_gate_of_the_kernels_own_readout(variant, out_dtype):
         if out_dtype == torch.float32:
             assert np.allclose(host64(out), y, rtol=2e-6, atol=1e-6 * np.abs(y).max())
         else:
-            fused = dtype == torch.bfloat16   # this shape on bf16 inputs runs the tensor-core kernel
+            # only the split kernel fuses the gate into its epilogue; every other case
+            # gates a bf16 `out` in place after the prefill
+            fused = dtype == torch.bfloat16 and variant == kda.PREFILL_TC_SPLIT
             rel = 2.0 ** -8 if fused else 2.0 ** -7
             assert np.all(np.abs(host64(out) - y) <= rel * np.abs(y) + 1e-6 * np.abs(y).max())
 
