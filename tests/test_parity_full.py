@@ -1,9 +1,10 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
 benchmark times (default variant, whole batch in one call).  Every (sequence,
 head) pair is independent, so the oracle checks all of them where it finishes
-in seconds (the 8K prefill, the decode workload) and a seeded sample of
-pairs, each over its whole length, where it does not (the packed varlen batch,
-the 256K context)."""
+in seconds (the 8K prefill, the decode workload), every sequence with a
+quarter of the heads for the packed varlen batch, and 16 heads over the whole
+length of the 262,144-token context (host memory and the oracle's minutes
+bound the rest)."""
 import numpy as np
 import pytest
 import torch
@@ -23,20 +24,6 @@ def _gpu(inp, out_dtype):
                            out_dtype=out_dtype)
 
 
-def _oracle_pairs(inp, pairs):
-    """Run the oracle on the given (sequence, head) pairs; returns lists of
-    (slice, head, o_ref, s_ref)."""
-    cu = inp["cu_seqlens"].cpu().numpy()
-    res = []
-    for n, h in pairs:
-        sl = slice(int(cu[n]), int(cu[n + 1]))
-        args = [host64(inp[x][sl, h:h + 1]) for x in ("q", "k", "v", "g", "beta")]
-        init = None if inp["init_state"] is None else host64(inp["init_state"][n:n + 1, h:h + 1])
-        o, s = oracle.prefill(*args, init_state=init)
-        res.append((n, sl, h, o[:, 0], s[0, 0]))
-    return res
-
-
 def test_prefill_8k_all_heads():
     w = synth.WORKLOADS["prefill_8k"]
     inp = synth.prefill_inputs(w, DEV)
@@ -50,37 +37,46 @@ def test_prefill_8k_all_heads():
     assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
 
 
-def test_varlen_packed_sampled_pairs():
+def _oracle_heads(inp, n, heads):
+    """The oracle on sequence n for the given heads, in one threaded call."""
+    cu = inp["cu_seqlens"].cpu().numpy()
+    sl = slice(int(cu[n]), int(cu[n + 1]))
+    args = [host64(inp[x][sl][:, heads]) for x in ("q", "k", "v", "g", "beta")]
+    init = None if inp["init_state"] is None else host64(inp["init_state"][n:n + 1][:, heads])
+    o, s = oracle.prefill(*args, init_state=init, num_threads=oracle.num_cpus())
+    return sl, o, s[0]
+
+
+def test_varlen_packed_every_sequence():
+    """All eight sequences of the packed batch (nonzero initial states), 24 of
+    the 96 heads each (every fourth head), against the oracle."""
     w = synth.WORKLOADS["varlen_8seq"]
     inp = synth.prefill_inputs(w, DEV)
     out32, fin32 = _gpu(inp, torch.float32)
-    rng = np.random.default_rng(2024)
-    longest = int(np.argmax(w.lengths))
-    pairs = [(longest, 0), (longest, w.heads - 1)] + [
-        (int(rng.integers(w.num_seqs)), int(rng.integers(w.heads))) for _ in range(6)]
-    o_all, s_all = [], []
-    g_o, g_s = [], []
-    for n, sl, h, o, s in _oracle_pairs(inp, pairs):
-        o_all.append(o); s_all.append(s)
-        g_o.append(host64(out32[sl, h])); g_s.append(host64(fin32[n, h]))
+    heads = list(range(0, w.heads, 4))
+    g_o, g_s, o_all, s_all = [], [], [], []
+    for n in range(w.num_seqs):
+        sl, o, s = _oracle_heads(inp, n, heads)
+        o_all.append(o.reshape(-1)); s_all.append(s.reshape(-1))
+        g_o.append(host64(out32[sl][:, heads]).reshape(-1))
+        g_s.append(host64(fin32[n][heads]).reshape(-1))
     eo = rel_err(np.concatenate(g_o), np.concatenate(o_all))
-    es = rel_err(np.stack(g_s), np.stack(s_all))
-    print(f"varlen_8seq (8 pairs): err_o {eo:.3e} err_S {es:.3e}")
+    es = rel_err(np.concatenate(g_s), np.concatenate(s_all))
+    print(f"varlen_8seq (8 sequences x 24 heads): err_o {eo:.3e} err_S {es:.3e}")
     assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
 
 
-def test_prefill_256k_sampled_heads():
+def test_prefill_256k_sixteen_heads():
+    """The 262,144-token context (long retention, x ~ N(4, 1)): 16 heads spread
+    over the 96, each over its whole length."""
     w = synth.WORKLOADS["prefill_256k"]
     inp = synth.prefill_inputs(w, DEV)
     out32, fin32 = _gpu(inp, torch.float32)
-    pairs = [(0, 0), (0, 41), (0, 95)]
-    g_o, g_s, o_all, s_all = [], [], [], []
-    for n, sl, h, o, s in _oracle_pairs(inp, pairs):
-        o_all.append(o); s_all.append(s)
-        g_o.append(host64(out32[sl, h])); g_s.append(host64(fin32[n, h]))
-    eo = rel_err(np.concatenate(g_o), np.concatenate(o_all))
-    es = rel_err(np.stack(g_s), np.stack(s_all))
-    print(f"prefill_256k (3 heads): err_o {eo:.3e} err_S {es:.3e}")
+    heads = list(range(0, w.heads, 6))
+    sl, o, s = _oracle_heads(inp, 0, heads)
+    eo = rel_err(host64(out32[sl][:, heads]), o)
+    es = rel_err(host64(fin32[0][heads]), s)
+    print(f"prefill_256k (16 heads): err_o {eo:.3e} err_S {es:.3e}")
     assert eo <= TOL[torch.bfloat16] and es <= TOL[torch.bfloat16]
     assert torch.isfinite(out32).all() and torch.isfinite(fin32).all()
 
@@ -144,9 +140,9 @@ def test_gated_prefill_8k_sampled_heads():
 
 
 def test_output_gated_8k_sampled_heads():
-    """The 8K layer with the output gate fused into the store (bf16 out, the
-    launch the benchmark times): three heads against the oracle's prefill
-    followed by the oracle's output gate."""
+    """The 8K layer through kda_prefill_output_gated (bf16 out, the launch the
+    benchmark times: the prefill, then the gate in place): three heads against
+    the oracle's prefill followed by the oracle's output gate."""
     w = synth.WORKLOADS["prefill_8k"]
     inp = synth.prefill_inputs(w, "cuda")
     og = synth.output_gate_inputs(w.total_tokens, w.heads, w.d, dtype=w.dtype, seed=83,
