@@ -378,6 +378,17 @@ def run_gpu(args):
     legs["split"] = leg_summary(ms_sp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
                                 "kda_prefill_chain_kernel")
 
+    # ---------------- the same layer in two passes (intra-chunk products, then the chain) ----
+    def two_pass_step():
+        kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                        cu_seqlens=inp["cu_seqlens"], out=out, final_state=fin,
+                        variant=kda.PREFILL_TC_2PASS, stream=stream)
+
+    ms_tp, _, _ = time_steps(two_pass_step, short, max(args.warmup, 3), world, stream)
+    check_device_status(kda, stream, "two_pass")
+    legs["two_pass"] = leg_summary(ms_tp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
+                                   "kda_intra_kernel + kda_chain2_kernel")
+
     # ---------------- the same layer with state checkpoints every 1024 tokens ----------------
     interval = 1024
     ck = torch.empty((kda.checkpoint_count(T, interval, inp["cu_seqlens"]), w.heads, w.d, w.d),

@@ -16,11 +16,12 @@
  * Conventions shared by every entry point
  * ----------------------------------------
  *  - All tensors are row-major and contiguous, in DEVICE memory, owned by
- *    the caller.  The library allocates no device memory, with one exception:
- *    the KDA_PREFILL_TC_SPLIT prefill variant takes stream-ordered scratch
- *    (its ring of chunk operands, about 0.28 MB per (sequence, head) it runs
- *    at once, at most 27 MB) from a memory pool of the library's own, and
- *    returns it on the same stream when the call's work is done.
+ *    the caller.  The library allocates no device memory, with two
+ *    exceptions: the KDA_PREFILL_TC_SPLIT prefill variant (its ring of chunk
+ *    operands, about 0.28 MB per (sequence, head) it runs at once, at most
+ *    27 MB) and the KDA_PREFILL_TC_2PASS variant (8 KB per chunk and head)
+ *    take stream-ordered scratch from a memory pool of the library's own, and
+ *    return it on the same stream when the call's work is done.
  *  - q, k  [T_tot, H, d_k];  v, out [T_tot, H, d_v];  g [T_tot, H, d_k] fp32
  *    (log-decay); beta [T_tot, H] fp32; states [N, H, d_k, d_v] fp32 with row
  *    i = key channel i (the decay scales rows: "Hybrid Attention", section
@@ -60,17 +61,22 @@ typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
 /* Prefill kernel selection: a diagnostic and test selector, not a tuning
  * knob.  KDA_PREFILL_DEFAULT (what callers should pass) picks TC where it
- * supports the call, else FP32.  TC_SPLIT runs only when named (it is slower
- * than TC on the 96-head layer).  The tensor-core kernels take d_k = d_v =
- * 128, bf16 q/k/v, and q, k, v, g (or z) and out 16-byte aligned; TC_SPLIT
- * also needs a device that supports cooperative launches.  Naming a variant
- * that does not support the call returns KDA_ERR_UNSUPPORTED. */
+ * supports the call, else FP32.  TC_SPLIT and TC_2PASS run only when named
+ * (both are slower than TC on the 96-head layer).  The tensor-core kernels
+ * take d_k = d_v = 128, bf16 q/k/v, and q, k, v, g (or z) and out 16-byte
+ * aligned; TC_SPLIT also needs a device that supports cooperative launches.
+ * TC_2PASS takes 8 KB of stream-ordered scratch per chunk and head (about
+ * 0.2 GB for a 96-head, 8192-token layer) from a pool of the library's own.
+ * Naming a variant that does not support the call returns
+ * KDA_ERR_UNSUPPORTED. */
 typedef enum {
     KDA_PREFILL_DEFAULT = 0,
     KDA_PREFILL_FP32 = 1,     /* CUDA-core fp32 chunked kernel (any supported shape) */
     KDA_PREFILL_TC = 2,       /* tcgen05 kernel, one CTA per (sequence, head) (d = 128) */
-    KDA_PREFILL_TC_SPLIT = 3  /* tcgen05 kernel with the state recurrence and the intra-chunk
+    KDA_PREFILL_TC_SPLIT = 3, /* tcgen05 kernel with the state recurrence and the intra-chunk
                                  work on different SMs, one cooperative launch (d = 128) */
+    KDA_PREFILL_TC_2PASS = 4  /* tcgen05, two launches: the intra-chunk products of every
+                                 chunk on every SM, then the state recurrence (d = 128) */
 } kda_prefill_variant;
 
 typedef void *kda_stream_t; /* a cudaStream_t */

@@ -29,14 +29,14 @@ __all__ = ["KdaError", "kda_prefill", "kda_prefill_noalloc", "kda_prefill_checkp
            "kda_output_gate", "kda_qkv_prologue", "checkpoint_count", "kda_decode",
            "kda_status_string", "lib", "library_path",
            "kda_get_last_device_error", "kda_selftest_timeout",
-           "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "PREFILL_TC_SPLIT", "Dims"]
+           "PREFILL_DEFAULT", "PREFILL_FP32", "PREFILL_TC", "PREFILL_TC_SPLIT", "PREFILL_TC_2PASS", "Dims"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libkda.so")
 
 KDA_OK = 0
 DTYPE_F32, DTYPE_BF16 = 0, 1
-PREFILL_DEFAULT, PREFILL_FP32, PREFILL_TC, PREFILL_TC_SPLIT = 0, 1, 2, 3
+PREFILL_DEFAULT, PREFILL_FP32, PREFILL_TC, PREFILL_TC_SPLIT, PREFILL_TC_2PASS = 0, 1, 2, 3, 4
 CHUNK = 32   # chunk length of the prefill kernels (KDA_CHUNK)
 _DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}
 

@@ -56,7 +56,7 @@ kda_status check_dims(const kda_dims *d, kda::Problem &P) {
     if (d->num_seqs < 0 || d->total_tokens < 0 || d->num_heads < 1 || d->d_k < 1 || d->d_v < 1)
         return KDA_ERR_INVALID_ARGUMENT;
     if (!valid_dtype(d->in_dtype) || !valid_dtype(d->out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
-    if (d->variant < KDA_PREFILL_DEFAULT || d->variant > KDA_PREFILL_TC_SPLIT) return KDA_ERR_INVALID_ARGUMENT;
+    if (d->variant < KDA_PREFILL_DEFAULT || d->variant > KDA_PREFILL_TC_2PASS) return KDA_ERR_INVALID_ARGUMENT;
     if (d->d_k != d->d_v || (d->d_k != 64 && d->d_k != 128)) return KDA_ERR_UNSUPPORTED;
     // element counts must fit the kernels' 64-bit index arithmetic comfortably
     const int64_t elems = (int64_t)d->total_tokens * d->num_heads * d->d_k;
@@ -178,19 +178,24 @@ kda_status prefill_common(const kda_dims *dims, const void *q, const void *k, co
                                     : tc_ok && kda_prefill_chain_supported(P, q, k, v, (const float *)g_in, out);
     if (P.variant == KDA_PREFILL_TC && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (P.variant == KDA_PREFILL_TC_SPLIT && !split_ok) return KDA_ERR_UNSUPPORTED;
+    const bool twopass_ok = tc_ok && kda_prefill_2pass_supported(P);
+    if (P.variant == KDA_PREFILL_TC_2PASS && !twopass_ok) return KDA_ERR_UNSUPPORTED;
     if (P.N == 0) return KDA_OK;
     cudaStream_t s = (cudaStream_t)stream;
     // the default takes the one-CTA-per-head tensor-core kernel where it supports the
     // call, else the CUDA-core kernel; the split kernel runs only when it is named
     const bool use_split = P.variant == KDA_PREFILL_TC_SPLIT;
+    const bool use_2pass = P.variant == KDA_PREFILL_TC_2PASS;
     const bool use_tc = P.variant == KDA_PREFILL_TC || (P.variant == KDA_PREFILL_DEFAULT && tc_ok);
     // The split kernel gates a bf16 output in its epilogue, off the state chain's
     // critical path.  Every other case gates `out` in place after the prefill:
     // on the one-CTA-per-head kernel the fused epilogue sat on the chain warps and
     // made the call slower than the two calls.
-    P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 && use_split;
+    P.ogate_fused = P.ogate && !P.a_log && P.out_dtype == KDA_DTYPE_BF16 && (use_split || use_2pass);
     cudaError_t e = x.noalloc ? kda_launch_prefill_noalloc(P, q, k, v, g, beta, init_state, cu_seqlens,
                                                            out, final_state, s)
+                    : use_2pass ? kda_launch_prefill_2pass(P, q, k, v, g, beta, init_state, cu_seqlens, out,
+                                                           final_state, s)
                     : use_split ? kda_launch_prefill_chain(P, q, k, v, g, beta, init_state, cu_seqlens, out,
                                                          final_state, s)
                     : use_tc  ? kda_launch_prefill_tc(P, q, k, v, g, beta, init_state, cu_seqlens,

@@ -151,6 +151,12 @@ cudaError_t kda_launch_prefill_noalloc(const kda::Problem &P, const void *q, con
                                        const void *v, const float *g, const float *beta,
                                        const float *init_state, const int32_t *cu, void *out,
                                        float *final_state, cudaStream_t stream);
+bool kda_prefill_2pass_supported(const kda::Problem &P);
+cudaError_t kda_launch_prefill_2pass(const kda::Problem &P, const void *q, const void *k,
+                                     const void *v, const float *g, const float *beta,
+                                     const float *init_state, const int32_t *cu, void *out,
+                                     float *final_state, cudaStream_t stream);
+cudaError_t kda_2pass_read_status(unsigned *status);
 cudaError_t kda_launch_prefill_fp32(const kda::Problem &P, const void *q, const void *k,
                                     const void *v, const float *g, const float *beta,
                                     const float *init_state, const int32_t *cu, void *out,

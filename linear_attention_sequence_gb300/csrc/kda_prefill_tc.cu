@@ -956,6 +956,13 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
 
 }  // namespace
 
+// The 3-D TMA view of a [T, H, 128] tensor (box: one head's 128-byte segments
+// for 32 tokens, 128-byte swizzle), for the other kernels that load chunk tiles.
+bool kda_make_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                       int64_t T, int H) {
+    return make_map(m, base, dt, esize, T, H);
+}
+
 bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const void *out) {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
@@ -1003,6 +1010,8 @@ cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
     e = cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     e = kda_chain_read_status(status);   // the split kernel's status word
+    if (e != cudaSuccess) return e;
+    e = kda_2pass_read_status(status);   // the two-pass kernels' status word
     if (e != cudaSuccess) return e;
     return kda_bwd_read_status(status);  // the backward's argument check
 }

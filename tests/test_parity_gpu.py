@@ -13,13 +13,14 @@ from kda_testutil import TOL, rel_err, host64
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-VARIANTS = [kda.PREFILL_DEFAULT, kda.PREFILL_FP32, kda.PREFILL_TC, kda.PREFILL_TC_SPLIT]
+VARIANTS = [kda.PREFILL_DEFAULT, kda.PREFILL_FP32, kda.PREFILL_TC, kda.PREFILL_TC_SPLIT,
+            kda.PREFILL_TC_2PASS]
 
 
 def supported(variant, d, dtype):
     """The tensor-core kernel takes d = 128 with bf16 inputs only (its tf32
     operands cannot meet the 1e-4 bound of fp32 inputs)."""
-    if variant in (kda.PREFILL_TC, kda.PREFILL_TC_SPLIT):
+    if variant in (kda.PREFILL_TC, kda.PREFILL_TC_SPLIT, kda.PREFILL_TC_2PASS):
         return d == 128 and dtype == torch.bfloat16
     return True
 
@@ -450,7 +451,7 @@ def test_output_gate_of_the_kernels_own_readout(variant, out_dtype):
         else:
             # only the split kernel fuses the gate into its epilogue; every other case
             # gates a bf16 `out` in place after the prefill
-            fused = dtype == torch.bfloat16 and variant == kda.PREFILL_TC_SPLIT
+            fused = dtype == torch.bfloat16 and variant in (kda.PREFILL_TC_SPLIT, kda.PREFILL_TC_2PASS)
             rel = 2.0 ** -8 if fused else 2.0 ** -7
             assert np.all(np.abs(host64(out) - y) <= rel * np.abs(y) + 1e-6 * np.abs(y).max())
 
