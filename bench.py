@@ -375,8 +375,11 @@ def run_gpu(args):
 
     ms_sp, _, _ = time_steps(split_step, short, max(args.warmup, 3), world, stream)
     check_device_status(kda, stream, "split")
-    legs["split"] = leg_summary(ms_sp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
-                                "kda_prefill_chain_kernel")
+    legs["split"] = leg_summary(
+        ms_sp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short, "kda_prefill_chain_kernel",
+        {"traffic": profiled_traffic("kda_prefill_chain_kernel",
+                                     "linear_attention_sequence_gb300/csrc/kda_prefill_chain.cu",
+                                     "prefill_8k")})
 
     # ---------------- the same layer in two passes (intra-chunk products, then the chain) ----
     def two_pass_step():
@@ -386,8 +389,15 @@ def run_gpu(args):
 
     ms_tp, _, _ = time_steps(two_pass_step, short, max(args.warmup, 3), world, stream)
     check_device_status(kda, stream, "two_pass")
-    legs["two_pass"] = leg_summary(ms_tp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
-                                   "kda_intra_kernel + kda_chain2_kernel")
+    # DRAM traffic of both passes: the 8 KB a chunk and head of intra-chunk products
+    # is written by the first and read by the second, on top of the algorithmic bytes
+    tp_src = "linear_attention_sequence_gb300/csrc/kda_prefill_2pass.cu"
+    tp_a = profiled_traffic("kda_intra_kernel", tp_src, "prefill_8k")
+    tp_b = profiled_traffic("kda_chain2_kernel", tp_src, "prefill_8k")
+    legs["two_pass"] = leg_summary(
+        ms_tp, T * world, PREFILL_BYTES_PER_TOKEN * T, hbm_gbs, short,
+        "kda_intra_kernel + kda_chain2_kernel",
+        {"traffic": tp_a + tp_b if tp_a is not None and tp_b is not None else None})
 
     # ---------------- the same layer with state checkpoints every 1024 tokens ----------------
     interval = 1024
