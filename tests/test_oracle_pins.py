@@ -93,31 +93,41 @@ def pin_beta_zero_closed_form(orc):
 
 
 def pin_toy_memory(orc, gold):
-    """The toy experiment with alpha = 1 (g = 0), beta = 1: regenerate the
-    stream with the same generator and draw order, check it with a plain
-    linear-attention sum (independent of the oracle), then feed it through
-    the oracle and compare its errors with the printed ones."""
+    """The associative-memory experiment of "Kimi K3.1 and the Road From
+    Softmax Attention to Kimi Delta Attention", section "3. The delta rule:
+    write only the correction", with alpha = 1 (g = 0) and beta = 1.
+
+    Only the draws follow the page (seed, d, pair count, and the order: the
+    unit keys, then the values, then the replacement value of key 0), since
+    the printed errors depend on them.  The memory of plain linear attention
+    is then the closed form K^T V of the written stream, checked without the
+    oracle; the delta-rule memory is the oracle's final state, checked against
+    the unrolled products of the factored update as well.  The read-out error
+    of a key is |S^T key - target| / |target|, compared at two decimals."""
     d, n = int(gold["d"]), int(gold["pairs"])
     rng = np.random.default_rng(int(gold["seed"]))
-    keys = np.stack([_unit(rng.standard_normal(d)) for _ in range(n)])
-    vals = np.stack([rng.standard_normal(d) for _ in range(n)])
-    new0 = rng.standard_normal(d)
-    ks = np.concatenate([keys, keys[:1]])                 # 20 writes, then key 0 again
-    vs = np.concatenate([vals, new0[None]])
+    keys = _unit(rng.standard_normal((n, d)))     # row by row: the same draws as one at a time
+    vals = rng.standard_normal((n, d))
+    replacement = rng.standard_normal(d)
+    stream_k = np.vstack([keys, keys[0]])         # the n pairs, then key 0 once more
+    stream_v = np.vstack([vals, replacement])
 
-    def rel(S, key, target):
-        return np.linalg.norm(S.T @ key - target) / np.linalg.norm(target)
+    def read_error(S, i, target):
+        return float(np.linalg.norm(S.T @ keys[i] - target) / np.linalg.norm(target))
 
-    lin = sum(np.outer(a, b) for a, b in zip(ks, vs))
-    assert round(rel(lin, keys[0], new0), 2) == gold["linear_attention_key0"]
-    assert round(rel(lin, keys[5], vals[5]), 2) == gold["linear_attention_key5"]
+    linear = stream_k.T @ stream_v                # sum over the stream of k v^T
+    assert round(read_error(linear, 0, replacement), 2) == gold["linear_attention_key0"]
+    assert round(read_error(linear, 5, vals[5]), 2) == gold["linear_attention_key5"]
 
-    T = ks.shape[0]
-    _, fin = orc.prefill(ks[:, None], ks[:, None], vs[:, None], np.zeros((T, 1, d)),
-                         np.ones((T, 1)))
-    S = fin[0, 0]
-    assert round(rel(S, keys[0], new0), 2) == gold["delta_rule_key0"]
-    assert round(rel(S, keys[5], vals[5]), 2) == gold["delta_rule_key5"]
+    T = stream_k.shape[0]
+    _, fin = orc.prefill(stream_k[:, None], stream_k[:, None], stream_v[:, None],
+                         np.zeros((T, 1, d)), np.ones((T, 1)))
+    delta = fin[0, 0]
+    _, unrolled = _brute(stream_k, stream_k, stream_v, np.zeros((T, d)), np.ones(T),
+                         np.zeros((d, d)))
+    np.testing.assert_allclose(delta, unrolled, rtol=0, atol=1e-10)
+    assert round(read_error(delta, 0, replacement), 2) == gold["delta_rule_key0"]
+    assert round(read_error(delta, 5, vals[5]), 2) == gold["delta_rule_key5"]
 
 
 def _brute(q, k, v, g, beta, S0):
