@@ -517,6 +517,10 @@ cudaError_t kda_launch_backward(const kda::Problem &P, const void *q, const void
                                 void *dv, float *dg, float *dbeta, float *d_init,
                                 cudaStream_t stream) {
     if (P.N == 0) return cudaSuccess;
+    // bf16 inputs at d = 128: the tensor-core kernel (kda_backward_tc.cu)
+    if (kda_backward_tc_supported(P, q, k, v, g, d_out))
+        return kda_launch_backward_tc(P, q, k, v, g, beta, init_state, cu, chunk_states, chunk_capacity,
+                                      d_out, d_final, dq, dk, dv, dg, dbeta, d_init, stream);
     if (P.dk == 128)
         return dispatch<128>(P, q, k, v, g, beta, init_state, cu, chunk_states, chunk_capacity, d_out, d_final, dq,
                              dk, dv, dg, dbeta, d_init, stream);

@@ -145,6 +145,16 @@ cudaError_t kda_launch_prefill_chain(const kda::Problem &P, const void *q, const
                                      float *final_state, cudaStream_t stream);
 cudaError_t kda_chain_read_status(unsigned *status);
 cudaError_t kda_bwd_read_status(unsigned *status);
+bool kda_backward_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
+                               const float *g, const void *d_out);
+cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const void *k,
+                                   const void *v, const float *g, const float *beta,
+                                   const float *init_state, const int32_t *cu,
+                                   const float *chunk_states, int64_t chunk_capacity,
+                                   const void *d_out, const float *d_final, void *dq, void *dk,
+                                   void *dv, float *dg, float *dbeta, float *d_init,
+                                   cudaStream_t stream);
+cudaError_t kda_bwdtc_read_status(unsigned *status);
 bool kda_prefill_noalloc_fits(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const void *out);
 cudaError_t kda_launch_prefill_noalloc(const kda::Problem &P, const void *q, const void *k,

@@ -1013,5 +1013,7 @@ cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
     if (e != cudaSuccess) return e;
     e = kda_2pass_read_status(status);   // the two-pass kernels' status word
     if (e != cudaSuccess) return e;
-    return kda_bwd_read_status(status);  // the backward's argument check
+    e = kda_bwd_read_status(status);     // the backward's argument check
+    if (e != cudaSuccess) return e;
+    return kda_bwdtc_read_status(status);   // the tensor-core backward's word
 }
