@@ -72,7 +72,8 @@ struct Small {
     float G[C][LDS32], P[C][LDS32], T[C][LDS32], dP[C][LDS32], dT[C][LDS32];
     float beta[C], dbeta[C], red[4][C];
     float e15[D], fC[D], gC[D], gsum[D];
-    uint64_t tma_bar, mma_bar;
+    float red2[4][D];
+    uint64_t tma_bar, s0_bar, mma_bar;
     uint32_t tmem_base;
     int abort;
 };
@@ -102,6 +103,23 @@ __device__ __forceinline__ void st_op(unsigned char *base, int rows, int row, in
     *reinterpret_cast<float *>(base + sw_off(rows, row, k)) = to_tf32(x);
 }
 
+// Byte offsets of column k in row r of a K-major SW128 operand with `rows` rows
+// (without the r * 128), for the eight values of r % 8; and the same for
+// column c of the bf16 and fp32 TMA tiles.
+__device__ __forceinline__ void op_offsets(int rows, int k, uint32_t (&o)[8]) {
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8)
+        o[k8] = (uint32_t)((k >> 5) * rows * 128 + ((((k & 31) >> 2) ^ k8) << 4) + ((k & 3) << 2));
+}
+__device__ __forceinline__ void bf16_offsets(int c, uint32_t (&o)[8]) {
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) o[k8] = (uint32_t)((c >> 6) * 4096 + ((((c & 63) >> 3) ^ k8) << 4) + ((c & 7) << 1));
+}
+__device__ __forceinline__ void f32_offsets(int c, uint32_t (&o)[8]) {
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) o[k8] = (uint32_t)((c >> 5) * 4096 + ((((c & 31) >> 2) ^ k8) << 4) + ((c & 3) << 2));
+}
+
 // One MMA group: D[m][n] (+)= sum_k A[m][k] B[n][k], A and B K-major SW128 in
 // shared memory (SS) with K-blocks of `akb` and `bkb` bytes; `ksteps` steps of 8.
 __device__ __forceinline__ void mma_ss_group(uint32_t d, const unsigned char *a, uint32_t akb,
@@ -126,7 +144,9 @@ template <typename OUT_T>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_g, const float *__restrict__ beta,
+                       const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_cs,
+                       const __grid_constant__ CUtensorMap tm_init, int has_cs, int has_init,
+                       const float *__restrict__ beta,
                        const float *init_state, const int32_t *__restrict__ cu,
                        const float *__restrict__ chunk_states, int64_t chunk_capacity,
                        const float *__restrict__ d_final, OUT_T *__restrict__ dq,
@@ -152,6 +172,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 
     if (t == 0) {
         mbar_init(&sm.tma_bar, 1);
+        mbar_init(&sm.s0_bar, 1);
         mbar_init(&sm.mma_bar, 1);
         fence_mbar_init();
         sm.abort = 0;
@@ -160,6 +181,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
         prefetch_tmap(&tm_g);
+        if (has_cs) prefetch_tmap(&tm_cs);
+        if (has_init) prefetch_tmap(&tm_init);
     }
     if (warp == 0) {
         tmem_alloc(&sm.tmem_base, 512);
@@ -170,7 +193,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     tc_fence_after();
     const uint32_t tb = sm.tmem_base;
     const uint32_t tl = tb + lane_off;
-    uint32_t tma_par = 0, mma_par = 0;
+    uint32_t tma_par = 0, s0_par = 0, mma_par = 0;
 
     // MMA groups are issued and awaited by thread 0; the barrier releases the rest.
     auto mma_wait = [&]() {
@@ -211,6 +234,15 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                            : (chunk_states && crow < chunk_capacity) ? chunk_states + (crow * H + h) * sdd
                                                                      : nullptr;
         if (ch > 0 && S0g == nullptr && t == 0) atomicOr(&g_kda_bwdtc_status, kda::kBwdMissingState);
+        // the state by TMA: four 128-row boxes of 32 columns = S0 as a K-major SW128
+        // operand (rows = key channel c, K = value j) in STG
+        const CUtensorMap *s0map = ch == 0 ? &tm_init : &tm_cs;
+        const int s0row = (int)((ch == 0 ? (int64_t)n * H + h : crow * H + h) * D);
+        auto load_s0 = [&](uint64_t *bar) {
+            mbar_arrive_expect_tx(bar, 65536);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) tma_load_2d(base + STG + kb * 16384, s0map, bar, 32 * kb, s0row);
+        };
 
         // ---- phase 0: the chunk's tiles by TMA; beta ----
         if (t == 0) {
@@ -220,7 +252,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tma_load_3d(base + T_V, &tm_v, &sm.tma_bar, 0, (int)t0, 2 * h);
             tma_load_3d(base + T_DO, &tm_do, &sm.tma_bar, 0, (int)t0, 2 * h);
             tma_load_3d(base + T_G, &tm_g, &sm.tma_bar, 0, (int)t0, 4 * h);
+            if (S0g) load_s0(&sm.s0_bar);
         }
+        if (!S0g)   // no state: S0 = 0
+            for (int i = t; i < 65536 / 16; i += kThreads)
+                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < C) {
             sm.beta[t] = t < L ? beta[(t0 + t) * H + h] : 0.f;
             sm.dbeta[t] = 0.f;
@@ -230,42 +266,63 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             atomicOr(&g_kda_bwdtc_status, 0x800u);
         }
         tma_par ^= 1u;
+        if (S0g && t == 0 && !mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit)) {
+            sm.abort = 1;
+            atomicOr(&g_kda_bwdtc_status, 0x800u);
+        }
+        if (S0g) s0_par ^= 1u;
         __syncthreads();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 1: threads 0-127 (channel c): Gamma and the decay-weighted
-        // operands; threads 128-383: S0^T into STG (rows j, K = c) ----
-        if (t < D) {
-            const int c = t;
-            float gam[C];
+        // ---- phase 1: Gamma and the decay-weighted operands on warps 0-3 and 12-15
+        // (thread = channel c, tokens 16 part .. 16 part + 15; the two parts of a
+        // channel in adjacent lanes), while warps 4-11 move S0^T into TMEM ----
+        if (warp < 4 || warp >= 12) {
+            const int tp = warp < 4 ? t : t - 256;
+            const int c = tp >> 1, part = tp & 1;
+            uint32_t ob[8], of[8], ok[8];
+            bf16_offsets(c, ob);
+            f32_offsets(c, of);
+            op_offsets(32, c, ok);
+            float gam[16];
 #pragma unroll
-            for (int r = 0; r < C; ++r)
-                gam[r] = r < L ? *reinterpret_cast<const float *>(base + T_G + off_f32(r, c)) : 0.f;
+            for (int u = 0; u < 16; ++u) {
+                const int r = 16 * part + u;
+                gam[u] = r < L ? *reinterpret_cast<const float *>(base + T_G + r * 128 + of[u & 7]) : 0.f;
+            }
 #pragma unroll
-            for (int r = 1; r < C; ++r) gam[r] += gam[r - 1];
+            for (int u = 1; u < 16; ++u) gam[u] += gam[u - 1];
+            const float lo = __shfl_up_sync(0xffffffffu, gam[15], 1, 2);
+            if (part) {
 #pragma unroll
-            for (int r = 0; r < C; ++r) *reinterpret_cast<float *>(base + T_G + off_f32(r, c)) = gam[r];
-            const float g15 = gam[15], gl = gam[C - 1];
-            sm.e15[c] = __expf(g15);
-            sm.fC[c] = __expf(gl - g15);
-            sm.gC[c] = __expf(gl);
-            sm.gsum[c] = 0.f;
+                for (int u = 0; u < 16; ++u) gam[u] += lo;
+            }
+            const float g15 = __shfl_sync(0xffffffffu, gam[15], lane & ~1);
+            const float gl = __shfl_sync(0xffffffffu, gam[15], lane | 1);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) *reinterpret_cast<float *>(base + T_G + (16 * part + u) * 128 + of[u & 7]) = gam[u];
+            if (part == 0) {
+                sm.e15[c] = __expf(g15);
+                sm.fC[c] = __expf(gl - g15);
+                sm.gC[c] = __expf(gl);
+            }
             float q1[4], a1[4], b1[4];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
+            for (int u = 0; u < 16; ++u) {
+                const int r = 16 * part + u;
                 float qv = 0.f, kv = 0.f;
                 if (r < L) {
-                    qv = lds_bf16(base + T_Q + off_bf16(r, c));
-                    kv = lds_bf16(base + T_K + off_bf16(r, c));
+                    qv = lds_bf16(base + T_Q + r * 128 + ob[u & 7]);
+                    kv = lds_bf16(base + T_K + r * 128 + ob[u & 7]);
                 }
-                const float x = gam[r] - g15;
+                const float x = gam[u] - g15;
                 const float e1 = __expf(x), inv = __expf(-x);
-                st_op(base + O_KT, 32, r, c, kv * __expf(gam[r]));    // Kt = k e^{Gamma}
-                st_op(base + O_KB, 32, r, c, kv * __expf(gl - gam[r]));   // Kb = k e^{Gamma_C - Gamma}
-                q1[r & 3] = to_tf32(qv * e1);
-                a1[r & 3] = to_tf32(kv * e1);
-                b1[r & 3] = to_tf32(kv * inv);
-                if ((r & 3) == 3) {
+                *reinterpret_cast<float *>(base + O_KT + r * 128 + ok[u & 7]) = to_tf32(kv * __expf(gam[u]));
+                *reinterpret_cast<float *>(base + O_KB + r * 128 + ok[u & 7]) = to_tf32(kv * __expf(gl - gam[u]));
+                q1[u & 3] = to_tf32(qv * e1);
+                a1[u & 3] = to_tf32(kv * e1);
+                b1[u & 3] = to_tf32(kv * inv);
+                if ((u & 3) == 3) {
                     const uint32_t pos = (uint32_t)((((r >> 2) ^ (c & 7)) & 7) << 4);
                     *reinterpret_cast<float4 *>(base + OPQA + c * 128 + pos) = make_float4(q1[0], q1[1], q1[2], q1[3]);
                     *reinterpret_cast<float4 *>(base + OPQA + 16384 + c * 128 + pos) =
@@ -273,66 +330,122 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     *reinterpret_cast<float4 *>(base + OPB1T + c * 128 + pos) = make_float4(b1[0], b1[1], b1[2], b1[3]);
                 }
             }
-        } else if (t < D + 256) {
-            const int u = t - D, j = u & 127, half = u >> 7;   // channels [64 half, 64 half + 64)
-            float x[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = S0g ? S0g[(int64_t)(64 * half + i) * D + j] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) st_op(base + STG, 128, j, 64 * half + i, x[i]);
         }
         fence_proxy_async_smem();
+        // S0^T into tensor memory (lane j, columns c of this warp's half) for the X
+        // product, and gsum[c] = sum_j dS[c][j] S0[c][j] with dS^T from TMEM (warps 4-11)
+        if (warp >= 4 && warp < 12) {
+            const int half = (warp - 4) >> 2;
+            float p[64];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int c0 = 64 * half + 32 * h2;
+                float x[32], d[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = *reinterpret_cast<const float *>(base + STG + sw_off(128, c0 + i, jl));
+                tmem_st32(tl + TM_DN + c0, x);
+                tmem_ld32(tl + TM_DS + c0, d);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) p[32 * h2 + i] = x[i] * d[i];
+            }
+            tmem_wait_st();
+            // reduce-scatter over the warp's 32 lanes: lane l ends with the sums for
+            // channels 64 half + l and 64 half + 32 + l
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float *y = p + 32 * h2;
+#pragma unroll
+                for (int sh = 16; sh >= 1; sh >>= 1) {
+                    const bool up = (lane & sh) != 0;
+#pragma unroll
+                    for (int i = 0; i < sh; ++i) {
+                        const float send = up ? y[i] : y[i + sh];
+                        const float keep = up ? y[i + sh] : y[i];
+                        y[i] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
+                    }
+                }
+                sm.red2[q4][64 * half + 32 * h2 + lane] = y[0];
+            }
+            if (warp < 8) {   // dO^T into tensor memory (lane j, column r)
+                float x[32];
+                uint32_t ob[8];
+                bf16_offsets(jl, ob);
+#pragma unroll
+                for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f;
+                tmem_st32(tl + TM_DOT, x);
+                tmem_wait_st();
+            }
+        }
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
 
+        if (t < D) sm.gsum[t] = sm.red2[0][t] + sm.red2[1][t] + sm.red2[2][t] + sm.red2[3][t];
         // ---- phase 2: G = A1 B1^T (strict) and P = Q1 B1^T (inclusive) from the
         // transposed operand blocks (threads: product, 2 x 2 tile) ----
         {
-            const int prod = t >> 8, th = t & 255;
-            const int r0 = (th >> 4) * 2, i0 = (th & 15) * 2;
+            // thread: product (G for warps 0-3 and 8-11, P for 4-7 and 12-15), rows
+            // r0..r0+3, columns i0 and i0+16; warps 8-15 sum the channels 64-127 and
+            // hand their partial sums to warps 0-7 through STG
+            const int tp = t & 255, kh = t >> 8;
+            const int prod = tp >> 7, th = tp & 127;
+            const int r0 = (th >> 4) * 4, i0 = th & 15;
             const unsigned char *Am = base + OPQA + (prod == 0 ? 16384 : 0);   // A1^T or Q1^T
-            float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-#pragma unroll 4
-            for (int c = 0; c < D; ++c) {
-                const float2 x = *reinterpret_cast<const float2 *>(Am + sw_off(128, c, r0));
-                const float2 y = *reinterpret_cast<const float2 *>(base + OPB1T + sw_off(128, c, i0));
-                a00 += x.x * y.x;
-                a01 += x.x * y.y;
-                a10 += x.y * y.x;
-                a11 += x.y * y.y;
+            const unsigned char *Bm = base + OPB1T;
+            uint32_t oa[8], ob0[8], ob1[8];   // byte offsets of (row c, k) inside row c, for c % 8
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                oa[u] = (uint32_t)((((r0 >> 2) ^ u) & 7) << 4);
+                ob0[u] = (uint32_t)(((((i0 >> 2) ^ u) & 7) << 4) + (i0 & 3) * 4);
+                ob1[u] = (uint32_t)((((((i0 + 16) >> 2) ^ u) & 7) << 4) + (i0 & 3) * 4);
             }
-            const float av[2][2] = {{a00, a01}, {a10, a11}};
+            float acc[4][2];
 #pragma unroll
-            for (int u2 = 0; u2 < 2; ++u2)
+            for (int e = 0; e < 4; ++e) acc[e][0] = acc[e][1] = 0.f;
+#pragma unroll 2
+            for (int c0 = 64 * kh; c0 < 64 * kh + 64; c0 += 8) {
 #pragma unroll
-                for (int w2 = 0; w2 < 2; ++w2) {
-                    const int r = r0 + u2, i = i0 + w2;
-                    if (prod == 0) sm.G[r][i] = i < r ? av[u2][w2] : 0.f;
-                    else sm.P[r][i] = i <= r ? av[u2][w2] : 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    const float4 x = *reinterpret_cast<const float4 *>(Am + (c0 + u) * 128 + oa[u]);
+                    const float y0 = *reinterpret_cast<const float *>(Bm + (c0 + u) * 128 + ob0[u]);
+                    const float y1 = *reinterpret_cast<const float *>(Bm + (c0 + u) * 128 + ob1[u]);
+                    const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[e][0] += xv[e] * y0;
+                        acc[e][1] += xv[e] * y1;
+                    }
                 }
+            }
+            float *part = reinterpret_cast<float *>(base + STG) + tp * 8;
+            if (kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    part[2 * e] = acc[e][0];
+                    part[2 * e + 1] = acc[e][1];
+                }
+            }
+            __syncthreads();
+            if (!kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int w2 = 0; w2 < 2; ++w2) {
+                        const int r = r0 + e, i = i0 + 16 * w2;
+                        const float v = acc[e][w2] + part[2 * e + w2];
+                        if (prod == 0) sm.G[r][i] = i < r ? v : 0.f;
+                        else sm.P[r][i] = i <= r ? v : 0.f;
+                    }
+            }
         }
         __syncthreads();
-        // T = (I + diag(beta) G)^{-1}: lane j solves column j (warp 0); warps 4-7:
-        // dO^T into tensor memory (lane j, column r)
-        if (warp == 0) {
-            float x[C];
+        if (warp == 0) {   // blocked solve; STG holds its scratch (the state is in TMEM now)
+            float d[32];
 #pragma unroll
-            for (int i = 0; i < C; ++i) x[i] = i == lane ? 1.f : 0.f;
-#pragma unroll
-            for (int i = 1; i < C; ++i) {
-                float acc = x[i];
-                const float bi = sm.beta[i];
-#pragma unroll
-                for (int m = 0; m < i; ++m) acc -= bi * sm.G[i][m] * x[m];
-                x[i] = acc;
-            }
-#pragma unroll
-            for (int i = 0; i < C; ++i) sm.T[i][lane] = x[i];
-        } else if (warp >= 4 && warp < 8) {
-            float x[32];
-#pragma unroll
-            for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_DO + off_bf16(r, jl)) : 0.f;
-            tmem_st32(tl + TM_DOT, x);
-            tmem_wait_st();
+            for (int i = 0; i < C; ++i) d[i] = sm.G[lane][i];
+            solve_t(d, sm.beta[lane], lane, &sm.T[0][0], LDS32,
+                    reinterpret_cast<float(*)[32]>(base + STG),
+                    reinterpret_cast<float(*)[16][20]>(base + STG + 4096));
         }
         tc_fence_before();
         __syncthreads();
@@ -350,7 +463,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // ---- phase 3: X = S0^T Kt^T (Y = V - X), dU^T = dS^T Kb^T + dO^T P ----
         if (t == 0) {
             tc_fence_after();
-            mma_ss_group(tb + TM_X, base + STG, 16384, base + O_KT, 4096, 16, 32, false);
+            mma_ts_group(tb + TM_X, tb + TM_DN, base + O_KT, 4096, 16, 32, false);
             mma_ts_group(tb + TM_DU, tb + TM_DS, base + O_KB, 4096, 16, 32, false);
             mma_ts_group(tb + TM_DU, tb + TM_DOT, base + O_PT, 4096, 4, 32, true);
         }
@@ -377,20 +490,17 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 5 (warps 0-3, lane j): dV = dY = diag(beta) dB; the dB . Y row
-        // sums; -dY^T into tensor memory; U, dU, Y (fp32, STG) and the operands
-        // [dO ; -dY] (rows, K = j) and U (rows, K = j) ----
+        // ---- phase 5 (lane j): dV = dY = diag(beta) dB and the dB . Y row sums
+        // (warps 0-3); U (warps 4-7) and dU, Y (warps 8-11) in fp32 into STG and U as
+        // an operand; the operand rows [dO ; -dY] (warps 12-15) ----
         if (warp < 4) {
             float y[32], x[32];
             tmem_ld32(tl + TM_DB, x);
             tmem_ld32(tl + TM_Y, y);
-            float *sY = reinterpret_cast<float *>(base + STG) + 2 * C * LU;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
                 const float dy = sm.beta[r] * x[r];
                 if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + jl, dy);
-                sY[r * LU + jl] = y[r];
-                st_op(base + O_OY, 64, 32 + r, jl, -dy);
                 x[r] *= y[r];          // dB . Y
                 y[r] = -dy;
             }
@@ -410,12 +520,14 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tmem_wait_st();
         } else if (warp < 8) {
             float x[32];
+            uint32_t o[8];
+            op_offsets(32, jl, o);
             tmem_ld32(tl + TM_U, x);
             float *sU = reinterpret_cast<float *>(base + STG);
 #pragma unroll
             for (int r = 0; r < C; ++r) {
                 sU[r * LU + jl] = x[r];
-                st_op(base + O_U, 32, r, jl, x[r]);
+                *reinterpret_cast<float *>(base + O_U + r * 128 + o[r & 7]) = to_tf32(x[r]);
             }
         } else if (warp < 12) {
             float x[32];
@@ -423,76 +535,116 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             float *sDU = reinterpret_cast<float *>(base + STG) + C * LU;
 #pragma unroll
             for (int r = 0; r < C; ++r) sDU[r * LU + jl] = x[r];
-        } else {
+            tmem_ld32(tl + TM_Y, x);
+            float *sY = reinterpret_cast<float *>(base + STG) + 2 * C * LU;
 #pragma unroll
-            for (int r = 0; r < C; ++r)
-                st_op(base + O_OY, 64, r, jl, r < L ? lds_bf16(base + T_DO + off_bf16(r, jl)) : 0.f);
+            for (int r = 0; r < C; ++r) sY[r * LU + jl] = x[r];
+        } else {
+            float x[32];
+            uint32_t o[8], ob[8];
+            op_offsets(64, jl, o);
+            bf16_offsets(jl, ob);
+            tmem_ld32(tl + TM_DB, x);
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                *reinterpret_cast<float *>(base + O_OY + r * 128 + o[r & 7]) =
+                    to_tf32(r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f);
+                *reinterpret_cast<float *>(base + O_OY + (32 + r) * 128 + o[r & 7]) = to_tf32(-sm.beta[r] * x[r]);
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // dP = tril(dO U^T) and dT = dU (beta Y)^T (strict), 2 x 2 tiles over j
+        // dP = tril(dO U^T) (warps 0-3 and 8-11) and dT = dU (beta Y)^T (strict, warps
+        // 4-7 and 12-15): thread = rows r0..r0+3, columns i0 and i0+16, 8 values of j
+        // per step; warps 8-15 sum j = 64..127 and hand their partial sums over
         {
-            const int prod = t >> 8, th = t & 255;
-            const int r0 = (th >> 4) * 2, i0 = (th & 15) * 2;
+            const int tp = t & 255, kh = t >> 8;
+            const int prod = tp >> 7, th = tp & 127;
+            const int r0 = (th >> 4) * 4, i0 = th & 15;
             const float *sU = reinterpret_cast<const float *>(base + STG);
             const float *sDU = sU + C * LU, *sY = sU + 2 * C * LU;
-            float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-            if (prod == 0) {
-#pragma unroll 4
-                for (int j = 0; j < D; ++j) {
-                    const float x0 = lds_bf16(base + T_DO + off_bf16(r0, j));
-                    const float x1 = lds_bf16(base + T_DO + off_bf16(r0 + 1, j));
-                    const float y0 = sU[i0 * LU + j], y1 = sU[(i0 + 1) * LU + j];
-                    a00 += x0 * y0;
-                    a01 += x0 * y1;
-                    a10 += x1 * y0;
-                    a11 += x1 * y1;
-                }
-            } else {
-#pragma unroll 4
-                for (int j = 0; j < D; ++j) {
-                    const float x0 = sDU[r0 * LU + j], x1 = sDU[(r0 + 1) * LU + j];
-                    const float y0 = sY[i0 * LU + j], y1 = sY[(i0 + 1) * LU + j];
-                    a00 += x0 * y0;
-                    a01 += x0 * y1;
-                    a10 += x1 * y0;
-                    a11 += x1 * y1;
-                }
-            }
-            const float av[2][2] = {{a00, a01}, {a10, a11}};
+            const float *By = prod == 0 ? sU : sY;
+            float acc[4][2];
 #pragma unroll
-            for (int u2 = 0; u2 < 2; ++u2)
+            for (int e = 0; e < 4; ++e) acc[e][0] = acc[e][1] = 0.f;
+#pragma unroll 2
+            for (int m = 8 * kh; m < 8 * kh + 8; ++m) {
+                float x[4][8];
+                if (prod == 0) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = r0 + e;
+                        const uint4 w = *reinterpret_cast<const uint4 *>(base + T_DO + (m >> 3) * 4096 + r * 128 +
+                                                                         ((((m & 7) ^ (r & 7)) & 7) << 4));
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            x[e][2 * q] = __uint_as_float(wv[q] << 16);
+                            x[e][2 * q + 1] = __uint_as_float(wv[q] & 0xffff0000u);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 p0 = *reinterpret_cast<const float4 *>(sDU + (r0 + e) * LU + 8 * m);
+                        const float4 p1 = *reinterpret_cast<const float4 *>(sDU + (r0 + e) * LU + 8 * m + 4);
+                        x[e][0] = p0.x; x[e][1] = p0.y; x[e][2] = p0.z; x[e][3] = p0.w;
+                        x[e][4] = p1.x; x[e][5] = p1.y; x[e][6] = p1.z; x[e][7] = p1.w;
+                    }
+                }
 #pragma unroll
                 for (int w2 = 0; w2 < 2; ++w2) {
-                    const int r = r0 + u2, i = i0 + w2;
-                    // rows past the chunk's end hold dO = 0 (U rows are 0 there too)
-                    if (prod == 0) sm.dP[r][i] = (i <= r && r < L) ? av[u2][w2] : 0.f;
-                    else sm.dT[r][i] = i < r ? av[u2][w2] * sm.beta[i] : 0.f;
+                    const float *yp = By + (i0 + 16 * w2) * LU + 8 * m;
+                    const float4 ya = *reinterpret_cast<const float4 *>(yp), yb = *reinterpret_cast<const float4 *>(yp + 4);
+                    const float y[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[e][w2] += x[e][q] * y[q];
                 }
+            }
+            float *part = reinterpret_cast<float *>(base + STG + 51200) + tp * 8;   // past the fp32 staging
+            if (kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    part[2 * e] = acc[e][0];
+                    part[2 * e + 1] = acc[e][1];
+                }
+            }
+            __syncthreads();
+            if (!kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int w2 = 0; w2 < 2; ++w2) {
+                        const int r = r0 + e, i = i0 + 16 * w2;
+                        const float v = acc[e][w2] + part[2 * e + w2];
+                        // rows past the chunk's end hold other tokens' dO: their dP is 0
+                        if (prod == 0) sm.dP[r][i] = (i <= r && r < L) ? v : 0.f;
+                        else sm.dT[r][i] = i < r ? v * sm.beta[i] : 0.f;
+                    }
+            }
         }
         if (t < C) sm.dbeta[t] += sm.red[0][t] + sm.red[1][t] + sm.red[2][t] + sm.red[3][t];
         __syncthreads();
-        // S0 (rows c, K = j) into STG: four threads per row, 32 channels of j each
-        {
-            const int c = t >> 2, j0 = (t & 3) * 32;
-            float x[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (S0g) v4 = *reinterpret_cast<const float4 *>(S0g + (int64_t)c * D + j0 + i);
-                x[i] = v4.x;
-                x[i + 1] = v4.y;
-                x[i + 2] = v4.z;
-                x[i + 3] = v4.w;
+        // S0 (rows c, K = j) into STG again by TMA (the staging above is consumed)
+        if (S0g) {
+            if (t == 0) {
+                fence_proxy_async_smem();
+                load_s0(&sm.s0_bar);
+                if (!mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit)) {
+                    sm.abort = 1;
+                    atomicOr(&g_kda_bwdtc_status, 0x800u);
+                }
             }
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4 *>(base + STG + sw_off(128, c, j0 + i)) =
-                    make_float4(to_tf32(x[i]), to_tf32(x[i + 1]), to_tf32(x[i + 2]), to_tf32(x[i + 3]));
+            s0_par ^= 1u;
+        } else {
+            for (int i = t; i < 65536 / 16; i += kThreads)
+                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncthreads();
 
         // ---- phase 6: [aQ^T | aK^T] / e15 = S0 [dO ; -dY]^T ----
@@ -520,62 +672,84 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             mma_ss_group(tb + TM_AB, base + STG, 16384, base + O_U, 4096, 16, 32, false);
             mma_ts_group(tb + TM_DN, tb + TM_DOT, base + OPQA, 16384, 8, 128, false);
         }
-        // meanwhile: gsum[c] = sum_j dS[c][j] S0[c][j] (four threads per channel)
-        {
-            const int c = t >> 2, j0 = (t & 3) * 32;
-            float s = 0.f;
-            if (S0g) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(base + STG + sw_off(128, c, j0 + i));
-                    const float4 s4 = *reinterpret_cast<const float4 *>(S0g + (int64_t)c * D + j0 + i);
-                    s += d4.x * s4.x + d4.y * s4.y + d4.z * s4.z + d4.w * s4.w;
-                }
-            }
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((t & 3) == 0) sm.gsum[c] = s;
-        }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 7: dS^T <- dS^T Diag(gamma_C) + (increment)^T Diag(e15) (lane j,
-        // its quarter of the channels); dA, dG and the dA . G row sums ----
-        {
-            float x[32], y[32];
-            tmem_ld32(tl + TM_DS + 32 * slice, x);
-            tmem_ld32(tl + TM_DN + 32 * slice, y);
+        // ---- phase 7: dS^T <- dS^T Diag(gamma_C) + (increment)^T Diag(e15) on warps
+        // 0-7 (lane j, half of the channels each), while warps 8-15 form dA, dG and
+        // the dA . G row sums ----
+        if (warp < 8) {
+            const int hh = warp >> 2;
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {
+                const int c0 = 64 * hh + 32 * q;
+                float x[32], y[32];
+                tmem_ld32(tl + TM_DS + c0, x);
+                tmem_ld32(tl + TM_DN + c0, y);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = 32 * slice + i;
-                x[i] = sm.gC[c] * x[i] + sm.e15[c] * y[i];
+                for (int i = 0; i < 32; ++i) x[i] = sm.gC[c0 + i] * x[i] + sm.e15[c0 + i] * y[i];
+                tmem_st32(tl + TM_DS + c0, x);
             }
-            tmem_st32(tl + TM_DS + 32 * slice, x);
             tmem_wait_st();
-        }
-        {
-            // M1 = tril_s(dT) T^T into dP's neighbour (the G array keeps G until dG)
+        } else {
+            // dA = -T^T tril_s(dT) T^T as two 32 x 32 products (T lower triangular and dT
+            // strictly lower, so full-length sums need no bounds): M1 = dT T^T, then
+            // dA = -T^T M1; thread = rows r0, r0+1 x columns i0, i0+1
+            const int tp = t - 256;
+            const int r0 = (tp >> 4) * 2, i0 = (tp & 15) * 2;
             float(*M1)[LDS32] = reinterpret_cast<float(*)[LDS32]>(base + STG);   // STG is free again
-            for (int idx = t; idx < C * C; idx += kThreads) {
-                const int r = idx >> 5, i = idx & 31;
-                float s = 0.f;
-                for (int bb = 0; bb < r && bb <= i; ++bb) s += sm.dT[r][bb] * sm.T[i][bb];
-                M1[r][i] = s;
+            float m00 = 0.f, m01 = 0.f, m10 = 0.f, m11 = 0.f;
+#pragma unroll 8
+            for (int bb = 0; bb < C; ++bb) {
+                const float d0 = sm.dT[r0][bb], d1 = sm.dT[r0 + 1][bb];
+                const float t0v = sm.T[i0][bb], t1v = sm.T[i0 + 1][bb];
+                m00 += d0 * t0v;
+                m01 += d0 * t1v;
+                m10 += d1 * t0v;
+                m11 += d1 * t1v;
             }
-            __syncthreads();
-            for (int idx = t; idx < C * C; idx += kThreads) {   // a warp = one row r
-                const int r = idx >> 5, i = idx & 31;
-                float s = 0.f;
-                for (int a2 = r; a2 < C; ++a2) s -= sm.T[a2][r] * M1[a2][i];
-                const float da = i < r ? s : 0.f;
-                float gb = da * sm.G[r][i];
+            M1[r0][i0] = m00;
+            M1[r0][i0 + 1] = m01;
+            M1[r0 + 1][i0] = m10;
+            M1[r0 + 1][i0 + 1] = m11;
+            named_sync(1, 256);
+            float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll 8
+            for (int a2 = 0; a2 < C; ++a2) {
+                const float t0v = sm.T[a2][r0], t1v = sm.T[a2][r0 + 1];
+                const float x0 = M1[a2][i0], x1 = M1[a2][i0 + 1];
+                a00 -= t0v * x0;
+                a01 -= t0v * x1;
+                a10 -= t1v * x0;
+                a11 -= t1v * x1;
+            }
+            const float dav[2][2] = {{a00, a01}, {a10, a11}};
+            float gb0 = 0.f, gb1 = 0.f;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) gb += __shfl_xor_sync(0xffffffffu, gb, o);
-                sm.G[r][i] = sm.beta[r] * da;   // dG
-                if (i == 0) sm.dbeta[r] += gb;
+            for (int u2 = 0; u2 < 2; ++u2)
+#pragma unroll
+                for (int w2 = 0; w2 < 2; ++w2) {
+                    const int r = r0 + u2, i = i0 + w2;
+                    const float da = i < r ? dav[u2][w2] : 0.f;
+                    const float gbv = da * sm.G[r][i];
+                    if (u2 == 0) gb0 += gbv;
+                    else gb1 += gbv;
+                    sm.G[r][i] = sm.beta[r] * da;   // dG
+                }
+            // the dA . G row sums over the 16 threads of a row pair (adjacent lanes)
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                gb0 += __shfl_xor_sync(0xffffffffu, gb0, o);
+                gb1 += __shfl_xor_sync(0xffffffffu, gb1, o);
+            }
+            if ((tp & 15) == 0) {
+                sm.dbeta[r0] += gb0;
+                sm.dbeta[r0 + 1] += gb1;
             }
         }
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
         // [dP ; dG] (rows, K = i) and the B operand of R3 (rows x, K = [i | i']:
         // dP[i][x], dG[i][x]) into OPA
         for (int idx = t; idx < C * C; idx += kThreads) {
@@ -596,47 +770,52 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 8 (warps 0-3, lane = key channel c): dq, dk, dGamma, dg ----
-        if (warp < 4) {
-            const int c = jl;
+        // ---- phase 8 (lane = key channel c, tokens 8 slice .. 8 slice + 7): dq, dk,
+        // dGamma (into STG), then dg as the reverse running sum (threads 0-127) ----
+        {
+            const int c = jl, x0 = 8 * slice;
             const float e15 = sm.e15[c], fC = sm.fC[c];
             const float gl = *reinterpret_cast<const float *>(base + T_G + off_f32(C - 1, c));
             const float g15 = *reinterpret_cast<const float *>(base + T_G + off_f32(15, c));
-            float dgam[C];
+            float aq[8], ak[8], ab[8], r1[8], r2[8], r3[8];
+            tmem_ld8(tl + TM_AQK + x0, aq);
+            tmem_ld8(tl + TM_AQK + 32 + x0, ak);
+            tmem_ld8(tl + TM_AB + x0, ab);
+            tmem_ld8(tl + TM_R12 + x0, r1);
+            tmem_ld8(tl + TM_R12 + 32 + x0, r2);
+            tmem_ld8(tl + TM_R3 + x0, r3);
+            float *sDG = reinterpret_cast<float *>(base + STG);   // [C][LU]
             float kbk = 0.f;
 #pragma unroll
-            for (int x8 = 0; x8 < C; x8 += 8) {
-                float aq[8], ak[8], ab[8], r1[8], r2[8], r3[8];
-                tmem_ld8(tl + TM_AQK + x8, aq);
-                tmem_ld8(tl + TM_AQK + 32 + x8, ak);
-                tmem_ld8(tl + TM_AB + x8, ab);
-                tmem_ld8(tl + TM_R12 + x8, r1);
-                tmem_ld8(tl + TM_R12 + 32 + x8, r2);
-                tmem_ld8(tl + TM_R3 + x8, r3);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int x = x8 + u;
-                    const float gx = *reinterpret_cast<const float *>(base + T_G + off_f32(x, c));
-                    const float ex = __expf(gx - g15), ix = __expf(g15 - gx);
-                    const float sq = e15 * aq[u] + r1[u], sk = e15 * ak[u] + r2[u];
-                    const float fb = fC * ab[u];
-                    if (x < L) {
-                        const int64_t off = (t0 + x) * rowK + (int64_t)h * D + c;
-                        kda::st_elem(dq + off, ex * sq);
-                        kda::st_elem(dk + off, ex * sk + __expf(gl - gx) * ab[u] + ix * r3[u]);
-                    }
-                    const float q1 = *reinterpret_cast<const float *>(base + OPQA + sw_off(128, c, x));
-                    const float a1 = *reinterpret_cast<const float *>(base + OPQA + 16384 + sw_off(128, c, x));
-                    const float b1 = *reinterpret_cast<const float *>(base + OPB1T + sw_off(128, c, x));
-                    dgam[x] = q1 * sq + a1 * sk - b1 * (fb + r3[u]);
-                    kbk += fb * b1;
+            for (int u = 0; u < 8; ++u) {
+                const int x = x0 + u;
+                const float gx = *reinterpret_cast<const float *>(base + T_G + off_f32(x, c));
+                const float ex = __expf(gx - g15), ix = __expf(g15 - gx);
+                const float sq = e15 * aq[u] + r1[u], sk = e15 * ak[u] + r2[u];
+                const float fb = fC * ab[u];
+                if (x < L) {
+                    const int64_t off = (t0 + x) * rowK + (int64_t)h * D + c;
+                    kda::st_elem(dq + off, ex * sq);
+                    kda::st_elem(dk + off, ex * sk + __expf(gl - gx) * ab[u] + ix * r3[u]);
                 }
+                const float q1 = *reinterpret_cast<const float *>(base + OPQA + sw_off(128, c, x));
+                const float a1 = *reinterpret_cast<const float *>(base + OPQA + 16384 + sw_off(128, c, x));
+                const float b1 = *reinterpret_cast<const float *>(base + OPB1T + sw_off(128, c, x));
+                sDG[x * LU + c] = q1 * sq + a1 * sk - b1 * (fb + r3[u]);
+                kbk += fb * b1;
             }
+            sm.red2[slice][c] = kbk;
+        }
+        __syncthreads();
+        if (t < D) {
+            const int c = t;
+            const float *sDG = reinterpret_cast<const float *>(base + STG);
             float run = 0.f;
-            const float last = fC * e15 * sm.gsum[c] + kbk;
-#pragma unroll
+            const float last = sm.fC[c] * sm.e15[c] * sm.gsum[c] + sm.red2[0][c] + sm.red2[1][c] +
+                               sm.red2[2][c] + sm.red2[3][c];
+#pragma unroll 4
             for (int r = C - 1; r >= 0; --r) {
-                run += dgam[r] + (r == C - 1 ? last : 0.f);
+                run += sDG[r * LU + c] + (r == C - 1 ? last : 0.f);
                 if (r < L) dg[(t0 + r) * rowK + (int64_t)h * D + c] = run;
             }
         }
@@ -689,6 +868,13 @@ cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const v
         !kda_make_tile_map(&mdo, d_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
         !kda_make_tile_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H))
         return cudaErrorInvalidValue;
+    CUtensorMap mcs = {}, minit = {};
+    const int has_cs = chunk_states && chunk_capacity > 0;
+    const int has_init = init_state != nullptr;
+    if (has_cs && !kda_make_state_map(&mcs, chunk_states, chunk_capacity * P.H * (int64_t)D))
+        return cudaErrorInvalidValue;
+    if (has_init && !kda_make_state_map(&minit, init_state, (int64_t)P.N * P.H * D))
+        return cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((int64_t)P.N * P.H);
     if (P.out_dtype == KDA_DTYPE_BF16) {
         auto kern = kda_backward_tc_kernel<__nv_bfloat16>;
@@ -696,20 +882,21 @@ cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const v
         static cudaError_t attr = cudaSuccess;
         std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem); });
         if (attr != cudaSuccess) return attr;
-        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, beta, init_state, cu, chunk_states,
-                                                  chunk_capacity, d_final, (__nv_bfloat16 *)dq,
-                                                  (__nv_bfloat16 *)dk, (__nv_bfloat16 *)dv, dg, dbeta,
-                                                  d_init, P.H, (int64_t)P.T, P.seq_len);
+        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, beta,
+                                                  init_state, cu, chunk_states, chunk_capacity, d_final,
+                                                  (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk,
+                                                  (__nv_bfloat16 *)dv, dg, dbeta, d_init, P.H,
+                                                  (int64_t)P.T, P.seq_len);
     } else {
         auto kern = kda_backward_tc_kernel<float>;
         static std::once_flag once;
         static cudaError_t attr = cudaSuccess;
         std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem); });
         if (attr != cudaSuccess) return attr;
-        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, beta, init_state, cu, chunk_states,
-                                                  chunk_capacity, d_final, (float *)dq, (float *)dk,
-                                                  (float *)dv, dg, dbeta, d_init, P.H, (int64_t)P.T,
-                                                  P.seq_len);
+        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, beta,
+                                                  init_state, cu, chunk_states, chunk_capacity, d_final,
+                                                  (float *)dq, (float *)dk, (float *)dv, dg, dbeta, d_init,
+                                                  P.H, (int64_t)P.T, P.seq_len);
     }
     return cudaGetLastError();
 }

@@ -963,6 +963,21 @@ bool kda_make_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt,
     return make_map(m, base, dt, esize, T, H);
 }
 
+// The TMA view of an fp32 state array [rows, 128] (rows = states x 128 key
+// channels): box = 128 rows x 32 columns, 128-byte swizzle, so that four boxes
+// give a 128-row K-major SW128 operand (rows = key channel, K = value index).
+bool kda_make_state_map(CUtensorMap *m, const float *base, int64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const void *out) {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
