@@ -53,14 +53,20 @@ constexpr uint32_t kPollLimit = 1u << 23;
 //   TILE   TMA tiles of the chunk: q, k, v, dO (bf16, 8 KB each), g (fp32, 16 KB;
 //          Gamma in place).  After the preparation the q and k tiles hold the
 //          operands T diag(beta), T^T, P^T (4 KB each), later U (16 KB).
-//   STG    64 KB staging of 128-row operands: S0^T (rows j), then the fp32
-//          copies of U, dU and Y, then S0 (rows c), then dS (rows c).
+//   STG    64 KB staging: the Gram operands [A1 ; Q1] and B1 (rows, K = c), then
+//          S0 by TMA (rows c, K = j; read transposed into TMEM), then the dT
+//          operands dU and beta Y (rows, K = j), then S0 again, then dS (rows c),
+//          then the fp32 dGamma rows of the epilogue.
 //   OPA    Kt rows (16 KB) and Kb rows (16 KB); later [dO ; -dY] (32 KB), then
 //          [dP ; dG] (8 KB) and the B operand of R3 (8 KB).
 //   OPQA   [Q1^T | A1^T] (rows c, K = 64, 32 KB).   OPB1T  B1^T (rows c, 16 KB).
 constexpr uint32_t T_Q = 0, T_K = 8192, T_V = 16384, T_DO = 24576, T_G = 32768;
 constexpr uint32_t O_TB = 0, O_TT = 4096, O_PT = 8192, O_U = 0;
 constexpr uint32_t STG = 49152;
+// inside STG: the Gram operands [A1 ; Q1] (64 rows) and B1 (rows, K = c), then
+// the dT operands dU (rows, K = j; an M = 64 product reads 32 further rows past it
+// and ignores what they give) and beta Y (rows, K = j)
+constexpr uint32_t O_AQ = STG, O_B1 = STG + 32768, O_DU = STG, O_BY = STG + 16384;
 constexpr uint32_t OPA = STG + 65536;          // 114688
 constexpr uint32_t O_KT = OPA, O_KB = OPA + 16384, O_OY = OPA, O_PG = OPA, O_R3B = OPA + 8192;
 constexpr uint32_t OPQA = OPA + 32768;         // 147456
@@ -73,18 +79,21 @@ struct Small {
     float beta[C], dbeta[C], red[4][C];
     float e15[D], fC[D], gC[D], gsum[D];
     float red2[4][D];
+    float akkT[C][C];          // solve scratch
+    float tsc[3][16][20];
     uint64_t tma_bar, s0_bar, mma_bar;
     uint32_t tmem_base;
     int abort;
 };
 constexpr size_t kSmem = SMALL + sizeof(Small) + 1024;
 static_assert(kSmem <= 232448, "shared memory budget");
-// fp32 staging of U, dU and Y inside STG (rows of 132 floats)
+// fp32 rows of dGamma in STG (132 floats each)
 constexpr int LU = D + 4;
-static_assert(3 * C * LU * 4 <= 65536, "U, dU, Y staging fits");
 
 // Tensor-memory columns (lanes = value j for dS^T, X, Y, U, dU, dB, dO^T, dS_new;
-// lanes = key channel c for aQ|aK, aB, R1|R2, R3).
+// lanes = key channel c for aQ|aK, aB, R1|R2, R3).  The M = 64 products [G ; P]
+// (in TM_DN, before S0^T) and dP, dT (in TM_X, TM_Y after X and Y are read) put
+// their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47 and so on.
 constexpr uint32_t TM_DS = 0, TM_DN = 128, TM_X = 256, TM_Y = 288, TM_U = 320, TM_DU = 352,
                    TM_DB = 384, TM_DOT = 416, TM_R3 = 480;
 constexpr uint32_t TM_AQK = 256, TM_AB = 320, TM_R12 = 352;
@@ -124,11 +133,11 @@ __device__ __forceinline__ void f32_offsets(int c, uint32_t (&o)[8]) {
 // shared memory (SS) with K-blocks of `akb` and `bkb` bytes; `ksteps` steps of 8.
 __device__ __forceinline__ void mma_ss_group(uint32_t d, const unsigned char *a, uint32_t akb,
                                              const unsigned char *b, uint32_t bkb, int ksteps, int n,
-                                             bool acc) {
+                                             bool acc, int m = 128) {
     const uint64_t da = sdesc_sw128(smem_u32(a)), db = sdesc_sw128(smem_u32(b));
     for (int kk = 0; kk < ksteps; ++kk)
         mma_tf32_ss(d, da + (uint64_t)(((kk >> 2) * akb + (kk & 3) * 32) >> 4),
-                    db + (uint64_t)(((kk >> 2) * bkb + (kk & 3) * 32) >> 4), idesc_tf32(128, n),
+                    db + (uint64_t)(((kk >> 2) * bkb + (kk & 3) * 32) >> 4), idesc_tf32(m, n),
                     (acc || kk > 0) ? 1u : 0u);
 }
 // The same with A in tensor memory (8 columns per K step).
@@ -252,11 +261,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tma_load_3d(base + T_V, &tm_v, &sm.tma_bar, 0, (int)t0, 2 * h);
             tma_load_3d(base + T_DO, &tm_do, &sm.tma_bar, 0, (int)t0, 2 * h);
             tma_load_3d(base + T_G, &tm_g, &sm.tma_bar, 0, (int)t0, 4 * h);
-            if (S0g) load_s0(&sm.s0_bar);
         }
-        if (!S0g)   // no state: S0 = 0
-            for (int i = t; i < 65536 / 16; i += kThreads)
-                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < C) {
             sm.beta[t] = t < L ? beta[(t0 + t) * H + h] : 0.f;
             sm.dbeta[t] = 0.f;
@@ -266,11 +271,6 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             atomicOr(&g_kda_bwdtc_status, 0x800u);
         }
         tma_par ^= 1u;
-        if (S0g && t == 0 && !mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit)) {
-            sm.abort = 1;
-            atomicOr(&g_kda_bwdtc_status, 0x800u);
-        }
-        if (S0g) s0_par ^= 1u;
         __syncthreads();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
@@ -280,10 +280,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (warp < 4 || warp >= 12) {
             const int tp = warp < 4 ? t : t - 256;
             const int c = tp >> 1, part = tp & 1;
-            uint32_t ob[8], of[8], ok[8];
+            uint32_t ob[8], of[8], ok[8], og[8];
             bf16_offsets(c, ob);
             f32_offsets(c, of);
             op_offsets(32, c, ok);
+            op_offsets(64, c, og);
             float gam[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
@@ -322,6 +323,10 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 q1[u & 3] = to_tf32(qv * e1);
                 a1[u & 3] = to_tf32(kv * e1);
                 b1[u & 3] = to_tf32(kv * inv);
+                // the Gram operands: [A1 ; Q1] and B1 as rows (K = c)
+                *reinterpret_cast<float *>(base + O_AQ + r * 128 + og[u & 7]) = a1[u & 3];
+                *reinterpret_cast<float *>(base + O_AQ + (32 + r) * 128 + og[u & 7]) = q1[u & 3];
+                *reinterpret_cast<float *>(base + O_B1 + r * 128 + ok[u & 7]) = b1[u & 3];
                 if ((u & 3) == 3) {
                     const uint32_t pos = (uint32_t)((((r >> 2) ^ (c & 7)) & 7) << 4);
                     *reinterpret_cast<float4 *>(base + OPQA + c * 128 + pos) = make_float4(q1[0], q1[1], q1[2], q1[3]);
@@ -331,10 +336,69 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 }
             }
         }
+        if (warp >= 4 && warp < 8) {   // dO^T into tensor memory (lane j, column r)
+            float x[32];
+            uint32_t ob[8];
+            bf16_offsets(jl, ob);
+#pragma unroll
+            for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f;
+            tmem_st32(tl + TM_DOT, x);
+            tmem_wait_st();
+        }
         fence_proxy_async_smem();
-        // S0^T into tensor memory (lane j, columns c of this warp's half) for the X
-        // product, and gsum[c] = sum_j dS[c][j] S0[c][j] with dS^T from TMEM (warps 4-11)
-        if (warp >= 4 && warp < 12) {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        // ---- phase 2: [G ; P] = [A1 ; Q1] B1^T (M = 64: rows r of G on lanes 0-15 and
+        // 32-47, of P on lanes 64-79 and 96-111); then the state by TMA into STG ----
+        if (t == 0) {
+            tc_fence_after();
+            mma_ss_group(tb + TM_DN, base + O_AQ, 8192, base + O_B1, 4096, 16, 32, false, 64);
+        }
+        mma_wait();
+        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
+        if (S0g) {
+            if (t == 0) {   // STG's Gram operands are consumed: the state goes there
+                fence_proxy_async_smem();
+                load_s0(&sm.s0_bar);
+            }
+        } else {
+            for (int i = t; i < 65536 / 16; i += kThreads)
+                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (warp < 4) {
+            // the collective load runs on every lane of the warp; lanes 0-15 hold rows
+            float x[32];
+            tmem_ld32(tl + TM_DN, x);
+            if (lane < 16) {
+                const int row = 16 * warp + lane;   // 0..63: G rows 0-31, then P rows 0-31
+                const int r = row & 31;
+#pragma unroll
+                for (int i = 0; i < C; ++i) {
+                    if (row < 32) sm.G[r][i] = i < r ? x[i] : 0.f;
+                    else sm.P[r][i] = i <= r ? x[i] : 0.f;
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 0) {   // blocked solve (scratch in the small arrays)
+            float d[32];
+#pragma unroll
+            for (int i = 0; i < C; ++i) d[i] = sm.G[lane][i];
+            solve_t(d, sm.beta[lane], lane, &sm.T[0][0], LDS32, sm.akkT, sm.tsc);
+        } else if (warp >= 4 && warp < 12) {
+            // once the state has landed: S0^T into tensor memory (lane j, columns c of
+            // this warp's half) for the X product, and gsum[c] = sum_j dS[c][j] S0[c][j]
+            bool ok = true;
+            if (S0g && lane == 0) ok = mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok && lane == 0) {
+                sm.abort = 1;
+                atomicOr(&g_kda_bwdtc_status, 0x800u);
+            }
             const int half = (warp - 4) >> 2;
             float p[64];
 #pragma unroll
@@ -349,8 +413,6 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 for (int i = 0; i < 32; ++i) p[32 * h2 + i] = x[i] * d[i];
             }
             tmem_wait_st();
-            // reduce-scatter over the warp's 32 lanes: lane l ends with the sums for
-            // channels 64 half + l and 64 half + 32 + l
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 float *y = p + 32 * h2;
@@ -366,90 +428,12 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 }
                 sm.red2[q4][64 * half + 32 * h2 + lane] = y[0];
             }
-            if (warp < 8) {   // dO^T into tensor memory (lane j, column r)
-                float x[32];
-                uint32_t ob[8];
-                bf16_offsets(jl, ob);
-#pragma unroll
-                for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f;
-                tmem_st32(tl + TM_DOT, x);
-                tmem_wait_st();
-            }
         }
+        if (S0g) s0_par ^= 1u;
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-
         if (t < D) sm.gsum[t] = sm.red2[0][t] + sm.red2[1][t] + sm.red2[2][t] + sm.red2[3][t];
-        // ---- phase 2: G = A1 B1^T (strict) and P = Q1 B1^T (inclusive) from the
-        // transposed operand blocks (threads: product, 2 x 2 tile) ----
-        {
-            // thread: product (G for warps 0-3 and 8-11, P for 4-7 and 12-15), rows
-            // r0..r0+3, columns i0 and i0+16; warps 8-15 sum the channels 64-127 and
-            // hand their partial sums to warps 0-7 through STG
-            const int tp = t & 255, kh = t >> 8;
-            const int prod = tp >> 7, th = tp & 127;
-            const int r0 = (th >> 4) * 4, i0 = th & 15;
-            const unsigned char *Am = base + OPQA + (prod == 0 ? 16384 : 0);   // A1^T or Q1^T
-            const unsigned char *Bm = base + OPB1T;
-            uint32_t oa[8], ob0[8], ob1[8];   // byte offsets of (row c, k) inside row c, for c % 8
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                oa[u] = (uint32_t)((((r0 >> 2) ^ u) & 7) << 4);
-                ob0[u] = (uint32_t)(((((i0 >> 2) ^ u) & 7) << 4) + (i0 & 3) * 4);
-                ob1[u] = (uint32_t)((((((i0 + 16) >> 2) ^ u) & 7) << 4) + (i0 & 3) * 4);
-            }
-            float acc[4][2];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e][0] = acc[e][1] = 0.f;
-#pragma unroll 2
-            for (int c0 = 64 * kh; c0 < 64 * kh + 64; c0 += 8) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float4 x = *reinterpret_cast<const float4 *>(Am + (c0 + u) * 128 + oa[u]);
-                    const float y0 = *reinterpret_cast<const float *>(Bm + (c0 + u) * 128 + ob0[u]);
-                    const float y1 = *reinterpret_cast<const float *>(Bm + (c0 + u) * 128 + ob1[u]);
-                    const float xv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        acc[e][0] += xv[e] * y0;
-                        acc[e][1] += xv[e] * y1;
-                    }
-                }
-            }
-            float *part = reinterpret_cast<float *>(base + STG) + tp * 8;
-            if (kh) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    part[2 * e] = acc[e][0];
-                    part[2 * e + 1] = acc[e][1];
-                }
-            }
-            __syncthreads();
-            if (!kh) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-#pragma unroll
-                    for (int w2 = 0; w2 < 2; ++w2) {
-                        const int r = r0 + e, i = i0 + 16 * w2;
-                        const float v = acc[e][w2] + part[2 * e + w2];
-                        if (prod == 0) sm.G[r][i] = i < r ? v : 0.f;
-                        else sm.P[r][i] = i <= r ? v : 0.f;
-                    }
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {   // blocked solve; STG holds its scratch (the state is in TMEM now)
-            float d[32];
-#pragma unroll
-            for (int i = 0; i < C; ++i) d[i] = sm.G[lane][i];
-            solve_t(d, sm.beta[lane], lane, &sm.T[0][0], LDS32,
-                    reinterpret_cast<float(*)[32]>(base + STG),
-                    reinterpret_cast<float(*)[16][20]>(base + STG + 4096));
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
         // T diag(beta), T^T and P^T as 32-row operands (in the q tile)
         for (int idx = t; idx < C * C; idx += kThreads) {
             const int r = idx >> 5, i = idx & 31;
@@ -523,22 +507,21 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             uint32_t o[8];
             op_offsets(32, jl, o);
             tmem_ld32(tl + TM_U, x);
-            float *sU = reinterpret_cast<float *>(base + STG);
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                sU[r * LU + jl] = x[r];
+            for (int r = 0; r < C; ++r)
                 *reinterpret_cast<float *>(base + O_U + r * 128 + o[r & 7]) = to_tf32(x[r]);
-            }
         } else if (warp < 12) {
             float x[32];
+            uint32_t o[8];
+            op_offsets(32, jl, o);
             tmem_ld32(tl + TM_DU, x);
-            float *sDU = reinterpret_cast<float *>(base + STG) + C * LU;
 #pragma unroll
-            for (int r = 0; r < C; ++r) sDU[r * LU + jl] = x[r];
+            for (int r = 0; r < C; ++r)
+                *reinterpret_cast<float *>(base + O_DU + r * 128 + o[r & 7]) = to_tf32(x[r]);
             tmem_ld32(tl + TM_Y, x);
-            float *sY = reinterpret_cast<float *>(base + STG) + 2 * C * LU;
 #pragma unroll
-            for (int r = 0; r < C; ++r) sY[r * LU + jl] = x[r];
+            for (int r = 0; r < C; ++r)
+                *reinterpret_cast<float *>(base + O_BY + r * 128 + o[r & 7]) = to_tf32(sm.beta[r] * x[r]);
         } else {
             float x[32];
             uint32_t o[8], ob[8];
@@ -556,75 +539,27 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // dP = tril(dO U^T) (warps 0-3 and 8-11) and dT = dU (beta Y)^T (strict, warps
-        // 4-7 and 12-15): thread = rows r0..r0+3, columns i0 and i0+16, 8 values of j
-        // per step; warps 8-15 sum j = 64..127 and hand their partial sums over
-        {
-            const int tp = t & 255, kh = t >> 8;
-            const int prod = tp >> 7, th = tp & 127;
-            const int r0 = (th >> 4) * 4, i0 = th & 15;
-            const float *sU = reinterpret_cast<const float *>(base + STG);
-            const float *sDU = sU + C * LU, *sY = sU + 2 * C * LU;
-            const float *By = prod == 0 ? sU : sY;
-            float acc[4][2];
+        // dP = dO U^T and dT = dU (beta Y)^T as M = 64 products (rows r on lanes 0-15
+        // and 32-47); the second reads 32 rows past dU, whose products it drops
+        if (t == 0) {
+            tc_fence_after();
+            mma_ss_group(tb + TM_X, base + O_OY, 8192, base + O_U, 4096, 16, 32, false, 64);
+            mma_ss_group(tb + TM_Y, base + O_DU, 4096, base + O_BY, 4096, 16, 32, false, 64);
+        }
+        mma_wait();
+        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
+        if (warp < 2) {
+            float x[32], y[32];
+            tmem_ld32(tl + TM_X, x);
+            tmem_ld32(tl + TM_Y, y);
+            if (lane < 16) {
+                const int r = 16 * warp + lane;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e][0] = acc[e][1] = 0.f;
-#pragma unroll 2
-            for (int m = 8 * kh; m < 8 * kh + 8; ++m) {
-                float x[4][8];
-                if (prod == 0) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = r0 + e;
-                        const uint4 w = *reinterpret_cast<const uint4 *>(base + T_DO + (m >> 3) * 4096 + r * 128 +
-                                                                         ((((m & 7) ^ (r & 7)) & 7) << 4));
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            x[e][2 * q] = __uint_as_float(wv[q] << 16);
-                            x[e][2 * q + 1] = __uint_as_float(wv[q] & 0xffff0000u);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 p0 = *reinterpret_cast<const float4 *>(sDU + (r0 + e) * LU + 8 * m);
-                        const float4 p1 = *reinterpret_cast<const float4 *>(sDU + (r0 + e) * LU + 8 * m + 4);
-                        x[e][0] = p0.x; x[e][1] = p0.y; x[e][2] = p0.z; x[e][3] = p0.w;
-                        x[e][4] = p1.x; x[e][5] = p1.y; x[e][6] = p1.z; x[e][7] = p1.w;
-                    }
+                for (int i = 0; i < C; ++i) {
+                    // rows past the chunk's end hold other tokens' dO: their dP is 0
+                    sm.dP[r][i] = (i <= r && r < L) ? x[i] : 0.f;
+                    sm.dT[r][i] = i < r ? y[i] : 0.f;
                 }
-#pragma unroll
-                for (int w2 = 0; w2 < 2; ++w2) {
-                    const float *yp = By + (i0 + 16 * w2) * LU + 8 * m;
-                    const float4 ya = *reinterpret_cast<const float4 *>(yp), yb = *reinterpret_cast<const float4 *>(yp + 4);
-                    const float y[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) acc[e][w2] += x[e][q] * y[q];
-                }
-            }
-            float *part = reinterpret_cast<float *>(base + STG + 51200) + tp * 8;   // past the fp32 staging
-            if (kh) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    part[2 * e] = acc[e][0];
-                    part[2 * e + 1] = acc[e][1];
-                }
-            }
-            __syncthreads();
-            if (!kh) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-#pragma unroll
-                    for (int w2 = 0; w2 < 2; ++w2) {
-                        const int r = r0 + e, i = i0 + 16 * w2;
-                        const float v = acc[e][w2] + part[2 * e + w2];
-                        // rows past the chunk's end hold other tokens' dO: their dP is 0
-                        if (prod == 0) sm.dP[r][i] = (i <= r && r < L) ? v : 0.f;
-                        else sm.dT[r][i] = i < r ? v * sm.beta[i] : 0.f;
-                    }
             }
         }
         if (t < C) sm.dbeta[t] += sm.red[0][t] + sm.red[1][t] + sm.red[2][t] + sm.red[3][t];
