@@ -60,8 +60,12 @@ BWD_MACS_PER_CHUNK_HEAD = (BWD_C * (BWD_C + 1) // 2 * 2 * BWD_D + 7 * BWD_C * BW
                            + 5 * BWD_C * BWD_C * BWD_D // 2 + 2 * BWD_C ** 3 // 3
                            + 3 * BWD_C * BWD_C * BWD_D)
 # fp32 CUDA-core peak of the part: SMs (read from the device) x 128 fp32 lanes x 2 flops
-# per FMA x SM clock
+# per FMA x SM clock (the backward of fp32 inputs or d = 64 runs on the CUDA cores)
 FP32_LANES_PER_SM = 128
+# The tensor-core backward (bf16 inputs, d = 128) multiplies in tf32: its peak is the
+# measured bf16 dense rate times the nominal tf32 / bf16 ratio of the part (1.1 / 2.25
+# PFLOP/s dense)
+TF32_PER_BF16 = 1.1 / 2.25
 # Decode, per (sequence, head) step: fp32 state read + write (2 x 65536),
 # q/k/v bf16 (768), g fp32 (512), beta (4), o bf16 (256).
 DECODE_BYTES_PER_HEAD_STEP = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 4 + 128 * 2  # 132612
@@ -504,12 +508,15 @@ def run_gpu(args):
     bw_flops = 2.0 * BWD_MACS_PER_CHUNK_HEAD * ((T + BWD_C - 1) // BWD_C) * w.heads
     sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
     fp32_peak = sm_count * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    tf32_peak = bf16_tf * TF32_PER_BF16
     bw_ach = bw_flops / (ms_bw * 1e-3) / 1e12
     legs["backward"] = {"ms": round(ms_bw, 3), "tok_s": round(T * world / (ms_bw * 1e-3)),
-                        "bound": "alu", "tflops": round(bw_ach, 2),
-                        "peak_tflops": round(fp32_peak, 2),
-                        "frac": round(bw_ach / fp32_peak, 4), "steps": bw_steps,
-                        "kernel": "kda_backward_kernel"}
+                        "bound": "tensor", "tflops": round(bw_ach, 2),
+                        "peak_tflops": round(tf32_peak, 1),
+                        "peak_source": f"tf32 = {peak_src} bf16 x {TF32_PER_BF16:.3f} (nominal ratio)",
+                        "frac": round(bw_ach / tf32_peak, 4),
+                        "frac_of_fp32_alu": round(bw_ach / fp32_peak, 4), "steps": bw_steps,
+                        "kernel": "kda_backward_tc_kernel"}
     del cstates, d_out
 
     # ---------------- e2e through the public API, host buffers ----------------

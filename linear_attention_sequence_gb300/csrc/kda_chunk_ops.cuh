@@ -5,17 +5,6 @@
 
 #include "sm100_ptx.cuh"
 
-// Host: the TMA view of a [T, H, 128] tensor that the tensor-core prefill uses:
-// (element within a 128-byte segment, token, segment index along the H*128 row),
-// box = one head's segments for 32 tokens, 128-byte swizzle.  False if the
-// driver entry point is missing or the encoding fails.
-bool kda_make_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
-                       int64_t T, int H);
-
-// Host: the TMA view of an fp32 array of 128 x 128 states as rows of 128
-// floats, box 128 rows x 32 floats, 128-byte swizzle.
-bool kda_make_state_map(CUtensorMap *m, const float *base, int64_t rows);
-
 namespace kda_chunk {
 
 using namespace sm100;

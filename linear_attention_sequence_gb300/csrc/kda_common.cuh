@@ -1,6 +1,7 @@
 // kda_common.cuh -- small helpers shared by the KDA kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -113,6 +114,17 @@ __device__ __forceinline__ int64_t ckpt_first_row(const int32_t *cu, int n, int6
 
 }  // namespace kda
 
+// Host: the TMA view of a [T, H, 128] tensor that the tensor-core prefill uses:
+// (element within a 128-byte segment, token, segment index along the H*128 row),
+// box = one head's segments for 32 tokens, 128-byte swizzle.  False if the
+// driver entry point is missing or the encoding fails.
+bool kda_make_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
+                       int64_t T, int H);
+
+// Host: the TMA view of an fp32 array of 128 x 128 states as rows of 128
+// floats, box 128 rows x 32 floats, 128-byte swizzle.
+bool kda_make_state_map(CUtensorMap *m, const float *base, int64_t rows);
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t kda_launch_decode(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const float *beta, float *state, void *out,
@@ -136,6 +148,8 @@ cudaError_t kda_launch_qkv_prologue(const kda::Problem &P, const void *xq, const
                                     const int32_t *cu, void *q, void *k, void *v, float *cout,
                                     float eps, cudaStream_t stream);
 cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status);
+cudaError_t kda_tc_read_status(unsigned *status);
+bool kda_tma_available();
 cudaError_t kda_launch_selftest_timeout(cudaStream_t stream);
 bool kda_prefill_chain_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
                                  const float *g, const void *out);

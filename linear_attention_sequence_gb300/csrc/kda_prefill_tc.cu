@@ -889,55 +889,19 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 3-D view of a [T, H, D] tensor: (element within a 128-byte segment, token,
-// segment index along the H*D row); box = one head's segments for C tokens,
-// stored segment by segment (C rows of 128 bytes each), 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int64_t T,
-              int H) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const int seg = 128 / esize, nseg = D / seg;
-    const cuuint64_t dims[3] = {(cuuint64_t)seg, (cuuint64_t)T, (cuuint64_t)H * nseg};
-    const cuuint64_t strides[2] = {(cuuint64_t)H * D * esize, 128};
-    const cuuint32_t box[3] = {(cuuint32_t)seg, (cuuint32_t)C, (cuuint32_t)nseg};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename OUT_T>
 cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const void *v,
                    const float *g, const float *beta, const float *init_state, const int32_t *cu,
                    void *out, float *final_state, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mg, mo;
-    if (!make_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
-        !make_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
-        !make_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
-        !(P.a_log          ? make_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
-          : P.scalar_decay ? make_map(&mg, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)   // unused
-                           : make_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)) ||
-        !(sizeof(OUT_T) == 2 ? make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
-                             : make_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
+    if (!kda_make_tile_map(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
+        !kda_make_tile_map(&mk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
+        !kda_make_tile_map(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H) ||
+        !(P.a_log          ? kda_make_tile_map(&mg, P.z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
+          : P.scalar_decay ? kda_make_tile_map(&mg, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)   // unused
+                           : kda_make_tile_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)) ||
+        !(sizeof(OUT_T) == 2 ? kda_make_tile_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, P.T, P.H)
+                             : kda_make_tile_map(&mo, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H)))
         return cudaErrorInvalidValue;
     auto kern = P.a_log          ? kda_prefill_tc_kernel<OUT_T, true, false>
                 : P.scalar_decay ? kda_prefill_tc_kernel<OUT_T, false, true>
@@ -956,34 +920,12 @@ cudaError_t launch(const kda::Problem &P, const void *q, const void *k, const vo
 
 }  // namespace
 
-// The 3-D TMA view of a [T, H, 128] tensor (box: one head's 128-byte segments
-// for 32 tokens, 128-byte swizzle), for the other kernels that load chunk tiles.
-bool kda_make_tile_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize,
-                       int64_t T, int H) {
-    return make_map(m, base, dt, esize, T, H);
-}
-
-// The TMA view of an fp32 state array [rows, 128] (rows = states x 128 key
-// channels): box = 128 rows x 32 columns, 128-byte swizzle, so that four boxes
-// give a 128-row K-major SW128 operand (rows = key channel, K = value index).
-bool kda_make_state_map(CUtensorMap *m, const float *base, int64_t rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || rows <= 0) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-    const cuuint32_t box[2] = {32, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool kda_prefill_tc_supported(const kda::Problem &P, const void *q, const void *k, const void *v,
                               const float *g, const void *out) {
     auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
     return P.dk == 128 && P.dv == 128 && P.in_dtype == KDA_DTYPE_BF16 && P.T > 0 &&
            P.T <= 0x7fffffff - C && al16(q) && al16(k) && al16(v) && (P.scalar_decay || al16(g)) && al16(out) &&
-           encode_fn() != nullptr;
+           kda_tma_available();
 }
 
 cudaError_t kda_launch_prefill_tc(const kda::Problem &P, const void *q, const void *k,
@@ -1016,19 +958,13 @@ cudaError_t kda_launch_selftest_timeout(cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t kda_read_device_status(cudaStream_t stream, unsigned *status) {
-    cudaError_t e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return e;
-    e = cudaMemcpyFromSymbol(status, g_kda_device_status, sizeof(unsigned));
+// Read and clear this kernel's status word (ORed into *status).
+cudaError_t kda_tc_read_status(unsigned *status) {
+    unsigned st = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&st, g_kda_device_status, sizeof(unsigned));
     if (e != cudaSuccess) return e;
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_kda_device_status, &zero, sizeof(unsigned));
-    if (e != cudaSuccess) return e;
-    e = kda_chain_read_status(status);   // the split kernel's status word
-    if (e != cudaSuccess) return e;
-    e = kda_2pass_read_status(status);   // the two-pass kernels' status word
-    if (e != cudaSuccess) return e;
-    e = kda_bwd_read_status(status);     // the backward's argument check
-    if (e != cudaSuccess) return e;
-    return kda_bwdtc_read_status(status);   // the tensor-core backward's word
+    *status |= st;
+    return e;
 }
