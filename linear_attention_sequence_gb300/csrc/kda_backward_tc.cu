@@ -28,8 +28,11 @@
 // a 128-long side is one tcgen05.mma kind::tf32 group with M = 128 (values or
 // key channels) and fp32 accumulation; its operands are written by the threads
 // as K-major SW128 tf32 blocks in shared memory, or read from tensor memory.
-// The 32 x 32 pieces (G, P, the solve, dP, dT, dA) run on the CUDA cores.  The
-// phases of a chunk run one after another, separated by block barriers.
+// The pairs [G ; P] and dP, dT are M = 64 products whose 32-row operands are
+// read with 32 further rows of shared memory past them (the rows of the result
+// that those give are not read).  The solve, dA = -T^T dT T^T and the pairwise
+// 32 x 32 terms run on the CUDA cores.  The phases of a chunk run one after
+// another, separated by block barriers.
 
 #include <mutex>
 
