@@ -53,13 +53,14 @@ constexpr int kThreads = 512;
 constexpr uint32_t kPollLimit = 1u << 23;
 
 // Shared memory (byte offsets from a 1024-aligned base).
-//   TILE   TMA tiles of the chunk: q, k, v, dO (bf16, 8 KB each), g (fp32, 16 KB;
-//          Gamma in place).  After the preparation the q and k tiles hold the
-//          operands T diag(beta), T^T, P^T (4 KB each), later U (16 KB).
+//   TILE   TMA tiles of the chunk: q, k, v, dO (bf16, 8 KB each), g (fp32, 16 KB).
+//          After the preparation the q and k tiles hold the operands T diag(beta),
+//          T^T, P^T (4 KB each), later U (16 KB).  Once the aB product has read U,
+//          the next chunk's tiles are loaded here.
 //   STG    64 KB staging: the Gram operands [A1 ; Q1] and B1 (rows, K = c), then
 //          S0 by TMA (rows c, K = j; read transposed into TMEM), then the dT
 //          operands dU and beta Y (rows, K = j), then S0 again, then dS (rows c),
-//          then the fp32 dGamma rows of the epilogue.
+//          then the epilogue's per-slice sums.
 //   OPA    Kt rows (16 KB) and Kb rows (16 KB); later [dO ; -dY] (32 KB), then
 //          [dP ; dG] (8 KB) and the B operand of R3 (8 KB).
 //   OPQA   [Q1^T | A1^T] (rows c, K = 64, 32 KB).   OPB1T  B1^T (rows c, 16 KB).
@@ -90,22 +91,20 @@ struct Small {
 };
 constexpr size_t kSmem = SMALL + sizeof(Small) + 1024;
 static_assert(kSmem <= 232448, "shared memory budget");
-// fp32 rows of dGamma in STG (132 floats each)
-constexpr int LU = D + 4;
 
 // Tensor-memory columns (lanes = value j for dS^T, X, Y, U, dU, dB, dO^T, dS_new;
-// lanes = key channel c for aQ|aK, aB, R1|R2, R3).  The M = 64 products [G ; P]
+// lanes = key channel c for aQ|aK, aB, R1|R2, R3, e^{Gamma - Gamma_15}).  The M = 64 products [G ; P]
 // (in TM_DN, before S0^T) and dP, dT (in TM_X, TM_Y after X and Y are read) put
 // their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47 and so on.
 constexpr uint32_t TM_DS = 0, TM_DN = 128, TM_X = 256, TM_Y = 288, TM_U = 320, TM_DU = 352,
-                   TM_DB = 384, TM_DOT = 416, TM_R3 = 480;
+                   TM_DB = 384, TM_DOT = 416, TM_EX = 480;
+// R3 goes where the dS0 increment was (read by then); TM_EX (lane c, column token)
+// keeps e^{Gamma - Gamma_15} from the preparation to the gradient epilogue
+constexpr uint32_t TM_R3 = TM_DN;
 constexpr uint32_t TM_AQK = 256, TM_AB = 320, TM_R12 = 352;
 
 __device__ __forceinline__ uint32_t off_bf16(int r, int c) {   // TMA tile (SW128), bf16
     return (uint32_t)((c >> 6) * 4096 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1));
-}
-__device__ __forceinline__ uint32_t off_f32(int r, int c) {    // TMA tile (SW128), fp32
-    return (uint32_t)((c >> 5) * 4096 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + ((c & 3) << 2));
 }
 __device__ __forceinline__ float lds_bf16(const unsigned char *p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
@@ -207,6 +206,29 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const uint32_t tl = tb + lane_off;
     uint32_t tma_par = 0, s0_par = 0, mma_par = 0;
 
+    // The tiles of the chunk at token tx (q, k, v, dO bf16; g fp32) by TMA on tma_bar.
+    // A chunk's tiles are issued while the chunk after it is finished (thread 0 keeps
+    // the parity of the group in flight so that a stop can still wait for it).
+    auto load_tiles = [&](int64_t tx) {
+        mbar_arrive_expect_tx(&sm.tma_bar, 4 * 8192 + 16384);
+        tma_load_3d(base + T_Q, &tm_q, &sm.tma_bar, 0, (int)tx, 2 * h);
+        tma_load_3d(base + T_K, &tm_k, &sm.tma_bar, 0, (int)tx, 2 * h);
+        tma_load_3d(base + T_V, &tm_v, &sm.tma_bar, 0, (int)tx, 2 * h);
+        tma_load_3d(base + T_DO, &tm_do, &sm.tma_bar, 0, (int)tx, 2 * h);
+        tma_load_3d(base + T_G, &tm_g, &sm.tma_bar, 0, (int)tx, 4 * h);
+    };
+    bool tiles_pending = false;
+    uint32_t pend_par = 0;
+    float bnext = 0.f;   // beta of the next chunk (threads 0..C-1)
+    if (nchunks > 0) {   // the last chunk comes first
+        const int64_t tx = a + (int64_t)(nchunks - 1) * C;
+        if (t == 0) {
+            load_tiles(tx);
+            tiles_pending = true;
+        }
+        if (t < C && tx + t < b) bnext = beta[(tx + t) * H + h];
+    }
+
     // MMA groups are issued and awaited by thread 0; the barrier releases the rest.
     auto mma_wait = [&]() {
         if (t == 0) {
@@ -256,96 +278,96 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int kb = 0; kb < 4; ++kb) tma_load_2d(base + STG + kb * 16384, s0map, bar, 32 * kb, s0row);
         };
 
-        // ---- phase 0: the chunk's tiles by TMA; beta ----
-        if (t == 0) {
-            mbar_arrive_expect_tx(&sm.tma_bar, 4 * 8192 + 16384);
-            tma_load_3d(base + T_Q, &tm_q, &sm.tma_bar, 0, (int)t0, 2 * h);
-            tma_load_3d(base + T_K, &tm_k, &sm.tma_bar, 0, (int)t0, 2 * h);
-            tma_load_3d(base + T_V, &tm_v, &sm.tma_bar, 0, (int)t0, 2 * h);
-            tma_load_3d(base + T_DO, &tm_do, &sm.tma_bar, 0, (int)t0, 2 * h);
-            tma_load_3d(base + T_G, &tm_g, &sm.tma_bar, 0, (int)t0, 4 * h);
-        }
+        // ---- phase 0: the chunk's tiles (issued a chunk ahead) have landed; beta ----
         if (t < C) {
-            sm.beta[t] = t < L ? beta[(t0 + t) * H + h] : 0.f;
+            sm.beta[t] = bnext;
             sm.dbeta[t] = 0.f;
         }
-        if (t == 0 && !mbar_wait_bounded(&sm.tma_bar, tma_par, kPollLimit)) {
-            sm.abort = 1;
-            atomicOr(&g_kda_bwdtc_status, 0x800u);
+        if (t == 0) {
+            if (mbar_wait_bounded(&sm.tma_bar, tma_par, kPollLimit)) {
+                tiles_pending = false;
+            } else {
+                sm.abort = 1;
+                atomicOr(&g_kda_bwdtc_status, 0x800u);
+            }
         }
         tma_par ^= 1u;
         __syncthreads();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 1: Gamma and the decay-weighted operands on warps 0-3 and 12-15
-        // (thread = channel c, tokens 16 part .. 16 part + 15; the two parts of a
-        // channel in adjacent lanes), while warps 4-11 move S0^T into TMEM ----
-        if (warp < 4 || warp >= 12) {
-            const int tp = warp < 4 ? t : t - 256;
-            const int c = tp >> 1, part = tp & 1;
+        // ---- phase 1 (all 16 warps; thread = key channel c = its TMEM lane, tokens
+        // 8 slice .. 8 slice + 7): Gamma, the decay-weighted operands, dO^T and
+        // e^{Gamma - Gamma_15} into tensor memory ----
+        {
+            const int c = jl, r0 = 8 * slice;
             uint32_t ob[8], of[8], ok[8], og[8];
             bf16_offsets(c, ob);
             f32_offsets(c, of);
             op_offsets(32, c, ok);
             op_offsets(64, c, og);
-            float gam[16];
+            float gam[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int r = 16 * part + u;
-                gam[u] = r < L ? *reinterpret_cast<const float *>(base + T_G + r * 128 + of[u & 7]) : 0.f;
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u;
+                gam[u] = r < L ? *reinterpret_cast<const float *>(base + T_G + r * 128 + of[u]) : 0.f;
             }
 #pragma unroll
-            for (int u = 1; u < 16; ++u) gam[u] += gam[u - 1];
-            const float lo = __shfl_up_sync(0xffffffffu, gam[15], 1, 2);
-            if (part) {
+            for (int u = 1; u < 8; ++u) gam[u] += gam[u - 1];
+            sm.red2[slice][c] = gam[7];
+            uint32_t dov[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) gam[u] += lo;
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u;
+                dov[u] = __float_as_uint(r < L ? lds_bf16(base + T_DO + r * 128 + ob[u]) : 0.f);
             }
-            const float g15 = __shfl_sync(0xffffffffu, gam[15], lane & ~1);
-            const float gl = __shfl_sync(0xffffffffu, gam[15], lane | 1);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) *reinterpret_cast<float *>(base + T_G + (16 * part + u) * 128 + of[u & 7]) = gam[u];
-            if (part == 0) {
-                sm.e15[c] = __expf(g15);
-                sm.fC[c] = __expf(gl - g15);
+            tmem_st8(tl + TM_DOT + r0, dov);
+            __syncthreads();
+            const float p0 = sm.red2[0][c], p1 = sm.red2[1][c], p2 = sm.red2[2][c], p3 = sm.red2[3][c];
+            const float g15 = p0 + p1, gl = g15 + p2 + p3;
+            // Gamma_r - Gamma_15 for this thread's tokens: the sums of the earlier slices
+            const float base_x = (slice == 0 ? 0.f : slice == 1 ? p0 : slice == 2 ? g15 : g15 + p2) - g15;
+            const float e15 = __expf(g15), fC = __expf(gl - g15);
+            if (slice == 0) {
+                sm.e15[c] = e15;
+                sm.fC[c] = fC;
                 sm.gC[c] = __expf(gl);
             }
-            float q1[4], a1[4], b1[4];
+            float q1[8], a1[8], b1[8];
+            uint32_t exv[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int r = 16 * part + u;
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u;
                 float qv = 0.f, kv = 0.f;
                 if (r < L) {
-                    qv = lds_bf16(base + T_Q + r * 128 + ob[u & 7]);
-                    kv = lds_bf16(base + T_K + r * 128 + ob[u & 7]);
+                    qv = lds_bf16(base + T_Q + r * 128 + ob[u]);
+                    kv = lds_bf16(base + T_K + r * 128 + ob[u]);
                 }
-                const float x = gam[u] - g15;
+                const float x = base_x + gam[u];             // in [-80, 80] by the log-decay bound
                 const float e1 = __expf(x), inv = __expf(-x);
-                *reinterpret_cast<float *>(base + O_KT + r * 128 + ok[u & 7]) = to_tf32(kv * __expf(gam[u]));
-                *reinterpret_cast<float *>(base + O_KB + r * 128 + ok[u & 7]) = to_tf32(kv * __expf(gl - gam[u]));
-                q1[u & 3] = to_tf32(qv * e1);
-                a1[u & 3] = to_tf32(kv * e1);
-                b1[u & 3] = to_tf32(kv * inv);
+                const float ka = kv * e1, kbv = kv * inv;
+                exv[u] = __float_as_uint(e1);
+                q1[u] = to_tf32(qv * e1);
+                a1[u] = to_tf32(ka);
+                b1[u] = to_tf32(kbv);
+                // Kt = k e^{Gamma} and Kb = k e^{Gamma_C - Gamma} as rows (K = c)
+                *reinterpret_cast<float *>(base + O_KT + r * 128 + ok[u]) = to_tf32(ka * e15);
+                *reinterpret_cast<float *>(base + O_KB + r * 128 + ok[u]) = to_tf32(kbv * fC);
                 // the Gram operands: [A1 ; Q1] and B1 as rows (K = c)
-                *reinterpret_cast<float *>(base + O_AQ + r * 128 + og[u & 7]) = a1[u & 3];
-                *reinterpret_cast<float *>(base + O_AQ + (32 + r) * 128 + og[u & 7]) = q1[u & 3];
-                *reinterpret_cast<float *>(base + O_B1 + r * 128 + ok[u & 7]) = b1[u & 3];
-                if ((u & 3) == 3) {
-                    const uint32_t pos = (uint32_t)((((r >> 2) ^ (c & 7)) & 7) << 4);
-                    *reinterpret_cast<float4 *>(base + OPQA + c * 128 + pos) = make_float4(q1[0], q1[1], q1[2], q1[3]);
-                    *reinterpret_cast<float4 *>(base + OPQA + 16384 + c * 128 + pos) =
-                        make_float4(a1[0], a1[1], a1[2], a1[3]);
-                    *reinterpret_cast<float4 *>(base + OPB1T + c * 128 + pos) = make_float4(b1[0], b1[1], b1[2], b1[3]);
-                }
+                *reinterpret_cast<float *>(base + O_AQ + r * 128 + og[u]) = a1[u];
+                *reinterpret_cast<float *>(base + O_AQ + (32 + r) * 128 + og[u]) = q1[u];
+                *reinterpret_cast<float *>(base + O_B1 + r * 128 + ok[u]) = b1[u];
             }
-        }
-        if (warp >= 4 && warp < 8) {   // dO^T into tensor memory (lane j, column r)
-            float x[32];
-            uint32_t ob[8];
-            bf16_offsets(jl, ob);
+            tmem_st8(tl + TM_EX + r0, exv);
+            // [Q1^T | A1^T] and B1^T as rows c (K = token), four tokens per 16-byte store
 #pragma unroll
-            for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f;
-            tmem_st32(tl + TM_DOT, x);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t pos = (uint32_t)(((((r0 >> 2) + h2) ^ (c & 7)) & 7) << 4);
+                const int u = 4 * h2;
+                *reinterpret_cast<float4 *>(base + OPQA + c * 128 + pos) = make_float4(q1[u], q1[u + 1], q1[u + 2], q1[u + 3]);
+                *reinterpret_cast<float4 *>(base + OPQA + 16384 + c * 128 + pos) =
+                    make_float4(a1[u], a1[u + 1], a1[u + 2], a1[u + 3]);
+                *reinterpret_cast<float4 *>(base + OPB1T + c * 128 + pos) = make_float4(b1[u], b1[u + 1], b1[u + 2], b1[u + 3]);
+            }
             tmem_wait_st();
         }
         fence_proxy_async_smem();
@@ -613,6 +635,17 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
+        // The tile area's last reader (the aB product) is complete: the next chunk's
+        // tiles and beta are fetched during the rest of this one.
+        if (ch > 0) {
+            if (t == 0) {
+                load_tiles(t0 - C);
+                tiles_pending = true;
+                pend_par = tma_par;
+            }
+            if (t < C) bnext = beta[(t0 - C + t) * H + h];   // chunk ch - 1 is a whole chunk
+        }
+
         // ---- phase 7: dS^T <- dS^T Diag(gamma_C) + (increment)^T Diag(e15) on warps
         // 0-7 (lane j, half of the channels each), while warps 8-15 form dA, dG and
         // the dA . G row sums ----
@@ -709,53 +742,62 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
         // ---- phase 8 (lane = key channel c, tokens 8 slice .. 8 slice + 7): dq, dk,
-        // dGamma (into STG), then dg as the reverse running sum (threads 0-127) ----
+        // dGamma, and dg as its reverse running sum (within the thread's tokens, then
+        // across the four slices through shared memory) ----
         {
             const int c = jl, x0 = 8 * slice;
             const float e15 = sm.e15[c], fC = sm.fC[c];
-            const float gl = *reinterpret_cast<const float *>(base + T_G + off_f32(C - 1, c));
-            const float g15 = *reinterpret_cast<const float *>(base + T_G + off_f32(15, c));
-            float aq[8], ak[8], ab[8], r1[8], r2[8], r3[8];
+            float aq[8], ak[8], ab[8], r1[8], r2[8], r3[8], ex[8];
             tmem_ld8(tl + TM_AQK + x0, aq);
             tmem_ld8(tl + TM_AQK + 32 + x0, ak);
             tmem_ld8(tl + TM_AB + x0, ab);
             tmem_ld8(tl + TM_R12 + x0, r1);
             tmem_ld8(tl + TM_R12 + 32 + x0, r2);
             tmem_ld8(tl + TM_R3 + x0, r3);
-            float *sDG = reinterpret_cast<float *>(base + STG);   // [C][LU]
-            float kbk = 0.f;
+            tmem_ld8(tl + TM_EX + x0, ex);
+            float q1[8], a1[8], b1[8];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t pos = (uint32_t)(((((x0 >> 2) + h2) ^ (c & 7)) & 7) << 4);
+                const float4 vq = *reinterpret_cast<const float4 *>(base + OPQA + c * 128 + pos);
+                const float4 va = *reinterpret_cast<const float4 *>(base + OPQA + 16384 + c * 128 + pos);
+                const float4 vb = *reinterpret_cast<const float4 *>(base + OPB1T + c * 128 + pos);
+                q1[4 * h2] = vq.x; q1[4 * h2 + 1] = vq.y; q1[4 * h2 + 2] = vq.z; q1[4 * h2 + 3] = vq.w;
+                a1[4 * h2] = va.x; a1[4 * h2 + 1] = va.y; a1[4 * h2 + 2] = va.z; a1[4 * h2 + 3] = va.w;
+                b1[4 * h2] = vb.x; b1[4 * h2 + 1] = vb.y; b1[4 * h2 + 2] = vb.z; b1[4 * h2 + 3] = vb.w;
+            }
+            float dgam[8], kbk = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int x = x0 + u;
-                const float gx = *reinterpret_cast<const float *>(base + T_G + off_f32(x, c));
-                const float ex = __expf(gx - g15), ix = __expf(g15 - gx);
+                const float ix = __fdividef(1.f, ex[u]);       // e^{Gamma_15 - Gamma_x}
                 const float sq = e15 * aq[u] + r1[u], sk = e15 * ak[u] + r2[u];
                 const float fb = fC * ab[u];
                 if (x < L) {
                     const int64_t off = (t0 + x) * rowK + (int64_t)h * D + c;
-                    kda::st_elem(dq + off, ex * sq);
-                    kda::st_elem(dk + off, ex * sk + __expf(gl - gx) * ab[u] + ix * r3[u]);
+                    kda::st_elem(dq + off, ex[u] * sq);
+                    // e^{Gamma_C - Gamma_x} aB + e^{Gamma_15 - Gamma_x} R3 = e^{Gamma_15 - Gamma_x} (fC aB + R3)
+                    kda::st_elem(dk + off, ex[u] * sk + ix * (fb + r3[u]));
                 }
-                const float q1 = *reinterpret_cast<const float *>(base + OPQA + sw_off(128, c, x));
-                const float a1 = *reinterpret_cast<const float *>(base + OPQA + 16384 + sw_off(128, c, x));
-                const float b1 = *reinterpret_cast<const float *>(base + OPB1T + sw_off(128, c, x));
-                sDG[x * LU + c] = q1 * sq + a1 * sk - b1 * (fb + r3[u]);
-                kbk += fb * b1;
+                dgam[u] = q1[u] * sq + a1[u] * sk - b1[u] * (fb + r3[u]);
+                kbk += fb * b1[u];
             }
-            sm.red2[slice][c] = kbk;
-        }
-        __syncthreads();
-        if (t < D) {
-            const int c = t;
-            const float *sDG = reinterpret_cast<const float *>(base + STG);
-            float run = 0.f;
-            const float last = sm.fC[c] * sm.e15[c] * sm.gsum[c] + sm.red2[0][c] + sm.red2[1][c] +
-                               sm.red2[2][c] + sm.red2[3][c];
-#pragma unroll 4
-            for (int r = C - 1; r >= 0; --r) {
-                run += sDG[r * LU + c] + (r == C - 1 ? last : 0.f);
-                if (r < L) dg[(t0 + r) * rowK + (int64_t)h * D + c] = run;
+#pragma unroll
+            for (int u = 6; u >= 0; --u) dgam[u] += dgam[u + 1];
+            float *part_sum = reinterpret_cast<float *>(base + STG);          // [4][D]
+            float *part_kbk = reinterpret_cast<float *>(base + STG) + 4 * D;  // [4][D]
+            part_sum[slice * D + c] = dgam[0];
+            part_kbk[slice * D + c] = kbk;
+            __syncthreads();
+            float later = sm.fC[c] * sm.e15[c] * sm.gsum[c];
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2) {
+                later += part_kbk[s2 * D + c];
+                if (s2 > slice) later += part_sum[s2 * D + c];
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (x0 + u < L) dg[(t0 + x0 + u) * rowK + (int64_t)h * D + c] = dgam[u] + later;
         }
         if (t < C && t < L) dbeta[(t0 + t) * H + h] = sm.dbeta[t];
         tc_fence_before();
@@ -772,10 +814,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int i = 0; i < 32; ++i) d_init[soff + (int64_t)(c0 + i) * D + jl] = x[i];
         }
     }
-    if (t == 0) {   // every MMA issued has completed (after a stop too)
+    if (t == 0) {   // every MMA and tile copy issued has completed (after a stop too)
         tc_fence_after();
         mma_commit(&sm.mma_bar);
         mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit);
+        if (tiles_pending) mbar_wait_bounded(&sm.tma_bar, pend_par, kPollLimit);
     }
     tc_fence_before();
     __syncthreads();
