@@ -55,22 +55,22 @@ constexpr uint32_t kPollLimit = 1u << 23;
 // Shared memory (byte offsets from a 1024-aligned base).
 //   TILE   TMA tiles of the chunk: q, k, v, dO (bf16, 8 KB each), g (fp32, 16 KB).
 //          After the preparation the q and k tiles hold the operands T diag(beta),
-//          T^T, P^T (4 KB each), later U (16 KB).  Once the aB product has read U,
-//          the next chunk's tiles are loaded here.
+//          T^T, P^T (4 KB each), later U, dU and beta Y (16 KB each).  Once the aB
+//          product has read U, the next chunk's tiles are loaded here.
 //   STG    64 KB staging: the Gram operands [A1 ; Q1] and B1 (rows, K = c), then
-//          S0 by TMA (rows c, K = j; read transposed into TMEM), then the dT
-//          operands dU and beta Y (rows, K = j), then S0 again, then dS (rows c),
-//          then the epilogue's per-slice sums.
+//          S0 by TMA (rows c, K = j; read transposed into TMEM, and the A operand
+//          of [aQ | aK]), then dS (rows c), then the epilogue's per-slice sums.
 //   OPA    Kt rows (16 KB) and Kb rows (16 KB); later [dO ; -dY] (32 KB), then
 //          [dP ; dG] (8 KB) and the B operand of R3 (8 KB).
 //   OPQA   [Q1^T | A1^T] (rows c, K = 64, 32 KB).   OPB1T  B1^T (rows c, 16 KB).
 constexpr uint32_t T_Q = 0, T_K = 8192, T_V = 16384, T_DO = 24576, T_G = 32768;
-constexpr uint32_t O_TB = 0, O_TT = 4096, O_PT = 8192, O_U = 0;
+constexpr uint32_t O_TB = 0, O_TT = 4096, O_PT = 8192;
+// the dP / dT operands U, dU and beta Y (rows, K = j; 16 KB each) in the tile area (an
+// M = 64 product reads 32 further rows past dU: the beta Y rows, whose products it drops)
+constexpr uint32_t O_U = 0, O_DU = 16384, O_BY = 32768;
 constexpr uint32_t STG = 49152;
-// inside STG: the Gram operands [A1 ; Q1] (64 rows) and B1 (rows, K = c), then
-// the dT operands dU (rows, K = j; an M = 64 product reads 32 further rows past it
-// and ignores what they give) and beta Y (rows, K = j)
-constexpr uint32_t O_AQ = STG, O_B1 = STG + 32768, O_DU = STG, O_BY = STG + 16384;
+// inside STG: the Gram operands [A1 ; Q1] (64 rows) and B1 (rows, K = c)
+constexpr uint32_t O_AQ = STG, O_B1 = STG + 32768;
 constexpr uint32_t OPA = STG + 65536;          // 114688
 constexpr uint32_t O_KT = OPA, O_KB = OPA + 16384, O_OY = OPA, O_PG = OPA, O_R3B = OPA + 8192;
 constexpr uint32_t OPQA = OPA + 32768;         // 147456
@@ -92,16 +92,15 @@ struct Small {
 constexpr size_t kSmem = SMALL + sizeof(Small) + 1024;
 static_assert(kSmem <= 232448, "shared memory budget");
 
-// Tensor-memory columns (lanes = value j for dS^T, X, Y, U, dU, dB, dO^T, dS_new;
-// lanes = key channel c for aQ|aK, aB, R1|R2, R3, e^{Gamma - Gamma_15}).  The M = 64 products [G ; P]
-// (in TM_DN, before S0^T) and dP, dT (in TM_X, TM_Y after X and Y are read) put
-// their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47 and so on.
+// Tensor-memory columns (lanes = value j for dS^T, X, Y, U, dU, dB, dO^T, the dS0
+// increment; lanes = key channel c for aQ|aK, aB, R1|R2, R3, e^{Gamma - Gamma_15}).
+// The M = 64 products [G ; P] (in TM_DN, before S0^T) and dP, dT (in TM_X, TM_Y
+// after X and Y are read) put their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47
+// and so on.  TM_DN holds the Gram, then S0^T, then aQ|aK; the dS0 increment takes
+// 256-383 once dP, dT, U and dU are read, and R1|R2, R3 take 256-351 after it.
 constexpr uint32_t TM_DS = 0, TM_DN = 128, TM_X = 256, TM_Y = 288, TM_U = 320, TM_DU = 352,
                    TM_DB = 384, TM_DOT = 416, TM_EX = 480;
-// R3 goes where the dS0 increment was (read by then); TM_EX (lane c, column token)
-// keeps e^{Gamma - Gamma_15} from the preparation to the gradient epilogue
-constexpr uint32_t TM_R3 = TM_DN;
-constexpr uint32_t TM_AQK = 256, TM_AB = 320, TM_R12 = 352;
+constexpr uint32_t TM_AQK = TM_DN, TM_INC = 256, TM_AB = 384, TM_R12 = 256, TM_R3 = 320;
 
 __device__ __forceinline__ uint32_t off_bf16(int r, int c) {   // TMA tile (SW128), bf16
     return (uint32_t)((c >> 6) * 4096 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1));
@@ -500,8 +499,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
         // ---- phase 5 (lane j): dV = dY = diag(beta) dB and the dB . Y row sums
-        // (warps 0-3); U (warps 4-7) and dU, Y (warps 8-11) in fp32 into STG and U as
-        // an operand; the operand rows [dO ; -dY] (warps 12-15) ----
+        // (warps 0-3); the operands U (warps 4-7), dU and beta Y (warps 8-11) and
+        // [dO ; -dY] (warps 12-15) as rows ----
         if (warp < 4) {
             float y[32], x[32];
             tmem_ld32(tl + TM_DB, x);
@@ -548,15 +547,14 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int r = 0; r < C; ++r)
                 *reinterpret_cast<float *>(base + O_BY + r * 128 + o[r & 7]) = to_tf32(sm.beta[r] * x[r]);
         } else {
-            float x[32];
-            uint32_t o[8], ob[8];
+            float x[32], y[32];
+            uint32_t o[8];
             op_offsets(64, jl, o);
-            bf16_offsets(jl, ob);
+            tmem_ld32(tl + TM_DOT, y);   // dO^T (zero past the chunk's end)
             tmem_ld32(tl + TM_DB, x);
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                *reinterpret_cast<float *>(base + O_OY + r * 128 + o[r & 7]) =
-                    to_tf32(r < L ? lds_bf16(base + T_DO + r * 128 + ob[r & 7]) : 0.f);
+                *reinterpret_cast<float *>(base + O_OY + r * 128 + o[r & 7]) = to_tf32(y[r]);
                 *reinterpret_cast<float *>(base + O_OY + (32 + r) * 128 + o[r & 7]) = to_tf32(-sm.beta[r] * x[r]);
             }
         }
@@ -565,11 +563,13 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         __syncthreads();
         tc_fence_after();
         // dP = dO U^T and dT = dU (beta Y)^T as M = 64 products (rows r on lanes 0-15
-        // and 32-47); the second reads 32 rows past dU, whose products it drops
+        // and 32-47; the second reads 32 rows past dU, whose products it drops), and
+        // [aQ^T | aK^T] / e15 = S0 [dO ; -dY]^T with S0 still in STG
         if (t == 0) {
             tc_fence_after();
             mma_ss_group(tb + TM_X, base + O_OY, 8192, base + O_U, 4096, 16, 32, false, 64);
             mma_ss_group(tb + TM_Y, base + O_DU, 4096, base + O_BY, 4096, 16, 32, false, 64);
+            mma_ss_group(tb + TM_AQK, base + STG, 16384, base + O_OY, 8192, 16, 64, false);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
@@ -588,34 +588,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             }
         }
         if (t < C) sm.dbeta[t] += sm.red[0][t] + sm.red[1][t] + sm.red[2][t] + sm.red[3][t];
-        __syncthreads();
-        // S0 (rows c, K = j) into STG again by TMA (the staging above is consumed)
-        if (S0g) {
-            if (t == 0) {
-                fence_proxy_async_smem();
-                load_s0(&sm.s0_bar);
-                if (!mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit)) {
-                    sm.abort = 1;
-                    atomicOr(&g_kda_bwdtc_status, 0x800u);
-                }
-            }
-            s0_par ^= 1u;
-        } else {
-            for (int i = t; i < 65536 / 16; i += kThreads)
-                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            fence_proxy_async_smem();
-        }
-        __syncthreads();
-
-        // ---- phase 6: [aQ^T | aK^T] / e15 = S0 [dO ; -dY]^T ----
-        if (t == 0) {
-            tc_fence_after();
-            mma_ss_group(tb + TM_AQK, base + STG, 16384, base + O_OY, 8192, 16, 64, false);
-        }
-        mma_wait();
-        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
-        // dS (rows c, K = j) into STG from dS^T in tensor memory: lane j, its
-        // quarter `slice` of the key channels
+        // ---- phase 6: dS (rows c, K = j) into STG from dS^T in tensor memory (lane
+        // j, its quarter `slice` of the key channels) ----
         {
             float x[32];
             tmem_ld32(tl + TM_DS + 32 * slice, x);
@@ -630,7 +604,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (t == 0) {
             tc_fence_after();
             mma_ss_group(tb + TM_AB, base + STG, 16384, base + O_U, 4096, 16, 32, false);
-            mma_ts_group(tb + TM_DN, tb + TM_DOT, base + OPQA, 16384, 8, 128, false);
+            mma_ts_group(tb + TM_INC, tb + TM_DOT, base + OPQA, 16384, 8, 128, false);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
@@ -656,7 +630,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 const int c0 = 64 * hh + 32 * q;
                 float x[32], y[32];
                 tmem_ld32(tl + TM_DS + c0, x);
-                tmem_ld32(tl + TM_DN + c0, y);
+                tmem_ld32(tl + TM_INC + c0, y);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = sm.gC[c0 + i] * x[i] + sm.e15[c0 + i] * y[i];
                 tmem_st32(tl + TM_DS + c0, x);
