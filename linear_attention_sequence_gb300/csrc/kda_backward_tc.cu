@@ -51,28 +51,30 @@ constexpr int C = 32;
 constexpr int D = 128;
 constexpr int kThreads = 512;
 constexpr uint32_t kPollLimit = 1u << 23;
+constexpr int kIssuers = 3;   // warps that issue MMA groups (one elected lane each)
 
 // Shared memory (byte offsets from a 1024-aligned base).
-//   TILE   TMA tiles of the chunk: q, k, v, dO (bf16, 8 KB each), g (fp32, 16 KB).
-//          After the preparation the q and k tiles hold the operands T diag(beta),
-//          T^T, P^T (4 KB each), later U, dU and beta Y (16 KB each).  Once the aB
-//          product has read U, the next chunk's tiles are loaded here.
-//   STG    64 KB staging: the Gram operands [A1 ; Q1] and B1 (rows, K = c), then
-//          S0 by TMA (rows c, K = j; read transposed into TMEM, and the A operand
-//          of [aQ | aK]), then dS (rows c), then the epilogue's per-slice sums.
-//   OPA    Kt rows (16 KB) and Kb rows (16 KB); later [dO ; -dY] (32 KB), then
-//          [dP ; dG] (8 KB) and the B operand of R3 (8 KB).
+//   TILE   TMA tiles of the chunk: q, k, dO (bf16, 8 KB each), g (fp32, 16 KB) and v
+//          (bf16, at 40 KB).  Once the preparation holds q, k, dO and g in registers,
+//          the Gram A operand [A1 ; Q1] (rows, K = c) goes over them; then T diag(beta)
+//          and T^T (4 KB each, at 32 KB); later U, dU and beta Y (16 KB each).  Once
+//          the aB product has read U, the next chunk's tiles are loaded here.
+//   STG    64 KB: S0 by TMA (rows c, K = j), loaded a chunk ahead; it is copied
+//          transposed into TMEM and is the A operand of [aQ | aK]; then dS (rows c).
+//   OPA    B1 rows and Kb rows (16 KB each); then P^T (4 KB); later [dO ; -dY]
+//          (32 KB), then [dP ; dG] (8 KB), the B operand of R3 (8 KB) and the dA
+//          scratch (4.2 KB); then the epilogue's per-slice sums.
 //   OPQA   [Q1^T | A1^T] (rows c, K = 64, 32 KB).   OPB1T  B1^T (rows c, 16 KB).
-constexpr uint32_t T_Q = 0, T_K = 8192, T_V = 16384, T_DO = 24576, T_G = 32768;
-constexpr uint32_t O_TB = 0, O_TT = 4096, O_PT = 8192;
+constexpr uint32_t T_Q = 0, T_K = 8192, T_DO = 16384, T_G = 24576, T_V = 40960;
+constexpr uint32_t O_AQ = 0;                   // [A1 ; Q1]: 4 K-blocks of 64 rows
+constexpr uint32_t O_TB = 32768, O_TT = 36864;
 // the dP / dT operands U, dU and beta Y (rows, K = j; 16 KB each) in the tile area (an
 // M = 64 product reads 32 further rows past dU: the beta Y rows, whose products it drops)
 constexpr uint32_t O_U = 0, O_DU = 16384, O_BY = 32768;
 constexpr uint32_t STG = 49152;
-// inside STG: the Gram operands [A1 ; Q1] (64 rows) and B1 (rows, K = c)
-constexpr uint32_t O_AQ = STG, O_B1 = STG + 32768;
 constexpr uint32_t OPA = STG + 65536;          // 114688
-constexpr uint32_t O_KT = OPA, O_KB = OPA + 16384, O_OY = OPA, O_PG = OPA, O_R3B = OPA + 8192;
+constexpr uint32_t O_B1 = OPA, O_KB = OPA + 16384, O_PT = OPA, O_OY = OPA, O_PG = OPA,
+                   O_R3B = OPA + 8192, O_M1 = OPA + 16384, O_PSUM = OPA;
 constexpr uint32_t OPQA = OPA + 32768;         // 147456
 constexpr uint32_t OPB1T = OPQA + 32768;       // 180224
 constexpr uint32_t SMALL = OPB1T + 16384;      // 196608
@@ -94,13 +96,13 @@ static_assert(kSmem <= 232448, "shared memory budget");
 
 // Tensor-memory columns (lanes = value j for dS^T, X, Y, U, dU, dB, dO^T, the dS0
 // increment; lanes = key channel c for aQ|aK, aB, R1|R2, R3, e^{Gamma - Gamma_15}).
-// The M = 64 products [G ; P] (in TM_DN, before S0^T) and dP, dT (in TM_X, TM_Y
-// after X and Y are read) put their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47
-// and so on.  TM_DN holds the Gram, then S0^T, then aQ|aK; the dS0 increment takes
-// 256-383 once dP, dT, U and dU are read, and R1|R2, R3 take 256-351 after it.
+// The M = 64 products [G ; P] (in TM_G, before dB) and dP, dT (in TM_X, TM_Y after
+// X and Y are read) put their rows 0-15 on lanes 0-15, 16-31 on lanes 32-47 and so
+// on.  TM_DN holds e15 S0^T, then aQ|aK; the dS0 increment takes 256-383 once dP,
+// dT, U and dU are read, and R1|R2, R3 take 256-351 after it.
 constexpr uint32_t TM_DS = 0, TM_DN = 128, TM_X = 256, TM_Y = 288, TM_U = 320, TM_DU = 352,
                    TM_DB = 384, TM_DOT = 416, TM_EX = 480;
-constexpr uint32_t TM_AQK = TM_DN, TM_INC = 256, TM_AB = 384, TM_R12 = 256, TM_R3 = 320;
+constexpr uint32_t TM_G = TM_DB, TM_AQK = TM_DN, TM_INC = 256, TM_AB = 384, TM_R12 = 256, TM_R3 = 320;
 
 __device__ __forceinline__ uint32_t off_bf16(int r, int c) {   // TMA tile (SW128), bf16
     return (uint32_t)((c >> 6) * 4096 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1));
@@ -130,14 +132,15 @@ __device__ __forceinline__ void f32_offsets(int c, uint32_t (&o)[8]) {
     for (int k8 = 0; k8 < 8; ++k8) o[k8] = (uint32_t)((c >> 5) * 4096 + ((((c & 31) >> 2) ^ k8) << 4) + ((c & 3) << 2));
 }
 
-// One MMA group: D[m][n] (+)= sum_k A[m][k] B[n][k], A and B K-major SW128 in
-// shared memory (SS) with K-blocks of `akb` and `bkb` bytes; `ksteps` steps of 8.
+// One MMA group, called by a whole warp (one elected lane issues): D[m][n] (+)=
+// sum_k A[m][k] B[n][k], A and B K-major SW128 in shared memory (SS) with K-blocks
+// of `akb` and `bkb` bytes; `ksteps` steps of 8.
 __device__ __forceinline__ void mma_ss_group(uint32_t d, const unsigned char *a, uint32_t akb,
                                              const unsigned char *b, uint32_t bkb, int ksteps, int n,
                                              bool acc, int m = 128) {
     const uint64_t da = sdesc_sw128(smem_u32(a)), db = sdesc_sw128(smem_u32(b));
     for (int kk = 0; kk < ksteps; ++kk)
-        mma_tf32_ss(d, da + (uint64_t)(((kk >> 2) * akb + (kk & 3) * 32) >> 4),
+        mma_tf32_ss_el(d, da + (uint64_t)(((kk >> 2) * akb + (kk & 3) * 32) >> 4),
                     db + (uint64_t)(((kk >> 2) * bkb + (kk & 3) * 32) >> 4), idesc_tf32(m, n),
                     (acc || kk > 0) ? 1u : 0u);
 }
@@ -146,7 +149,7 @@ __device__ __forceinline__ void mma_ts_group(uint32_t d, uint32_t a, const unsig
                                              uint32_t bkb, int ksteps, int n, bool acc) {
     const uint64_t db = sdesc_sw128(smem_u32(b));
     for (int kk = 0; kk < ksteps; ++kk)
-        mma_tf32_ts(d, a + 8 * kk, db + (uint64_t)(((kk >> 2) * bkb + (kk & 3) * 32) >> 4),
+        mma_tf32_ts_el(d, a + 8 * kk, db + (uint64_t)(((kk >> 2) * bkb + (kk & 3) * 32) >> 4),
                     idesc_tf32(128, n), (acc || kk > 0) ? 1u : 0u);
 }
 
@@ -183,7 +186,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     if (t == 0) {
         mbar_init(&sm.tma_bar, 1);
         mbar_init(&sm.s0_bar, 1);
-        mbar_init(&sm.mma_bar, 1);
+        mbar_init(&sm.mma_bar, kIssuers);
         fence_mbar_init();
         sm.abort = 0;
         prefetch_tmap(&tm_q);
@@ -218,6 +221,28 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     };
     bool tiles_pending = false;
     uint32_t pend_par = 0;
+    // The start state S0 of chunk cx (rows c, K = j) into STG, also a chunk ahead: four
+    // 128-row boxes of 32 columns by TMA from the initial state (chunk 0) or the
+    // checkpoint row, or zeros where there is none.  Called by every thread.
+    auto s0_present = [&](int cx) -> bool {
+        return cx == 0 ? init_state != nullptr : (chunk_states != nullptr && ck0 + cx - 1 < chunk_capacity);
+    };
+    bool s0_pending = false;   // thread 0: a state load that no chunk has awaited yet
+    auto fetch_s0 = [&](int cx) {
+        if (s0_present(cx)) {
+            if (t == 0) {
+                const CUtensorMap *map = cx == 0 ? &tm_init : &tm_cs;
+                const int row = (int)((cx == 0 ? (int64_t)n * H + h : (ck0 + cx - 1) * H + h) * D);
+                mbar_arrive_expect_tx(&sm.s0_bar, 65536);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) tma_load_2d(base + STG + kb * 16384, map, &sm.s0_bar, 32 * kb, row);
+                s0_pending = true;
+            }
+        } else {
+            for (int i = t; i < 65536 / 16; i += kThreads)
+                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
     float bnext = 0.f;   // beta of the next chunk (threads 0..C-1)
     if (nchunks > 0) {   // the last chunk comes first
         const int64_t tx = a + (int64_t)(nchunks - 1) * C;
@@ -225,17 +250,17 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             load_tiles(tx);
             tiles_pending = true;
         }
+        fetch_s0(nchunks - 1);
         if (t < C && tx + t < b) bnext = beta[(tx + t) * H + h];
     }
 
-    // MMA groups are issued and awaited by thread 0; the barrier releases the rest.
+    // An MMA group is split over warps 0 .. kIssuers-1 (products for different
+    // accumulators issue in parallel), each ending its share with a commit to mma_bar
+    // (kIssuers arrivals a phase); thread 0 waits, the barrier releases the rest.
     auto mma_wait = [&]() {
-        if (t == 0) {
-            mma_commit(&sm.mma_bar);
-            if (!mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit)) {
-                sm.abort = 1;
-                atomicOr(&g_kda_bwdtc_status, 0x400u);
-            }
+        if (t == 0 && !mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit)) {
+            sm.abort = 1;
+            atomicOr(&g_kda_bwdtc_status, 0x400u);
         }
         mma_par ^= 1u;
         tc_fence_before();
@@ -267,15 +292,6 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                            : (chunk_states && crow < chunk_capacity) ? chunk_states + (crow * H + h) * sdd
                                                                      : nullptr;
         if (ch > 0 && S0g == nullptr && t == 0) atomicOr(&g_kda_bwdtc_status, kda::kBwdMissingState);
-        // the state by TMA: four 128-row boxes of 32 columns = S0 as a K-major SW128
-        // operand (rows = key channel c, K = value j) in STG
-        const CUtensorMap *s0map = ch == 0 ? &tm_init : &tm_cs;
-        const int s0row = (int)((ch == 0 ? (int64_t)n * H + h : crow * H + h) * D);
-        auto load_s0 = [&](uint64_t *bar) {
-            mbar_arrive_expect_tx(bar, 65536);
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb) tma_load_2d(base + STG + kb * 16384, s0map, bar, 32 * kb, s0row);
-        };
 
         // ---- phase 0: the chunk's tiles (issued a chunk ahead) have landed; beta ----
         if (t < C) {
@@ -320,6 +336,14 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 dov[u] = __float_as_uint(r < L ? lds_bf16(base + T_DO + r * 128 + ob[u]) : 0.f);
             }
             tmem_st8(tl + TM_DOT + r0, dov);
+            float qv[8], kv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = r0 + u;
+                qv[u] = r < L ? lds_bf16(base + T_Q + r * 128 + ob[u]) : 0.f;
+                kv[u] = r < L ? lds_bf16(base + T_K + r * 128 + ob[u]) : 0.f;
+            }
+            // every q, k, dO and g value is in registers: [A1 ; Q1] may go over the tiles
             __syncthreads();
             const float p0 = sm.red2[0][c], p1 = sm.red2[1][c], p2 = sm.red2[2][c], p3 = sm.red2[3][c];
             const float g15 = p0 + p1, gl = g15 + p2 + p3;
@@ -336,20 +360,15 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int r = r0 + u;
-                float qv = 0.f, kv = 0.f;
-                if (r < L) {
-                    qv = lds_bf16(base + T_Q + r * 128 + ob[u]);
-                    kv = lds_bf16(base + T_K + r * 128 + ob[u]);
-                }
                 const float x = base_x + gam[u];             // in [-80, 80] by the log-decay bound
                 const float e1 = __expf(x), inv = __expf(-x);
-                const float ka = kv * e1, kbv = kv * inv;
+                const float ka = kv[u] * e1, kbv = kv[u] * inv;
                 exv[u] = __float_as_uint(e1);
-                q1[u] = to_tf32(qv * e1);
+                q1[u] = to_tf32(qv[u] * e1);
                 a1[u] = to_tf32(ka);
                 b1[u] = to_tf32(kbv);
-                // Kt = k e^{Gamma} and Kb = k e^{Gamma_C - Gamma} as rows (K = c)
-                *reinterpret_cast<float *>(base + O_KT + r * 128 + ok[u]) = to_tf32(ka * e15);
+                // Kb = k e^{Gamma_C - Gamma} as rows (K = c); Kt = k e^{Gamma} = A1 e15
+                // enters as A1 with e15 folded into S0^T
                 *reinterpret_cast<float *>(base + O_KB + r * 128 + ok[u]) = to_tf32(kbv * fC);
                 // the Gram operands: [A1 ; Q1] and B1 as rows (K = c)
                 *reinterpret_cast<float *>(base + O_AQ + r * 128 + og[u]) = a1[u];
@@ -375,26 +394,28 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         tc_fence_after();
 
         // ---- phase 2: [G ; P] = [A1 ; Q1] B1^T (M = 64: rows r of G on lanes 0-15 and
-        // 32-47, of P on lanes 64-79 and 96-111); then the state by TMA into STG ----
-        if (t == 0) {
+        // 32-47, of P on lanes 64-79 and 96-111) on warp 0, dU^T = dS^T Kb^T on warp 1.
+        // Meanwhile warps 4-11 copy e15 S0^T into tensor memory (lane j, columns c of
+        // this warp's half) once the state has landed, with the partial sums
+        // gsum[c] = sum_j dS[c][j] S0[c][j].  Warps 0-3 then read G and P, hand G to
+        // the solve (warp 12) and store P^T as an operand; thread 0 issues X =
+        // (e15 S0^T) A1^T and dU^T += dO^T P, and warps 0-3 form Y^T = V^T - X. ----
+        if (warp < kIssuers) {
             tc_fence_after();
-            mma_ss_group(tb + TM_DN, base + O_AQ, 8192, base + O_B1, 4096, 16, 32, false, 64);
-        }
-        mma_wait();
-        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
-        if (S0g) {
-            if (t == 0) {   // STG's Gram operands are consumed: the state goes there
-                fence_proxy_async_smem();
-                load_s0(&sm.s0_bar);
-            }
-        } else {
-            for (int i = t; i < 65536 / 16; i += kThreads)
-                reinterpret_cast<float4 *>(base + STG)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (warp == 0) mma_ss_group(tb + TM_G, base + O_AQ, 8192, base + O_B1, 4096, 16, 32, false, 64);
+            mma_commit_el(&sm.mma_bar);   // this phase of mma_bar waits for the Gram alone
+            if (warp == 1) mma_ts_group(tb + TM_DU, tb + TM_DS, base + O_KB, 4096, 16, 32, false);
         }
         if (warp < 4) {
+            if (t == 0 && !mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit)) {
+                sm.abort = 1;
+                atomicOr(&g_kda_bwdtc_status, 0x400u);
+            }
+            named_sync(3, 128);
+            tc_fence_after();
             // the collective load runs on every lane of the warp; lanes 0-15 hold rows
             float x[32];
-            tmem_ld32(tl + TM_DN, x);
+            tmem_ld32(tl + TM_G, x);
             if (lane < 16) {
                 const int row = 16 * warp + lane;   // 0..63: G rows 0-31, then P rows 0-31
                 const int r = row & 31;
@@ -404,18 +425,14 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     else sm.P[r][i] = i <= r ? x[i] : 0.f;
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (warp == 0) {   // blocked solve (scratch in the small arrays)
-            float d[32];
-#pragma unroll
-            for (int i = 0; i < C; ++i) d[i] = sm.G[lane][i];
-            solve_t(d, sm.beta[lane], lane, &sm.T[0][0], LDS32, sm.akkT, sm.tsc);
-        } else if (warp >= 4 && warp < 12) {
-            // once the state has landed: S0^T into tensor memory (lane j, columns c of
-            // this warp's half) for the X product, and gsum[c] = sum_j dS[c][j] S0[c][j]
+            named_arrive(4, 160);   // G is ready for the solve
+            named_sync(3, 128);
+            for (int idx = t; idx < C * C; idx += 128) {
+                const int r = idx >> 5, i = idx & 31;
+                st_op(base + O_PT, 32, r, i, sm.P[i][r]);
+            }
+            fence_proxy_async_smem();
+        } else if (warp < 12) {
             bool ok = true;
             if (S0g && lane == 0) ok = mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -430,11 +447,15 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 const int c0 = 64 * half + 32 * h2;
                 float x[32], d[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = *reinterpret_cast<const float *>(base + STG + sw_off(128, c0 + i, jl));
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = *reinterpret_cast<const float *>(base + STG + sw_off(128, c0 + i, jl));
+                    p[32 * h2 + i] = x[i];
+                    x[i] *= sm.e15[c0 + i];
+                }
                 tmem_st32(tl + TM_DN + c0, x);
                 tmem_ld32(tl + TM_DS + c0, d);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) p[32 * h2 + i] = x[i] * d[i];
+                for (int i = 0; i < 32; ++i) p[32 * h2 + i] *= d[i];
             }
             tmem_wait_st();
 #pragma unroll
@@ -452,48 +473,61 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 }
                 sm.red2[q4][64 * half + 32 * h2 + lane] = y[0];
             }
+        } else if (warp == 12) {   // blocked solve (scratch in the small arrays)
+            named_sync(4, 160);
+            float d[32];
+#pragma unroll
+            for (int i = 0; i < C; ++i) d[i] = sm.G[lane][i];
+            solve_t(d, sm.beta[lane], lane, &sm.T[0][0], LDS32, sm.akkT, sm.tsc);
         }
+        mma_par ^= 1u;
+        if (warp < 12) {
+            tc_fence_before();
+            named_sync(2, 384);
+            if (warp < kIssuers) {
+                tc_fence_after();
+                if (warp == 0) mma_ts_group(tb + TM_X, tb + TM_DN, base + O_AQ, 8192, 16, 32, false);
+                else if (warp == 1) mma_ts_group(tb + TM_DU, tb + TM_DOT, base + O_PT, 4096, 4, 32, true);
+                mma_commit_el(&sm.mma_bar);
+            }
+            if (t == 0 && !mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit)) {
+                sm.abort = 1;
+                atomicOr(&g_kda_bwdtc_status, 0x400u);
+            }
+            if (warp < 4) {   // Y^T = V^T - X into tensor memory
+                named_sync(3, 128);
+                tc_fence_after();
+                float x[32];
+                tmem_ld32(tl + TM_X, x);
+#pragma unroll
+                for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_V + off_bf16(r, jl)) - x[r] : 0.f;
+                tmem_st32(tl + TM_Y, x);
+                tmem_wait_st();
+            }
+        }
+        mma_par ^= 1u;
         if (S0g) s0_par ^= 1u;
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (t == 0 && S0g) s0_pending = false;
+        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
         if (t < D) sm.gsum[t] = sm.red2[0][t] + sm.red2[1][t] + sm.red2[2][t] + sm.red2[3][t];
-        // T diag(beta), T^T and P^T as 32-row operands (in the q tile)
+        // T diag(beta) and T^T as 32-row operands
         for (int idx = t; idx < C * C; idx += kThreads) {
             const int r = idx >> 5, i = idx & 31;
             st_op(base + O_TB, 32, r, i, sm.T[r][i] * sm.beta[i]);
             st_op(base + O_TT, 32, r, i, sm.T[i][r]);
-            st_op(base + O_PT, 32, r, i, sm.P[i][r]);
         }
         fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- phase 3: X = S0^T Kt^T (Y = V - X), dU^T = dS^T Kb^T + dO^T P ----
-        if (t == 0) {
+        // ---- phases 3-4: U^T = Y^T (T diag beta)^T, dB^T = dU^T T ----
+        if (warp < kIssuers) {
             tc_fence_after();
-            mma_ts_group(tb + TM_X, tb + TM_DN, base + O_KT, 4096, 16, 32, false);
-            mma_ts_group(tb + TM_DU, tb + TM_DS, base + O_KB, 4096, 16, 32, false);
-            mma_ts_group(tb + TM_DU, tb + TM_DOT, base + O_PT, 4096, 4, 32, true);
-        }
-        mma_wait();
-        if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
-
-        // ---- phase 4: Y^T = V^T - X into tensor memory; U^T = Y^T (T diag beta)^T,
-        // dB^T = dU^T T ----
-        if (warp < 4) {
-            float x[32];
-            tmem_ld32(tl + TM_X, x);
-#pragma unroll
-            for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_V + off_bf16(r, jl)) - x[r] : 0.f;
-            tmem_st32(tl + TM_Y, x);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (t == 0) {
-            tc_fence_after();
-            mma_ts_group(tb + TM_U, tb + TM_Y, base + O_TB, 4096, 4, 32, false);
-            mma_ts_group(tb + TM_DB, tb + TM_DU, base + O_TT, 4096, 4, 32, false);
+            if (warp == 0) mma_ts_group(tb + TM_U, tb + TM_Y, base + O_TB, 4096, 4, 32, false);
+            else if (warp == 1) mma_ts_group(tb + TM_DB, tb + TM_DU, base + O_TT, 4096, 4, 32, false);
+            mma_commit_el(&sm.mma_bar);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
@@ -565,11 +599,12 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // dP = dO U^T and dT = dU (beta Y)^T as M = 64 products (rows r on lanes 0-15
         // and 32-47; the second reads 32 rows past dU, whose products it drops), and
         // [aQ^T | aK^T] / e15 = S0 [dO ; -dY]^T with S0 still in STG
-        if (t == 0) {
+        if (warp < kIssuers) {
             tc_fence_after();
-            mma_ss_group(tb + TM_X, base + O_OY, 8192, base + O_U, 4096, 16, 32, false, 64);
-            mma_ss_group(tb + TM_Y, base + O_DU, 4096, base + O_BY, 4096, 16, 32, false, 64);
-            mma_ss_group(tb + TM_AQK, base + STG, 16384, base + O_OY, 8192, 16, 64, false);
+            if (warp == 0) mma_ss_group(tb + TM_X, base + O_OY, 8192, base + O_U, 4096, 16, 32, false, 64);
+            else if (warp == 1) mma_ss_group(tb + TM_Y, base + O_DU, 4096, base + O_BY, 4096, 16, 32, false, 64);
+            else mma_ss_group(tb + TM_AQK, base + STG, 16384, base + O_OY, 8192, 16, 64, false);
+            mma_commit_el(&sm.mma_bar);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
@@ -601,22 +636,25 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         __syncthreads();
         tc_fence_after();
         // aB^T = dS U^T; the dS_0 increment (Q1^T dO - A1^T dY)^T = [dO^T | -dY^T] [Q1^T | A1^T]^T
-        if (t == 0) {
+        if (warp < kIssuers) {
             tc_fence_after();
-            mma_ss_group(tb + TM_AB, base + STG, 16384, base + O_U, 4096, 16, 32, false);
-            mma_ts_group(tb + TM_INC, tb + TM_DOT, base + OPQA, 16384, 8, 128, false);
+            if (warp == 0) mma_ss_group(tb + TM_AB, base + STG, 16384, base + O_U, 4096, 16, 32, false);
+            else if (warp == 1) mma_ts_group(tb + TM_INC, tb + TM_DOT, base + OPQA, 16384, 8, 128, false);
+            mma_commit_el(&sm.mma_bar);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // The tile area's last reader (the aB product) is complete: the next chunk's
-        // tiles and beta are fetched during the rest of this one.
+        // The tile area's last reader (the aB product) and STG's (the same product) are
+        // complete: the next chunk's tiles, state and beta are fetched during the rest
+        // of this one.
         if (ch > 0) {
             if (t == 0) {
                 load_tiles(t0 - C);
                 tiles_pending = true;
                 pend_par = tma_par;
             }
+            fetch_s0(ch - 1);
             if (t < C) bnext = beta[(t0 - C + t) * H + h];   // chunk ch - 1 is a whole chunk
         }
 
@@ -642,7 +680,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             // dA = -T^T M1; thread = rows r0, r0+1 x columns i0, i0+1
             const int tp = t - 256;
             const int r0 = (tp >> 4) * 2, i0 = (tp & 15) * 2;
-            float(*M1)[LDS32] = reinterpret_cast<float(*)[LDS32]>(base + STG);   // STG is free again
+            float(*M1)[LDS32] = reinterpret_cast<float(*)[LDS32]>(base + O_M1);
             float m00 = 0.f, m01 = 0.f, m10 = 0.f, m11 = 0.f;
 #pragma unroll 8
             for (int bb = 0; bb < C; ++bb) {
@@ -707,10 +745,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (t == 0) {
+        if (warp < kIssuers) {
             tc_fence_after();
-            mma_ss_group(tb + TM_R12, base + OPB1T, 16384, base + O_PG, 8192, 4, 64, false);
-            mma_ss_group(tb + TM_R3, base + OPQA, 16384, base + O_R3B, 4096, 8, 32, false);
+            if (warp == 0) mma_ss_group(tb + TM_R12, base + OPB1T, 16384, base + O_PG, 8192, 4, 64, false);
+            else if (warp == 1) mma_ss_group(tb + TM_R3, base + OPQA, 16384, base + O_R3B, 4096, 8, 32, false);
+            mma_commit_el(&sm.mma_bar);
         }
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
@@ -758,8 +797,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             }
 #pragma unroll
             for (int u = 6; u >= 0; --u) dgam[u] += dgam[u + 1];
-            float *part_sum = reinterpret_cast<float *>(base + STG);          // [4][D]
-            float *part_kbk = reinterpret_cast<float *>(base + STG) + 4 * D;  // [4][D]
+            float *part_sum = reinterpret_cast<float *>(base + O_PSUM);          // [4][D]
+            float *part_kbk = reinterpret_cast<float *>(base + O_PSUM) + 4 * D;  // [4][D]
             part_sum[slice * D + c] = dgam[0];
             part_kbk[slice * D + c] = kbk;
             __syncthreads();
@@ -788,11 +827,15 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int i = 0; i < 32; ++i) d_init[soff + (int64_t)(c0 + i) * D + jl] = x[i];
         }
     }
-    if (t == 0) {   // every MMA and tile copy issued has completed (after a stop too)
+    // every MMA and tile copy issued has completed (after a stop too)
+    if (warp < kIssuers) {
         tc_fence_after();
-        mma_commit(&sm.mma_bar);
+        mma_commit_el(&sm.mma_bar);
+    }
+    if (t == 0) {
         mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit);
         if (tiles_pending) mbar_wait_bounded(&sm.tma_bar, pend_par, kPollLimit);
+        if (s0_pending) mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit);
     }
     tc_fence_before();
     __syncthreads();
