@@ -394,7 +394,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         tc_fence_after();
 
         // ---- phase 2: [G ; P] = [A1 ; Q1] B1^T (M = 64: rows r of G on lanes 0-15 and
-        // 32-47, of P on lanes 64-79 and 96-111) on warp 0, dU^T = dS^T Kb^T on warp 1.
+        // 32-47, of P on lanes 64-79 and 96-111), its K halves on warps 0 and 2 (into
+        // TM_G and TM_X, summed when read), dU^T = dS^T Kb^T on warp 1.
         // Meanwhile warps 4-11 copy e15 S0^T into tensor memory (lane j, columns c of
         // this warp's half) once the state has landed, with the partial sums
         // gsum[c] = sum_j dS[c][j] S0[c][j].  Warps 0-3 then read G and P, hand G to
@@ -402,7 +403,9 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // (e15 S0^T) A1^T and dU^T += dO^T P, and warps 0-3 form Y^T = V^T - X. ----
         if (warp < kIssuers) {
             tc_fence_after();
-            if (warp == 0) mma_ss_group(tb + TM_G, base + O_AQ, 8192, base + O_B1, 4096, 16, 32, false, 64);
+            if (warp == 0) mma_ss_group(tb + TM_G, base + O_AQ, 8192, base + O_B1, 4096, 8, 32, false, 64);
+            else if (warp == 2)
+                mma_ss_group(tb + TM_X, base + O_AQ + 2 * 8192, 8192, base + O_B1 + 2 * 4096, 4096, 8, 32, false, 64);
             mma_commit_el(&sm.mma_bar);   // this phase of mma_bar waits for the Gram alone
             if (warp == 1) mma_ts_group(tb + TM_DU, tb + TM_DS, base + O_KB, 4096, 16, 32, false);
         }
@@ -414,8 +417,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             named_sync(3, 128);
             tc_fence_after();
             // the collective load runs on every lane of the warp; lanes 0-15 hold rows
-            float x[32];
+            float x[32], x2[32];
             tmem_ld32(tl + TM_G, x);
+            tmem_ld32(tl + TM_X, x2);
+#pragma unroll
+            for (int i = 0; i < C; ++i) x[i] += x2[i];
             if (lane < 16) {
                 const int row = 16 * warp + lane;   // 0..63: G rows 0-31, then P rows 0-31
                 const int r = row & 31;
@@ -486,8 +492,10 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             named_sync(2, 384);
             if (warp < kIssuers) {
                 tc_fence_after();
-                if (warp == 0) mma_ts_group(tb + TM_X, tb + TM_DN, base + O_AQ, 8192, 16, 32, false);
+                // X in two K halves (warps 0 and 2, into TM_X and TM_Y, summed when read)
+                if (warp == 0) mma_ts_group(tb + TM_X, tb + TM_DN, base + O_AQ, 8192, 8, 32, false);
                 else if (warp == 1) mma_ts_group(tb + TM_DU, tb + TM_DOT, base + O_PT, 4096, 4, 32, true);
+                else mma_ts_group(tb + TM_Y, tb + TM_DN + 64, base + O_AQ + 2 * 8192, 8192, 8, 32, false);
                 mma_commit_el(&sm.mma_bar);
             }
             if (t == 0 && !mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit)) {
@@ -497,10 +505,11 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             if (warp < 4) {   // Y^T = V^T - X into tensor memory
                 named_sync(3, 128);
                 tc_fence_after();
-                float x[32];
+                float x[32], x2[32];
                 tmem_ld32(tl + TM_X, x);
+                tmem_ld32(tl + TM_Y, x2);
 #pragma unroll
-                for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_V + off_bf16(r, jl)) - x[r] : 0.f;
+                for (int r = 0; r < C; ++r) x[r] = r < L ? lds_bf16(base + T_V + off_bf16(r, jl)) - (x[r] + x2[r]) : 0.f;
                 tmem_st32(tl + TM_Y, x);
                 tmem_wait_st();
             }
@@ -532,8 +541,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         mma_wait();
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
 
-        // ---- phase 5 (lane j): dV = dY = diag(beta) dB and the dB . Y row sums
-        // (warps 0-3); the operands U (warps 4-7), dU and beta Y (warps 8-11) and
+        // ---- phase 5 (lane j): -dY^T = -diag(beta) dB^T into tensor memory and the
+        // dB . Y row sums (warps 0-3); the operands U (warps 4-7), dU and beta Y (warps 8-11) and
         // [dO ; -dY] (warps 12-15) as rows ----
         if (warp < 4) {
             float y[32], x[32];
@@ -542,7 +551,6 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 #pragma unroll
             for (int r = 0; r < C; ++r) {
                 const float dy = sm.beta[r] * x[r];
-                if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + jl, dy);
                 x[r] *= y[r];          // dB . Y
                 y[r] = -dy;
             }
@@ -658,9 +666,10 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             if (t < C) bnext = beta[(t0 - C + t) * H + h];   // chunk ch - 1 is a whole chunk
         }
 
-        // ---- phase 7: dS^T <- dS^T Diag(gamma_C) + (increment)^T Diag(e15) on warps
-        // 0-7 (lane j, half of the channels each), while warps 8-15 form dA, dG and
-        // the dA . G row sums ----
+        // ---- phase 7: dS^T <- dS^T Diag(gamma_C) + (increment)^T Diag(e15) and the
+        // stores of dV = dY (from -dY^T, still in TM_DOT) on warps 0-7 (lane j, half of
+        // the channels and of the tokens each), while warps 8-15 form dA, dG and the
+        // dA . G row sums ----
         if (warp < 8) {
             const int hh = warp >> 2;
 #pragma unroll 1
@@ -672,6 +681,13 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = sm.gC[c0 + i] * x[i] + sm.e15[c0 + i] * y[i];
                 tmem_st32(tl + TM_DS + c0, x);
+            }
+            float y[16];
+            tmem_ld16(tl + TM_DOT + 32 + 16 * hh, y);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int r = 16 * hh + u;
+                if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + jl, -y[u]);
             }
             tmem_wait_st();
         } else {
