@@ -106,7 +106,7 @@ def barrier(world: int):
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms in the background; samples are tagged
+    """nvidia-smi sampled every 20 ms in the background; samples are tagged
     with wall time so that those inside the timed region can be picked."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -123,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -154,7 +154,7 @@ class ClockSampler:
         note = None
         if not inside:  # region shorter than the sampling period: take the nearest
             near = min(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
-            inside, note = [near[1]], "nearest sample (timed region shorter than 50 ms)"
+            inside, note = [near[1]], "nearest sample (timed region shorter than the sampling period)"
 
         def num(x):
             try:
@@ -359,6 +359,16 @@ def run_gpu(args):
     sampler = ClockSampler(local).start() if rank == 0 else None
     ms, t0, t1 = time_steps(prefill_step, args.steps, args.warmup, world, stream)
     clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler and clocks.get("samples", 0) < 5:
+        # A short timed region holds few samples: the same step, untimed, for about
+        # 0.25 s right after it shows the clocks under that load as well.
+        tl0 = time.time()
+        while time.time() - tl0 < 0.25:
+            for _ in range(20):
+                prefill_step()
+            stream.synchronize()
+        clocks["same_load_after"] = {k: v for k, v in sampler.summary(tl0, time.time()).items()
+                                     if k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
     check_device_status(kda, stream, "prefill_8k")
     value = T * world / (ms * 1e-3)
     achieved = PREFILL_BYTES_PER_TOKEN * T / (ms * 1e-3) / 1e9
