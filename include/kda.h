@@ -385,7 +385,10 @@ kda_status kda_prefill_scalar_decay(const kda_dims *dims, const void *q, const v
  *   d_init_state   device fp32 [N, H, d_k, d_v] or NULL (not written).
  *
  * No gradient may share a byte with an input or with another gradient.
- * Arithmetic is fp32 on CUDA cores.
+ * Arithmetic: with bf16 inputs at d_k = d_v = 128 (16-byte aligned q, k, v, g
+ * and d_out) the products run on the tensor cores with tf32 operands and fp32
+ * accumulation; otherwise (fp32 inputs, d = 64) everything is fp32 on the CUDA
+ * cores.
  * Every other argument (q, k, v, g, beta, init_state, cu_seqlens, dims) and
  * every other error is as in kda_prefill; KDA_ERR_INVALID_ARGUMENT also if
  * chunk_capacity < 0, chunk_states is NULL or misaligned where it is needed,
