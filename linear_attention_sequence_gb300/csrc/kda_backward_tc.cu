@@ -52,6 +52,7 @@ constexpr int D = 128;
 constexpr int kThreads = 512;
 constexpr uint32_t kPollLimit = 1u << 23;
 constexpr int kIssuers = 3;   // warps that issue MMA groups (one elected lane each)
+constexpr int kS0Issuer = 32; // issues the state loads (the tiles come from thread 0)
 
 // Shared memory (byte offsets from a 1024-aligned base).
 //   TILE   TMA tiles of the chunk: q, k, dO (bf16, 8 KB each), g (fp32, 16 KB) and v
@@ -62,8 +63,8 @@ constexpr int kIssuers = 3;   // warps that issue MMA groups (one elected lane e
 //   STG    64 KB: S0 by TMA (rows c, K = j), loaded a chunk ahead; it is copied
 //          transposed into TMEM and is the A operand of [aQ | aK]; then dS (rows c).
 //   OPA    B1 rows and Kb rows (16 KB each); then P^T (4 KB); later [dO ; -dY]
-//          (32 KB), then [dP ; dG] (8 KB), the B operand of R3 (8 KB) and the dA
-//          scratch (4.2 KB); then the epilogue's per-slice sums.
+//          (32 KB), then [dP ; dG] (8 KB), the B operand of R3 (8 KB), the dA
+//          scratch (4.2 KB) and the dv rows; then the dq, dk and dg rows.
 //   OPQA   [Q1^T | A1^T] (rows c, K = 64, 32 KB).   OPB1T  B1^T (rows c, 16 KB).
 constexpr uint32_t T_Q = 0, T_K = 8192, T_DO = 16384, T_G = 24576, T_V = 40960;
 constexpr uint32_t O_AQ = 0;                   // [A1 ; Q1]: 4 K-blocks of 64 rows
@@ -74,7 +75,10 @@ constexpr uint32_t O_U = 0, O_DU = 16384, O_BY = 32768;
 constexpr uint32_t STG = 49152;
 constexpr uint32_t OPA = STG + 65536;          // 114688
 constexpr uint32_t O_B1 = OPA, O_KB = OPA + 16384, O_PT = OPA, O_OY = OPA, O_PG = OPA,
-                   O_R3B = OPA + 8192, O_M1 = OPA + 16384, O_PSUM = OPA;
+                   O_R3B = OPA + 8192, O_M1 = OPA + 16384;
+// bf16 gradient rows staged for 16-byte stores: dv [32][128] (phase 7, beside the dA
+// scratch), then dq, dk [32][128] and dg [32][128] fp32 (the epilogue)
+constexpr uint32_t O_SV = OPA + 24576, O_SQ = OPA, O_SK = OPA + 8192, O_SG = OPA + 16384;
 constexpr uint32_t OPQA = OPA + 32768;         // 147456
 constexpr uint32_t OPB1T = OPQA + 32768;       // 180224
 constexpr uint32_t SMALL = OPB1T + 16384;      // 196608
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_cs,
-                       const __grid_constant__ CUtensorMap tm_init, int has_cs, int has_init,
+                       const __grid_constant__ CUtensorMap tm_init, int has_cs, int has_init, int vec_out,
                        const float *__restrict__ beta,
                        const float *init_state, const int32_t *__restrict__ cu,
                        const float *__restrict__ chunk_states, int64_t chunk_capacity,
@@ -166,6 +170,9 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                        OUT_T *__restrict__ dk, OUT_T *__restrict__ dv, float *__restrict__ dg,
                        float *__restrict__ dbeta, float *d_init, int H, int64_t total,
                        int64_t seq_len) {
+    // bf16 gradients with 16-byte aligned rows go out through shared memory as
+    // 16-byte stores (a thread holds one channel of many tokens)
+    const bool vstore = sizeof(OUT_T) == 2 && vec_out;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Small &sm = *reinterpret_cast<Small *>(base + SMALL);
@@ -227,10 +234,10 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     auto s0_present = [&](int cx) -> bool {
         return cx == 0 ? init_state != nullptr : (chunk_states != nullptr && ck0 + cx - 1 < chunk_capacity);
     };
-    bool s0_pending = false;   // thread 0: a state load that no chunk has awaited yet
+    bool s0_pending = false;   // thread kS0Issuer: a state load that no chunk has awaited yet
     auto fetch_s0 = [&](int cx) {
         if (s0_present(cx)) {
-            if (t == 0) {
+            if (t == kS0Issuer) {
                 const CUtensorMap *map = cx == 0 ? &tm_init : &tm_cs;
                 const int row = (int)((cx == 0 ? (int64_t)n * H + h : (ck0 + cx - 1) * H + h) * D);
                 mbar_arrive_expect_tx(&sm.s0_bar, 65536);
@@ -519,7 +526,7 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (t == 0 && S0g) s0_pending = false;
+        if (t == kS0Issuer && S0g) s0_pending = false;
         if (*reinterpret_cast<volatile int *>(&sm.abort)) break;
         if (t < D) sm.gsum[t] = sm.red2[0][t] + sm.red2[1][t] + sm.red2[2][t] + sm.red2[3][t];
         // T diag(beta) and T^T as 32-row operands
@@ -684,10 +691,24 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             }
             float y[16];
             tmem_ld16(tl + TM_DOT + 32 + 16 * hh, y);
+            if (vstore) {
+                __nv_bfloat16 *sv = reinterpret_cast<__nv_bfloat16 *>(base + O_SV);   // [C][D]
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int r = 16 * hh + u;
-                if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + jl, -y[u]);
+                for (int u = 0; u < 16; ++u) sv[(16 * hh + u) * D + jl] = __float2bfloat16_rn(-y[u]);
+                named_sync(5, 256);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {   // 512 chunks of 8 channels
+                    const int q = t + 256 * i, r = q >> 4, c8 = (q & 15) * 8;
+                    if (r < L)
+                        *reinterpret_cast<uint4 *>(dv + (t0 + r) * rowK + (int64_t)h * D + c8) =
+                            *reinterpret_cast<const uint4 *>(sv + r * D + c8);
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * hh + u;
+                    if (r < L) kda::st_elem(dv + (t0 + r) * rowK + (int64_t)h * D + jl, -y[u]);
+                }
             }
             tmem_wait_st();
         } else {
@@ -802,19 +823,24 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 const float ix = __fdividef(1.f, ex[u]);       // e^{Gamma_15 - Gamma_x}
                 const float sq = e15 * aq[u] + r1[u], sk = e15 * ak[u] + r2[u];
                 const float fb = fC * ab[u];
-                if (x < L) {
+                const float dqv = ex[u] * sq;
+                // e^{Gamma_C - Gamma_x} aB + e^{Gamma_15 - Gamma_x} R3 = e^{Gamma_15 - Gamma_x} (fC aB + R3)
+                const float dkv = ex[u] * sk + ix * (fb + r3[u]);
+                if (vstore) {
+                    reinterpret_cast<__nv_bfloat16 *>(base + O_SQ)[x * D + c] = __float2bfloat16_rn(dqv);
+                    reinterpret_cast<__nv_bfloat16 *>(base + O_SK)[x * D + c] = __float2bfloat16_rn(dkv);
+                } else if (x < L) {
                     const int64_t off = (t0 + x) * rowK + (int64_t)h * D + c;
-                    kda::st_elem(dq + off, ex[u] * sq);
-                    // e^{Gamma_C - Gamma_x} aB + e^{Gamma_15 - Gamma_x} R3 = e^{Gamma_15 - Gamma_x} (fC aB + R3)
-                    kda::st_elem(dk + off, ex[u] * sk + ix * (fb + r3[u]));
+                    kda::st_elem(dq + off, dqv);
+                    kda::st_elem(dk + off, dkv);
                 }
                 dgam[u] = q1[u] * sq + a1[u] * sk - b1[u] * (fb + r3[u]);
                 kbk += fb * b1[u];
             }
 #pragma unroll
             for (int u = 6; u >= 0; --u) dgam[u] += dgam[u + 1];
-            float *part_sum = reinterpret_cast<float *>(base + O_PSUM);          // [4][D]
-            float *part_kbk = reinterpret_cast<float *>(base + O_PSUM) + 4 * D;  // [4][D]
+            // [4][D] each, in the dP array (staged as an operand by now)
+            float *part_sum = &sm.dP[0][0], *part_kbk = &sm.dP[0][0] + 4 * D;
             part_sum[slice * D + c] = dgam[0];
             part_kbk[slice * D + c] = kbk;
             __syncthreads();
@@ -824,9 +850,34 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 later += part_kbk[s2 * D + c];
                 if (s2 > slice) later += part_sum[s2 * D + c];
             }
+            if (vstore) {
+                float *sg = reinterpret_cast<float *>(base + O_SG);   // [C][D]
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (x0 + u < L) dg[(t0 + x0 + u) * rowK + (int64_t)h * D + c] = dgam[u] + later;
+                for (int u = 0; u < 8; ++u) sg[(x0 + u) * D + c] = dgam[u] + later;
+                __syncthreads();
+                // dq, dk: 512 chunks of 8 bf16 each; dg: 1024 chunks of 4 fp32
+                {
+                    const int r = t >> 4, c8 = (t & 15) * 8;
+                    if (r < L) {
+                        const int64_t off = (t0 + r) * rowK + (int64_t)h * D + c8;
+                        *reinterpret_cast<uint4 *>(dq + off) =
+                            *reinterpret_cast<const uint4 *>(base + O_SQ + (r * D + c8) * 2);
+                        *reinterpret_cast<uint4 *>(dk + off) =
+                            *reinterpret_cast<const uint4 *>(base + O_SK + (r * D + c8) * 2);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int q = t + kThreads * i, r = q >> 5, c4 = (q & 31) * 4;
+                    if (r < L)
+                        *reinterpret_cast<float4 *>(dg + (t0 + r) * rowK + (int64_t)h * D + c4) =
+                            *reinterpret_cast<const float4 *>(sg + r * D + c4);
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (x0 + u < L) dg[(t0 + x0 + u) * rowK + (int64_t)h * D + c] = dgam[u] + later;
+            }
         }
         if (t < C && t < L) dbeta[(t0 + t) * H + h] = sm.dbeta[t];
         tc_fence_before();
@@ -851,8 +902,8 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     if (t == 0) {
         mbar_wait_bounded(&sm.mma_bar, mma_par, kPollLimit);
         if (tiles_pending) mbar_wait_bounded(&sm.tma_bar, pend_par, kPollLimit);
-        if (s0_pending) mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit);
     }
+    if (t == kS0Issuer && s0_pending) mbar_wait_bounded(&sm.s0_bar, s0_par, kPollLimit);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -883,6 +934,8 @@ cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const v
         !kda_make_tile_map(&mg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P.T, P.H))
         return cudaErrorInvalidValue;
     CUtensorMap mcs = {}, minit = {};
+    auto al16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+    const int vec_out = P.out_dtype == KDA_DTYPE_BF16 && al16(dq) && al16(dk) && al16(dv) && al16(dg);
     const int has_cs = chunk_states && chunk_capacity > 0;
     const int has_init = init_state != nullptr;
     if (has_cs && !kda_make_state_map(&mcs, chunk_states, chunk_capacity * P.H * (int64_t)D))
@@ -896,8 +949,8 @@ cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const v
         static cudaError_t attr = cudaSuccess;
         std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem); });
         if (attr != cudaSuccess) return attr;
-        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, beta,
-                                                  init_state, cu, chunk_states, chunk_capacity, d_final,
+        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, vec_out,
+                                                  beta, init_state, cu, chunk_states, chunk_capacity, d_final,
                                                   (__nv_bfloat16 *)dq, (__nv_bfloat16 *)dk,
                                                   (__nv_bfloat16 *)dv, dg, dbeta, d_init, P.H,
                                                   (int64_t)P.T, P.seq_len);
@@ -907,8 +960,8 @@ cudaError_t kda_launch_backward_tc(const kda::Problem &P, const void *q, const v
         static cudaError_t attr = cudaSuccess;
         std::call_once(once, [&] { attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem); });
         if (attr != cudaSuccess) return attr;
-        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, beta,
-                                                  init_state, cu, chunk_states, chunk_capacity, d_final,
+        kern<<<blocks, kThreads, kSmem, stream>>>(mq, mk, mv, mdo, mg, mcs, minit, has_cs, has_init, 0,
+                                                  beta, init_state, cu, chunk_states, chunk_capacity, d_final,
                                                   (float *)dq, (float *)dk, (float *)dv, dg, dbeta, d_init,
                                                   P.H, (int64_t)P.T, P.seq_len);
     }
