@@ -146,3 +146,42 @@ def test_missing_chunk_states_are_reported():
     kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out,
                      cu_seqlens=cu, chunk_states=cs)
     assert kda.kda_get_last_device_error() == 0
+
+
+def test_backward_bf16_unaligned_gradients_match_aligned():
+    """The tensor-core backward writes bf16 gradient rows through shared memory as
+    16-byte stores when the gradient arrays are 16-byte aligned, and element by
+    element otherwise: both give the same bits (a ragged packed batch, so that the
+    last chunk of a sequence is partial)."""
+    import ctypes
+    H, d = 2, 128
+    lens = [70, 33, 96]
+    T = sum(lens)
+    inp = synth.random_inputs(T, H, d, dtype=torch.bfloat16, seed=121, device=DEV, num_seqs=len(lens),
+                              init_std=0.05)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=DEV)
+    d_out, d_fin = _upstream(T, H, len(lens), d, torch.bfloat16, 122)
+    ref = kda.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], d_out, d_fin,
+                           init_state=inp["init_state"], cu_seqlens=cu)
+    _, _, cst = kda.kda_prefill_checkpointed(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                             inp["init_state"], cu, interval=kda.CHUNK)
+    n = T * H * d
+    # each gradient 2 elements (4 or 8 bytes) past a 16-byte boundary
+    bufs = {name: torch.zeros(n + 8, dtype=dt, device=DEV)
+            for name, dt in (("dq", torch.bfloat16), ("dk", torch.bfloat16), ("dv", torch.bfloat16),
+                             ("dg", torch.float32))}
+    views = {name: b[2:2 + n].view(T, H, d) for name, b in bufs.items()}
+    dbeta = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    dinit = torch.empty((len(lens), H, d, d), dtype=torch.float32, device=DEV)
+    dims = kda.Dims(len(lens), T, H, d, d, kda._DTYPES[torch.bfloat16], kda._DTYPES[torch.bfloat16], 0)
+    p = lambda x: ctypes.c_void_p(x.data_ptr()) if x is not None else None
+    st = kda.lib().kda_backward(ctypes.byref(dims), p(inp["q"]), p(inp["k"]), p(inp["v"]), p(inp["g"]),
+                                p(inp["beta"]), p(inp["init_state"]), p(cu), p(cst), int(cst.shape[0]),
+                                p(d_out), p(d_fin), p(views["dq"]), p(views["dk"]), p(views["dv"]),
+                                p(views["dg"]), p(dbeta), p(dinit), None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_device_error() == 0
+    for name in ("dq", "dk", "dv", "dg"):
+        assert torch.equal(views[name], ref[name]), name
+    assert torch.equal(dbeta, ref["dbeta"]) and torch.equal(dinit, ref["d_init_state"])
