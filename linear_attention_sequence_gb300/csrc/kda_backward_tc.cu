@@ -454,26 +454,22 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 atomicOr(&g_kda_bwdtc_status, 0x800u);
             }
             const int half = (warp - 4) >> 2;
-            float p[64];
-#pragma unroll
+            // one 32-column block per iteration (the loop is kept rolled: code size)
+#pragma unroll 1
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int c0 = 64 * half + 32 * h2;
-                float x[32], d[32];
+                float x[32], y[32], d[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     x[i] = *reinterpret_cast<const float *>(base + STG + sw_off(128, c0 + i, jl));
-                    p[32 * h2 + i] = x[i];
+                    y[i] = x[i];
                     x[i] *= sm.e15[c0 + i];
                 }
                 tmem_st32(tl + TM_DN + c0, x);
                 tmem_ld32(tl + TM_DS + c0, d);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) p[32 * h2 + i] *= d[i];
-            }
-            tmem_wait_st();
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                float *y = p + 32 * h2;
+                for (int i = 0; i < 32; ++i) y[i] *= d[i];
+                // sum over this warp's 32 lanes j: reduce-scatter, lane i ends with column c0 + i
 #pragma unroll
                 for (int sh = 16; sh >= 1; sh >>= 1) {
                     const bool up = (lane & sh) != 0;
@@ -484,8 +480,9 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                         y[i] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
                     }
                 }
-                sm.red2[q4][64 * half + 32 * h2 + lane] = y[0];
+                sm.red2[q4][c0 + lane] = y[0];
             }
+            tmem_wait_st();
         } else if (warp == 12) {   // blocked solve (scratch in the small arrays)
             named_sync(4, 160);
             float d[32];
