@@ -494,7 +494,8 @@ __device__ __forceinline__ void st_stage(unsigned char *tile, int r, int c, floa
 // S^T <- S^T Diag(e^{Gamma_last}) on the 32 lanes of the calling warp (`tl` =
 // TMEM base + the warp's lane offset).
 __device__ __forceinline__ void scale_state(TcSmem &sm, uint32_t tl, int st) {
-#pragma unroll
+    // rolled (each load waits for its data anyway): less code for the instruction caches
+#pragma unroll 1
     for (int c0 = 0; c0 < D; c0 += 32) {
         float s0[16], s1[16];
         tmem_ld16x2(tl + TM_S + c0, tl + TM_S + c0 + 16, s0, s1);
