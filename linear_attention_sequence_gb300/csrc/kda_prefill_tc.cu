@@ -405,7 +405,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         if (warp < 2) {
             tc_fence_after();   // after the Gram MMA of chunk n-1 (awaited above)
             const int r = lane, row = 32 * warp + r;     // warp 0: k~ rows, warp 1: q~ rows
-#pragma unroll
+#pragma unroll 2
             for (int c0 = 0; c0 < D; c0 += 16) {
                 const float *blk = sm.gramA + (c0 >> 5) * 64 * 32;
                 float vals[16];
