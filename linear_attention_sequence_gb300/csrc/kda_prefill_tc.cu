@@ -449,7 +449,7 @@ __device__ __forceinline__ void prep_loop(TcSmem &sm, const CUtensorMap *mq, con
         if (P == kGramIssuer) {
             tc_fence_after();
             const uint64_t dB = sdesc_sw128(smem_u32(sm.gramB));
-#pragma unroll
+#pragma unroll 8
             for (int kk = 0; kk < 16; ++kk)
                 mma_tf32_ts(tb + TM_G + 32 * st, tb + TM_GA + kk * 8,
                             dB + (uint64_t)(((kk >> 2) * (32 * 128) + (kk & 3) * 32) >> 4),
@@ -548,7 +548,9 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
                 if (wait_phase(sm, &sm.bar_bxfull[st], bxf_par[st], 64u)) {
                     tc_fence_after();
                     const uint64_t dX = sdesc_sw128(smem_u32(&sm.in[st]));   // the chunk's stage
-#pragma unroll
+                    // partly unrolled: the loop's code stays small for the
+                    // instruction caches while the issues still run back to back
+#pragma unroll 4
                     for (int kk = 0; kk < 16; ++kk)
                         mma_tf32_ts(tb + TM_X, tb + TM_S + kk * 8,
                                     dX + (uint64_t)(((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4),
