@@ -756,10 +756,11 @@ __device__ __forceinline__ void chain_loop(TcSmem &sm, const CUtensorMap *mq, co
             const int64_t ck = ck_row0 + (n + 1) / ckpt_every - 1;
             if (ck < ckpt_cap) {
                 float *dstS = ckpt + (ck * H + h) * (int64_t)D * D + j;
+#pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float sv[16];
                     tmem_ld16(tb + lane_off + TM_S + c0, sv);
-#pragma unroll
+#pragma unroll 4
                     for (int i = 0; i < 16; ++i) dstS[(int64_t)(c0 + i) * D] = sv[i];
                 }
                 tc_fence_before();
