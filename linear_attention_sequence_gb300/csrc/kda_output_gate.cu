@@ -23,6 +23,12 @@
 
 namespace {
 
+// The kernels are launched as programmatic dependents of the previous kernel in
+// the stream (normally the prefill that wrote `out`): their blocks may be
+// scheduled while that kernel drains, and wait here until it has completed and
+// its writes are visible.  Launched without that attribute, this is a no-op.
+__device__ __forceinline__ void wait_for_producer() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr int kRowsPerBlock = 8;   // scalar kernel: one row per warp
 constexpr int kWarpsPerBlock = 8;  // vector kernel
 constexpr int kRowsPerWarp = 8;
@@ -31,6 +37,7 @@ template <typename G_T, typename OUT_T>
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
 kda_output_gate_kernel(OUT_T *__restrict__ out, const G_T *__restrict__ gate,
                        const float *__restrict__ w, float eps, int64_t rows, int dv) {
+    wait_for_producer();
     const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;   // whole warps only: the row index is warp-uniform
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 kda_output_gate_vec_kernel(OUT_T *__restrict__ out, const G_T *__restrict__ gate,
                            const float *__restrict__ w, float eps, int64_t rows) {
     constexpr int DV = 16 * EPL, NP = kRowsPerWarp / 2;
+    wait_for_producer();
     const int lane = threadIdx.x & 31, hl = lane & 15, hr = lane >> 4;
     const int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * kRowsPerWarp;
     Raw<OUT_T, EPL> ro[NP];
@@ -165,18 +173,24 @@ cudaError_t launch_gate(OUT_T *out, const G_T *gate, const float *w, float eps, 
     };
     const bool vec = (dv == 64 || dv == 128) && aligned(out, sizeof(OUT_T)) && aligned(gate, sizeof(G_T)) &&
                      (w == nullptr || ((uintptr_t)w % 4) == 0);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     if (vec) {
         const int64_t per_block = (int64_t)kWarpsPerBlock * kRowsPerWarp;
-        const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
+        cfg.gridDim = dim3((unsigned)((rows + per_block - 1) / per_block));
+        cfg.blockDim = dim3(32 * kWarpsPerBlock);
         if (dv == 128)
-            kda_output_gate_vec_kernel<G_T, OUT_T, 8><<<blocks, 32 * kWarpsPerBlock, 0, stream>>>(out, gate, w, eps, rows);
-        else
-            kda_output_gate_vec_kernel<G_T, OUT_T, 4><<<blocks, 32 * kWarpsPerBlock, 0, stream>>>(out, gate, w, eps, rows);
-    } else {
-        const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
-        kda_output_gate_kernel<<<blocks, 32 * kRowsPerBlock, 0, stream>>>(out, gate, w, eps, rows, dv);
+            return cudaLaunchKernelEx(&cfg, kda_output_gate_vec_kernel<G_T, OUT_T, 8>, out, gate, w, eps, rows);
+        return cudaLaunchKernelEx(&cfg, kda_output_gate_vec_kernel<G_T, OUT_T, 4>, out, gate, w, eps, rows);
     }
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock));
+    cfg.blockDim = dim3(32 * kRowsPerBlock);
+    return cudaLaunchKernelEx(&cfg, kda_output_gate_kernel<G_T, OUT_T>, out, gate, w, eps, rows, dv);
 }
 
 }  // namespace
