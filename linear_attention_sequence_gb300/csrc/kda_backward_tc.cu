@@ -677,14 +677,15 @@ kda_backward_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (warp < 8) {
             const int hh = warp >> 2;
 #pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
-                const int c0 = 64 * hh + 32 * q;
-                float x[32], y[32];
-                tmem_ld32(tl + TM_DS + c0, x);
-                tmem_ld32(tl + TM_INC + c0, y);
+            for (int q = 0; q < 8; ++q) {   // 8-column blocks, rolled (code size)
+                const int c0 = 64 * hh + 8 * q;
+                float x[8], y[8];
+                tmem_ld8(tl + TM_DS + c0, x);
+                tmem_ld8(tl + TM_INC + c0, y);
+                uint32_t z[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = sm.gC[c0 + i] * x[i] + sm.e15[c0 + i] * y[i];
-                tmem_st32(tl + TM_DS + c0, x);
+                for (int i = 0; i < 8; ++i) z[i] = __float_as_uint(sm.gC[c0 + i] * x[i] + sm.e15[c0 + i] * y[i]);
+                tmem_st8(tl + TM_DS + c0, z);
             }
             float y[16];
             tmem_ld16(tl + TM_DOT + 32 + 16 * hh, y);
