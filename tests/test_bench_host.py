@@ -81,3 +81,23 @@ def test_committed_traffic_lines_are_looked_up():
         assert re.fullmatch(r"[0-9a-f]{12}", digest)
         assert float(nbytes) > 0
         assert os.path.exists(os.path.join(ROOT, known[(kernel, workload)]))
+
+
+def test_clock_summary_inside_nearest_and_reasons():
+    """Clock samples inside the timed region are summarised (median SM clock,
+    max clock, active throttle reasons); a region shorter than the sampling
+    period falls back to the nearest sample and says so."""
+    s = bench.ClockSampler(0)
+
+    def row(mhz, *active):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        return ["0", str(mhz), "2070", "900.0", "0x0"] + ["Active" if n in active else "Not Active" for n in names]
+    s.samples = [(10.00, row(2070)), (10.02, row(1950, "sw_power_cap")), (10.04, row(2070)),
+                 (10.50, row(1500, "hw_slowdown"))]
+    out = s.summary(9.99, 10.05)
+    assert out["samples"] == 3 and out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"] and "note" not in out
+    near = s.summary(10.45, 10.46)
+    assert near["samples"] == 1 and near["sm_mhz"] == 1500.0 and near["reasons"] == ["hw_slowdown"]
+    assert "nearest" in near["note"]
+    assert bench.ClockSampler(0).summary(0, 1)["reasons"] == ["unavailable"]
