@@ -25,14 +25,20 @@
 //
 // One CTA of 512 threads per (sequence, head).  The adjoint stays in tensor
 // memory as dS^T (lane = value j, column = key channel c).  Every product with
-// a 128-long side is one tcgen05.mma kind::tf32 group with M = 128 (values or
+// a 128-long side is a tcgen05.mma kind::tf32 group with M = 128 (values or
 // key channels) and fp32 accumulation; its operands are written by the threads
 // as K-major SW128 tf32 blocks in shared memory, or read from tensor memory.
 // The pairs [G ; P] and dP, dT are M = 64 products whose 32-row operands are
 // read with 32 further rows of shared memory past them (the rows of the result
 // that those give are not read).  The solve, dA = -T^T dT T^T and the pairwise
 // 32 x 32 terms run on the CUDA cores.  The phases of a chunk run one after
-// another, separated by block barriers.
+// another, separated by block barriers; within a phase the MMA groups for
+// different accumulators are issued by elected lanes of up to three warps (the
+// Gram and X also as two K halves summed when read), the solve runs on its own
+// warp beside the state copy and X, and the next chunk's tiles and state are
+// fetched by TMA during the last phases of the current one.  The kernel's code
+// size matters: instruction fetch is a visible share of its stalls, so loops
+// off the critical path are kept rolled.
 
 #include <mutex>
 
