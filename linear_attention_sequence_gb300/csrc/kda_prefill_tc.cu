@@ -35,7 +35,10 @@
 // else to do at that point.  A tcgen05.mma costs a roughly fixed time per
 // instruction on these shapes, so the formulation minimises the instruction
 // count: 16 for the Gram and 16 for the readout (K = d_k = 128), 4 each for
-// U', U and the readout + state-carry group.
+// U', U and the readout + state-carry group.  The loop bodies are long, and
+// instruction fetch is a visible share of the stalls: a few loops are kept
+// rolled or only partly unrolled where that costs no latency on the chunk's
+// path (the state decay, the Gram A copy, the MMA issue loops).
 // tf32 (not bf16) operands: on these inputs the intermediate u_t and the
 // intra-chunk terms are several times larger than o_t, and bf16 operand
 // rounding alone costs more than the 2e-2 error budget; tf32 keeps it near
